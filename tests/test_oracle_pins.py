@@ -1,0 +1,421 @@
+"""Pins of the CPU oracle against things other than itself: format tables from
+their definitions, a library conversion (torch float8_e4m3fn), hand-worked
+blocks, published Philox known-answer values, Hadamard algebra checked
+against scipy, SR unbiasedness, brute force on tiny inputs, and invariants.
+No GPU is needed."""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.linalg
+import torch
+
+from nvfp4_precision_02_b300 import workloads as wl
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------ format tables
+def test_e2m1_table_from_bit_fields(orc):
+    # OCP MX E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa bit; exponent 0 is
+    # subnormal with value m * 2^-1.
+    for code in range(16):
+        s, e, m = code >> 3, (code >> 1) & 3, code & 1
+        mag = Fraction(m, 2) if e == 0 else Fraction(2) ** (e - 1) * (1 + Fraction(m, 2))
+        want = -float(mag) if s else float(mag)
+        got = orc.e2m1_value(code)
+        assert got == want and math.copysign(1, got) == math.copysign(1, want), code
+
+
+def test_e4m3_decode_matches_torch_float8(orc):
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([orc.e4m3_value(b) for b in range(256)])
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all()
+    assert nan.sum() == 2                      # 0x7F and 0xFF only
+    assert (got[~nan] == ref[~nan]).all()
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_in_range(orc):
+    # every representable value, every midpoint between neighbours, and a
+    # dense random sweep: torch's float8 cast rounds to nearest-even.
+    vals = sorted({orc.e4m3_value(b) for b in range(0x7F)})
+    mids = [(a + b) / 2 for a, b in zip(vals, vals[1:])]
+    rng = np.random.default_rng(0)
+    sweep = list(np.exp(rng.uniform(np.log(1e-4), np.log(448.0), 20000)).astype(np.float32))
+    xs = np.array(vals + mids + sweep + [0.0, 1e-30, 2.0 ** -10, 3 * 2.0 ** -11], dtype=np.float32)
+    want = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.e4m3_encode(float(x)) for x in xs], dtype=np.uint8)
+    assert (got == want).all(), np.nonzero(got != want)
+
+
+def test_e4m3_encode_saturates(orc):
+    # satfinite reading: anything at or above 448 encodes as 448 (0x7E)
+    for x in [448.0, 449.0, 464.0, 470.0, 1e6, 3.4e38]:
+        assert orc.e4m3_encode(x) == 0x7E
+
+
+def test_e2m1_rne_grid_and_ties(orc):
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for i, g in enumerate(grid):
+        assert orc.e2m1_rne(g) == i
+        assert orc.e2m1_rne(-g) == 8 | i
+    for v, code in [(0.25, 0), (0.75, 2), (1.25, 2), (1.75, 4), (2.5, 4), (3.5, 6), (5.0, 6),
+                    (0.2499, 0), (0.2501, 1), (5.001, 7), (6.5, 7), (1e9, 7), (-0.1, 8)]:
+        assert orc.e2m1_rne(v) == code, v
+
+
+def test_e2m1_rne_is_nearest_bruteforce(orc):
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    rng = np.random.default_rng(1)
+    for v in rng.uniform(-7, 7, 3000).astype(np.float32):
+        c = orc.e2m1_rne(float(v))
+        d = np.abs(abs(float(v)) - grid)
+        mag = grid[c & 7]
+        if abs(v) <= 6:
+            assert abs(abs(v) - mag) == d.min()
+        else:
+            assert mag == 6
+        assert (c >> 3) == (1 if v < 0 or (v == 0 and math.copysign(1, v) < 0) else 0)
+
+
+# ------------------------------------------------------------ scales
+def test_tensor_scale_special_cases(orc):
+    assert orc.tensor_scale(2688.0) == 1.0
+    assert orc.tensor_scale(0.0) == 1.0                     # empty / all-zero tensor
+    assert orc.tensor_scale(1.0) == 2688.0
+    assert orc.tensor_scale(1e-38) == np.finfo(np.float32).max   # quotient overflows: clamp
+    assert orc.decode_scale(2688.0) == 1.0
+
+
+def test_block_scale_max_maps_to_448(orc):
+    # the block holding the tensor amax gets scale 448 (largest E4M3) for any amax
+    rng = np.random.default_rng(2)
+    for amax in rng.uniform(1e-3, 1e3, 200).astype(np.float32):
+        s = orc.block_scale(float(amax), orc.tensor_scale(float(amax)))
+        assert s == 0x7E
+
+
+# ------------------------------------------------------------ hand-worked blocks
+@pytest.mark.parametrize("blk", _load("blocks.json")["blocks"], ids=lambda b: b["name"])
+def test_hand_worked_blocks(orc, blk):
+    sf, codes = orc.encode_block(np.array(blk["x"], dtype=np.float32), orc.tensor_scale(blk["amax"]))
+    assert sf == blk["sf"]
+    assert codes == blk["codes"]
+
+
+# ------------------------------------------------------------ Philox / SR
+def test_philox_known_answers(orc):
+    kat = _load("philox4x32_kat.json")
+    for v in kat["vectors"]:
+        ctr = [int(x, 16) for x in v["ctr"]]
+        key = [int(x, 16) for x in v["key"]]
+        assert orc.philox4x32(ctr, key, kat["rounds"]) == [int(x, 16) for x in v["out"]]
+
+
+def test_sr_word_counter_layout(orc):
+    # element e uses word e & 3 of Philox5(ctr = (e >> 2) split lo/hi, key = seed lo/hi)
+    seed = 0x0123456789ABCDEF
+    for e in [0, 1, 2, 3, 4, 7, 1 << 33 | 5]:
+        q = e >> 2
+        out = orc.philox4x32([q & 0xFFFFFFFF, q >> 32, 0, 0], [seed & 0xFFFFFFFF, seed >> 32], 5)
+        assert orc.sr_word(seed, e) == out[e & 3]
+
+
+@pytest.mark.parametrize("case", _load("sr_cases.json")["cases"], ids=lambda c: f'{c["v"]}-{c["u"]}')
+def test_sr_hand_cases(orc, case):
+    assert orc.e2m1_sr(case["v"], case["u"]) == case["code"]
+
+
+def test_sr_unbiased_rne_biased(orc):
+    """Over many random words SR's mean equals the input (CLT 4-sigma bound);
+    RTNE's error is systematic (Nemotron 3 Super summary, section 4.3)."""
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    n = 20000
+    words = [orc.sr_word(99, e) for e in range(n)]
+    for v in [0.1, 0.3, 0.625, 1.2, 2.7, 3.3, 4.9, 5.5]:
+        vals = np.array([grid[orc.e2m1_sr(v, u) & 7] for u in words])
+        lo = grid[grid <= v].max()
+        hi = grid[grid > v].min()
+        sigma = (hi - lo) * 0.5 / math.sqrt(n)
+        assert abs(vals.mean() - v) < 4 * sigma, v
+        assert set(np.unique(vals)) <= {lo, hi}
+        rne = grid[orc.e2m1_rne(v) & 7]
+        assert rne != v                 # RTNE is deterministic: error never averages out
+
+
+# ------------------------------------------------------------ layout
+def test_sf_layout_hand_offsets(orc):
+    cols = 128    # 8 scale columns -> 2 column atoms
+    assert orc.sf_offset(0, 0, cols) == 0
+    assert orc.sf_offset(1, 0, cols) == 16
+    assert orc.sf_offset(32, 0, cols) == 4
+    assert orc.sf_offset(33, 3, cols) == 16 + 4 + 3
+    assert orc.sf_offset(0, 4, cols) == 512
+    assert orc.sf_offset(128, 0, cols) == 1024
+    assert orc.sf_bytes(129, 128) == 256 * 8
+    assert orc.sf_bytes(1, 16) == 128 * 4
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (130, 48), (256, 256), (300, 1040)])
+def test_sf_layout_is_a_bijection(orc, rows, cols):
+    R = -(-rows // 128) * 128
+    C = -(-(cols // 16) // 4) * 4
+    offs = {orc.sf_offset(r, c, cols) for r in range(R) for c in range(C)}
+    assert offs == set(range(orc.sf_bytes(rows, cols)))
+
+
+# ------------------------------------------------------------ Hadamard
+def test_rht_matrix_is_scaled_sylvester_hadamard(orc):
+    H = scipy.linalg.hadamard(16).astype(np.float64)
+    for mask in [0, 0xFFFF, 0xA5C3, 1]:
+        s = np.array([-1.0 if (mask >> j) & 1 else 1.0 for j in range(16)])
+        Q = np.stack([orc.rht16(np.eye(16)[j], mask) for j in range(16)], axis=1).astype(np.float64)
+        assert (Q == 0.25 * H * s[None, :]).all()
+        assert (Q @ Q.T == np.eye(16)).all()       # orthogonal for every sign pattern
+    assert (H @ H.T == 16 * np.eye(16)).all()
+
+
+def test_rht_preserves_dot_products_and_concentrates_constants(orc):
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        a = rng.standard_normal(16).astype(np.float32)
+        b = rng.standard_normal(16).astype(np.float32)
+        mask = int(rng.integers(0, 1 << 16))
+        qa = orc.rht16(a, mask).astype(np.float64)
+        qb = orc.rht16(b, mask).astype(np.float64)
+        assert abs(qa @ qb - a.astype(np.float64) @ b) < 1e-5 * (np.abs(a) @ np.abs(b) + 1)
+    y = orc.rht16(np.full(16, 3.0), 0)
+    assert y[0] == 12.0 and (y[1:] == 0).all()
+
+
+# ------------------------------------------------------------ whole tensors
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _unpack(codes, cols):
+    lo = codes & 15
+    hi = codes >> 4
+    return np.stack([lo, hi], axis=-1).reshape(codes.shape[0], cols)
+
+
+def test_quantize_1d_bruteforce(orc):
+    """Tiny tensor: every block's scale and every code recomputed in numpy
+    FP32 by brute force over the grids, read back through the layout."""
+    rng = np.random.default_rng(4)
+    rows, cols = 37, 64
+    x = _bf16(rng.standard_normal((rows, cols)) * np.exp(rng.uniform(-6, 3, (rows, 1))))
+    q = orc.quantize_1d(x)
+    xf = x.float().numpy()
+    amax = np.float32(np.abs(xf).max())
+    assert q["amax"] == amax
+    s_enc = np.float32(2688.0) / amax
+    e4 = torch.arange(127, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], dtype=np.float64)
+    codes = _unpack(q["codes"], cols)
+    for r in range(rows):
+        for b in range(cols // 16):
+            blk = xf[r, b * 16:(b + 1) * 16]
+            sf_f = np.float32(np.float32(np.abs(blk).max()) / np.float32(6.0)) * s_enc
+            want_sf = torch.tensor([sf_f]).to(torch.float8_e4m3fn).view(torch.uint8).item()
+            sf = q["sf"][orc.sf_offset(r, b, cols)]
+            assert sf == want_sf
+            cb = codes[r, b * 16:(b + 1) * 16]
+            if sf == 0:
+                assert (cb == 0).all()
+                continue
+            rr = np.float32(s_enc / np.float32(e4[sf]))
+            v = (blk * rr).astype(np.float32)
+            for j in range(16):
+                d = np.abs(abs(float(v[j])) - grid)
+                mag = grid[cb[j] & 7]
+                assert abs(abs(float(v[j])) - mag) == d.min() or (abs(v[j]) > 6 and mag == 6)
+                assert (cb[j] >> 3) == (1 if np.signbit(v[j]) else 0)
+
+
+def test_quantize_1d_sr_matches_per_element_rule(orc):
+    rng = np.random.default_rng(5)
+    rows, cols, seed = 9, 48, 1234
+    x = _bf16(rng.standard_normal((rows, cols)))
+    q = orc.quantize_1d(x, mode=orc.SR, seed=seed)
+    qr = orc.quantize_1d(x)
+    assert (q["sf"] == qr["sf"]).all()               # scales are always RNE
+    codes = _unpack(q["codes"], cols)
+    s_enc = orc.tensor_scale(q["amax"])
+    xf = x.float().numpy()
+    for r in range(rows):
+        for c in range(cols):
+            sf = q["sf"][orc.sf_offset(r, c // 16, cols)]
+            rr = np.float32(np.float32(s_enc) / np.float32(orc.e4m3_value(sf)))
+            v = float(np.float32(xf[r, c]) * rr)
+            assert codes[r, c] == orc.e2m1_sr(v, orc.sr_word(seed, r * cols + c))
+
+
+def test_quantize_1d_supplied_amax(orc):
+    rng = np.random.default_rng(6)
+    x = _bf16(rng.standard_normal((16, 32)))
+    q1 = orc.quantize_1d(x)
+    q2 = orc.quantize_1d(x, amax_in=q1["amax"])
+    assert (q1["codes"] == q2["codes"]).all() and (q1["sf"] == q2["sf"]).all()
+    q3 = orc.quantize_1d(x, amax_in=4 * q1["amax"])
+    assert q3["amax"] == 4 * q1["amax"]
+
+
+def test_quantize_2d_transpose_invariant(orc):
+    """W and W^T quantise identically (2D blocks; Nemotron 3 Ultra report, 2.2)."""
+    rng = np.random.default_rng(7)
+    w = _bf16(rng.standard_normal((48, 80)) * 0.02)
+    a = orc.quantize_2d(w)
+    b = orc.quantize_2d(w.t().contiguous())
+    assert (a["codes_t"] == b["codes"]).all() and (a["codes"] == b["codes_t"]).all()
+    assert (a["sf_t"] == b["sf"]).all() and (a["sf"] == b["sf_t"]).all()
+    assert (a["tile_sf"][0] == b["tile_sf"][0].T).all()
+    assert a["amax"][0] == b["amax"][0]
+
+
+def test_quantize_2d_tile_scale_is_tile_amax(orc):
+    rng = np.random.default_rng(8)
+    w = _bf16(rng.standard_normal((32, 64)) * np.exp(rng.uniform(-4, 2, (32, 64))))
+    q = orc.quantize_2d(w)
+    wf = w.float().numpy()
+    s_enc = orc.tensor_scale(q["amax"][0])
+    for ti in range(2):
+        for tj in range(4):
+            t = wf[ti * 16:(ti + 1) * 16, tj * 16:(tj + 1) * 16]
+            s = orc.block_scale(float(np.abs(t).max()), s_enc)
+            assert q["tile_sf"][0, ti, tj] == s
+            for i in range(16):
+                assert q["sf"][orc.sf_offset(ti * 16 + i, tj, 64)] == s
+                assert q["sf_t"][orc.sf_offset(tj * 16 + i, ti, 32)] == s
+
+
+def test_quantize_2d_batched_equals_per_batch(orc):
+    rng = np.random.default_rng(9)
+    w = _bf16(rng.standard_normal((3, 32, 48)))
+    qb = orc.quantize_2d(w)
+    n = orc.sf_bytes(32, 48)
+    for b in range(3):
+        q = orc.quantize_2d(w[b])
+        assert (qb["codes"][b] == q["codes"][0]).all()
+        assert (qb["sf"][b * n:(b + 1) * n] == q["sf"]).all()
+        assert qb["amax"][b] == q["amax"][0]
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rht_quantize_equals_quantize_of_exact_transform(orc, mode):
+    """Integer inputs make the FP32 butterfly exact, so the RHT output equals
+    0.25*H*D*x from scipy's Hadamard in FP64, and it is bf16-representable:
+    quantising it with the 1D quantiser along tokens must give the same bytes
+    (same transpose, chunking, sign bit order, and SR index space)."""
+    rng = np.random.default_rng(10 + mode)
+    T, C, mask, seed = 64, 24, 0xB3E1, 77
+    x = _bf16(rng.integers(-8, 9, (T, C)))
+    H = scipy.linalg.hadamard(16).astype(np.float64)
+    s = np.array([-1.0 if (mask >> j) & 1 else 1.0 for j in range(16)])
+    xf = x.double().numpy()
+    y = np.zeros((C, T))
+    for t0 in range(0, T, 16):
+        y[:, t0:t0 + 16] = (0.25 * H @ (s[:, None] * xf[t0:t0 + 16, :])).T
+    yb = _bf16(y)
+    assert (yb.double().numpy() == y).all()
+    q = orc.rht_quantize(x, mask, mode=mode, seed=seed)
+    ref = orc.quantize_1d(yb, mode=mode, seed=seed)
+    assert q["amax"] == ref["amax"] == np.abs(y).max()
+    assert orc.rht_amax(x, mask) == q["amax"]
+    assert (q["codes"] == ref["codes"]).all() and (q["sf"] == ref["sf"]).all()
+
+
+def test_grouped_quantize_equals_per_group(orc):
+    rng = np.random.default_rng(12)
+    cols = 32
+    offsets = np.array([0, 5, 5, 140, 141, 300], dtype=np.int64)     # one empty group
+    x = _bf16(rng.standard_normal((300, cols)) * np.repeat([1, 1, 3, 0.01, 7], np.diff(offsets))[:, None])
+    q = orc.quantize_1d_grouped(x, offsets)
+    codes = q["codes"]
+    for g in range(len(offsets) - 1):
+        o, n = offsets[g], offsets[g + 1] - offsets[g]
+        po = orc.group_sf_row(offsets, g)
+        assert po % 128 == 0
+        if n == 0:
+            assert q["amax"][g] == 0
+            continue
+        ref = orc.quantize_1d(x[o:o + n])
+        assert q["amax"][g] == ref["amax"]
+        assert (codes[o:o + n] == ref["codes"]).all()
+        for r in range(n):
+            for b in range(cols // 16):
+                assert q["sf"][orc.sf_offset(po + r, b, cols)] == ref["sf"][orc.sf_offset(r, b, cols)]
+    # SR: one group covering everything is the plain 1D quantiser
+    one = orc.quantize_1d_grouped(x, np.array([0, 300]), mode=orc.SR, seed=5)
+    ref = orc.quantize_1d(x, mode=orc.SR, seed=5)
+    assert (one["codes"] == ref["codes"]).all()
+
+
+# ------------------------------------------------------------ GEMM definition
+def test_gemm_matches_numpy_float64(orc):
+    rng = np.random.default_rng(13)
+    A = rng.standard_normal((17, 48))
+    B = rng.standard_normal((9, 48))
+    ref, absum = orc.gemm(A, B)
+    assert np.allclose(ref, A @ B.T, rtol=1e-12, atol=1e-12)
+    assert np.allclose(absum, np.abs(A) @ np.abs(B).T, rtol=1e-12)
+
+
+def test_gemm_of_dequantised_one_hot_operands_is_exact(orc):
+    """One nonzero per row whose sixth is an E4M3 value: the block scale is
+    exact, the element encodes as 6, dequantisation returns the input, and
+    every output is a single exactly representable product."""
+    K = 64
+    A = np.zeros((16, K), dtype=np.float32)
+    B = np.zeros((16, K), dtype=np.float32)
+    for i in range(16):
+        A[i, (5 * i) % K] = [6, 3, 1.5, 0.75, 9, 4.5, 7.5, -10.5][i % 8]
+        B[i, (5 * i) % K] = [12, -6, 3, 1.5, 7.5, 0.375, 24, 9][i % 8]
+    qa = orc.quantize_1d(_bf16(A), amax_in=2688.0)
+    qb = orc.quantize_1d(_bf16(B), amax_in=2688.0)
+    Ah = orc.dequantize(qa, 16, K)
+    Bh = orc.dequantize(qb, 16, K)
+    assert (Ah == A).all() and (Bh == B).all()
+    ref, _ = orc.gemm(Ah, Bh)
+    assert (ref == A.astype(np.float64) @ B.astype(np.float64).T).all()
+
+
+def test_dequantise_roundtrip_error_bound(orc):
+    """RNE: |x_hat - x| is at most half a grid gap at the block scale
+    (the gap at 6 is 2, so <= 1 * scale), plus saturation never applies to
+    the block's own amax element (it maps to <= 6)."""
+    rng = np.random.default_rng(14)
+    x = _bf16(rng.standard_normal((64, 64)))
+    q = orc.quantize_1d(x)
+    xh = orc.dequantize(q, 64, 64)
+    xf = x.double().numpy()
+    dec = orc.decode_scale(q["amax"])
+    for r in range(64):
+        for b in range(4):
+            s = orc.e4m3_value(q["sf"][orc.sf_offset(r, b, 64)]) * dec
+            err = np.abs(xh[r, b * 16:(b + 1) * 16] - xf[r, b * 16:(b + 1) * 16])
+            # 1.02: the E4M3 rounding of the scale can shrink it by up to 1/16
+            assert (err <= 1.0 * s * 1.07 + 1e-12).all()
+
+
+# ------------------------------------------------------------ routing metric
+def test_maxvio_bound():
+    """MaxVio <= N/k, equal when one expert receives every token (Ultra report 2.7)."""
+    r = wl.zipf_routing(2048, 512, 22, seed=4)
+    assert r.max_vio <= wl.max_vio_bound(512, 22) + 1e-12
+    assert int(r.offsets[-1]) == 2048 * 22
+    assert (r.counts <= 2048).all()
+    counts = torch.zeros(512, dtype=torch.int64)
+    counts[:22] = 100          # every one of 100 tokens picks the same 22 experts
+    fake = wl.Routing(torch.zeros(0), torch.zeros(0), torch.zeros(513), counts, 22)
+    assert abs(fake.max_vio - 512 / 22) < 1e-12
