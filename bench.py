@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 training linear-layer hot path on B300.
+
+One step = one pass of every hot-path step over one batch of the Ultra-shaped
+workload (default ``--workload ultra``):
+  fprop   X[16384, 8192] 1x16 RNE, W[33024, 8192] 16x16 (+W^T), Y = X.W^T
+  dgrad   dY[16384, 33024] 1x16 SR (seed 7), dX = dY.(W^T)^T
+  wgrad   16-point RHT along tokens on dY (SR) and X (RNE), dW = dY^T.X (FP32 out)
+  MoE     512 experts, top-22 Zipf(1.1) routing of 16384 tokens (360448 rows):
+          W_up[512, 5120, 2048], W_down[512, 2048, 5120] 16x16; A 1x16 per expert;
+          H = up(A), requantised per expert, O = down(H)
+Inputs are generated on the device from seeded generators and are resident
+in HBM before the timed region; every step streams tens of GB, far more than
+the 126 MB L2, so no separate L2 flush is done.
+
+Printed: one JSON line (rank 0).  ``value`` = GEMM FLOPs of the step / step
+time (quantisers included).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 GEMM TFLOPS (% dense FP4 peak); quantize GB/s (% HBM) on 1 B300"
+FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense FP4 : BF16 tensor throughput on B300
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["ultra", "super"], default="ultra")
+    p.add_argument("--e2e-steps", type=int, default=2)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            mp = json.load(f)
+        return {"hbm_gbs": mp["hbm_gbs"], "bf16_burst": mp["bf16_tflops"],
+                "bf16_sustained": mp["bf16_tflops_sustained"], "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_burst": 1800.0, "bf16_sustained": 1400.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- workload
+class Workload:
+    def __init__(self, which: str, device):
+        import torch
+        from nvfp4_precision_02_b300 import workloads as wl
+        from nvfp4_precision_02_b300 import binding as B
+        self.B = B
+        self.which = which
+        self.dense = wl.ULTRA_DENSE if which == "ultra" else wl.SUPER_DENSE
+        self.moe = wl.ULTRA_MOE if which == "ultra" else wl.SUPER_MOE
+        d, m = self.dense, self.moe
+        dev = device
+        ins = wl.dense_inputs(d, which, device=dev)
+        self.x, self.w, self.dy = ins["x"], ins["w"], ins["dy"]
+        mi = wl.moe_inputs(m, which, device=dev)
+        self.routing = mi["routing"]
+        self.a, self.w_up, self.w_down = mi["a"], mi["w_up"], mi["w_down"]
+        del mi["x_lat"]
+        self.offsets = self.routing.offsets.to(dev)
+        self.seed = wl.SEEDS["sr"]
+        self.wseed = wl.wgrad_seed(self.seed)
+        self.mask = wl.sign_mask_from_seed(wl.SEEDS["rht_sign"])
+        T, K, N = d.tokens, d.hidden, d.out
+        R, L, Hh, E = int(self.routing.offsets[-1]), m.latent, m.expert_hidden, m.experts
+        self.R = R
+        q = B.empty_qtensor
+        self.qx = q(T, K, dev)
+        self.qw = q(N, K, dev)
+        self.qwt = q(K, N, dev)
+        self.qdy = q(T, N, dev)
+        self.sdy = q(N, T, dev)
+        self.sx = q(K, T, dev)
+        self.qwu = q(Hh, L, dev, batch=E, n_amax=E)
+        self.qwd = q(L, Hh, dev, batch=E, n_amax=E)
+        self.qa = q(R, L, dev, n_amax=E, sf_size=B.sf_bytes_grouped(R, L, E))
+        self.qh = q(R, Hh, dev, n_amax=E, sf_size=B.sf_bytes_grouped(R, Hh, E))
+        self.y = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty(T, K, dtype=torch.bfloat16, device=dev)
+        self.dw = torch.empty(N, K, dtype=torch.float32, device=dev)
+        self.h = torch.empty(R, Hh, dtype=torch.bfloat16, device=dev)
+        self.o = torch.empty(R, L, dtype=torch.bfloat16, device=dev)
+        # per-op accounting: (name, kind, algorithmic work per step)
+        gem = lambda M_, N_, K_: 2.0 * M_ * N_ * K_
+        self.ops = [
+            ("quantize_1d X (amax+RNE)", "hbm", 4.5625 * T * K),
+            ("quantize_2d W (amax+W,W^T)", "hbm", 5.125 * N * K),
+            ("gemm fprop", "tensor", gem(T, N, K)),
+            ("quantize_1d dY (amax+SR)", "hbm", 4.5625 * T * N),
+            ("gemm dgrad", "tensor", gem(T, K, N)),
+            ("rht_quantize dY (amax+SR)", "hbm", 4.5625 * T * N),
+            ("rht_quantize X (amax+RNE)", "hbm", 4.5625 * T * K),
+            ("gemm wgrad", "tensor", gem(N, K, T)),
+            ("quantize_2d W_up, W_down (amax+W)", "hbm", 4.5625 * 2 * E * Hh * L),
+            ("quantize_1d_grouped A", "hbm", 4.5625 * R * L),
+            ("grouped_gemm up", "tensor", gem(R, Hh, L)),
+            ("quantize_1d_grouped H", "hbm", 4.5625 * R * Hh),
+            ("grouped_gemm down", "tensor", gem(R, L, Hh)),
+        ]
+        self.gemm_flops = sum(w_ for _, k, w_ in self.ops if k == "tensor")
+        self.input_tensors = [self.x, self.w, self.dy, self.a, self.w_up, self.w_down]
+        self.output_tensors = [self.y, self.dx, self.dw, self.o]
+
+    def step(self, marks=None):
+        """Enqueue one step; `marks(i)` is called after op i (event hooks)."""
+        B = self.B
+        mk = marks or (lambda i: None)
+        B.quantize_1d(self.x, B.RNE, 0, out=self.qx); mk(0)
+        B.quantize_2d(self.w, want_t=True, out=self.qw, out_t=self.qwt); mk(1)
+        B.gemm(self.qx, self.qw, B.OUT_BF16, out=self.y); mk(2)
+        B.quantize_1d(self.dy, B.SR, self.seed, out=self.qdy); mk(3)
+        self.qwt.amax = self.qw.amax
+        B.gemm(self.qdy, self.qwt, B.OUT_BF16, out=self.dx); mk(4)
+        B.rht_quantize(self.dy, self.mask, B.SR, self.wseed, out=self.sdy); mk(5)
+        B.rht_quantize(self.x, self.mask, B.RNE, 0, out=self.sx); mk(6)
+        B.gemm(self.sdy, self.sx, B.OUT_FP32, out=self.dw); mk(7)
+        B.quantize_2d(self.w_up, want_t=False, out=self.qwu)
+        B.quantize_2d(self.w_down, want_t=False, out=self.qwd); mk(8)
+        B.quantize_1d_grouped(self.a, self.offsets, B.RNE, 0, out=self.qa); mk(9)
+        B.grouped_gemm(self.qa, self.offsets, self.qwu, self.moe.expert_hidden, B.OUT_BF16, out=self.h); mk(10)
+        B.quantize_1d_grouped(self.h, self.offsets, B.RNE, 0, out=self.qh); mk(11)
+        B.grouped_gemm(self.qh, self.offsets, self.qwd, self.moe.latent, B.OUT_BF16, out=self.o); mk(12)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", delete=False, suffix=".csv")
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [l.strip().split(", ") for l in self.f.read().splitlines() if l.strip()]
+        os.unlink(self.f.name)
+        sm = []
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        smax = None
+        power = []
+        for r in rows:
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                smax = float(r[1])
+                power.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample(which: str, budget_s: float):
+    """Time the oracle on a bounded slice of every op of the step and
+    extrapolate by element / multiply-add counts.  Returns (seconds per full
+    step, description, threads)."""
+    import numpy as np
+    import torch
+    import oracle as orc
+    from nvfp4_precision_02_b300 import workloads as wl
+    d = wl.ULTRA_DENSE if which == "ultra" else wl.SUPER_DENSE
+    m = wl.ULTRA_MOE if which == "ultra" else wl.SUPER_MOE
+    orc.build()
+    T, K, N = d.tokens, d.hidden, d.out
+    R = m.tokens * m.topk
+    E, L, Hh = m.experts, m.latent, m.expert_hidden
+    scale = max(0.05, min(1.0, budget_s / 20.0))
+    rows = max(16, int(256 * scale)) // 16 * 16
+    g = torch.Generator().manual_seed(0)
+    xs = (torch.randn(rows, K, generator=g)).to(torch.bfloat16)
+    dys = (torch.randn(rows, N, generator=g) * 1e-3).to(torch.bfloat16)
+    per = {}
+    t0 = time.perf_counter(); qx = orc.quantize_1d(xs); per["q1d_rne"] = (time.perf_counter() - t0) / xs.numel()
+    t0 = time.perf_counter(); orc.quantize_1d(dys, orc.SR, 7); per["q1d_sr"] = (time.perf_counter() - t0) / dys.numel()
+    t0 = time.perf_counter(); orc.quantize_2d(xs[:, :K]); per["q2d"] = (time.perf_counter() - t0) / xs.numel()
+    t0 = time.perf_counter(); orc.rht_quantize(dys, 0x1234, orc.SR, 9); per["rht"] = (time.perf_counter() - t0) / dys.numel()
+    mm = max(8, int(64 * scale))
+    A = orc.dequantize(qx, rows, K)[:mm]
+    Bm = orc.dequantize(qx, rows, K)[:mm]
+    t0 = time.perf_counter(); orc.gemm(A, Bm); per["gemm_mac"] = (time.perf_counter() - t0) / (mm * mm * K)
+    elems = {"q1d_rne": T * K + R * L + R * Hh, "q1d_sr": T * N, "q2d": N * K + 2 * E * Hh * L,
+             "rht": T * N + T * K}
+    macs = T * N * K * 3 + 2 * R * Hh * L
+    sec = sum(per[k] * v for k, v in elems.items()) + per["gemm_mac"] * macs
+    desc = (f"oracle on {rows} rows of X [.,{K}] and dY [.,{N}] (1D RNE/SR, 2D, RHT) and a {mm}x{mm}x{K} "
+            f"FP64 GEMM; per-element and per-multiply-add times extrapolated to the full step")
+    return sec, desc, orc.num_threads()
+
+
+# ---------------------------------------------------------------- main
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return reference_arm(args)
+
+    import torch
+    from nvfp4_precision_02_b300 import binding as B, build as nb
+    nb.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    B.lib()
+
+    wk = Workload(args.workload, dev)
+    torch.cuda.synchronize()
+    for _ in range(max(args.warmup, 0)):
+        wk.step()
+    torch.cuda.synchronize()
+    if B.device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    nops = len(wk.ops)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)] for _ in range(args.steps)]
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", ""))
+    if uuid and not uuid.startswith("GPU-"):
+        uuid = "GPU-" + uuid
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = B.launch_count()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for s in range(args.steps):
+        ev[s][0].record()
+        wk.step(marks=lambda i, s=s: ev[s][i + 1].record())
+    end.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = B.launch_count() - launches0
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    op_ms = [statistics.median(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps))
+             for i in range(nops)]
+    status = B.device_status()
+
+    pk = peaks()
+    fp4_peak_sust = pk["bf16_sustained"] * FP4_OVER_BF16
+    fp4_peak_burst = pk["bf16_burst"] * FP4_OVER_BF16
+    value = wk.gemm_flops * world / (ms_step * 1e-3) / 1e12
+    gemm_ms = sum(t for (n, k, _), t in zip(wk.ops, op_ms) if k == "tensor")
+    quant_ms = sum(t for (n, k, _), t in zip(wk.ops, op_ms) if k == "hbm")
+    quant_bytes = sum(w for _, k, w in wk.ops if k == "hbm")
+    ops = {}
+    for (n, k, w), t in zip(wk.ops, op_ms):
+        if k == "tensor":
+            ops[n] = {"ms": round(t, 4), "tflops": round(w / (t * 1e-3) / 1e12, 1),
+                      "frac_fp4_sustained": round(w / (t * 1e-3) / 1e12 / fp4_peak_sust, 4)}
+        else:
+            ops[n] = {"ms": round(t, 4), "gbs": round(w / (t * 1e-3) / 1e9, 1),
+                      "frac_hbm": round(w / (t * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+    # dominant kernel: the dense GEMM (three launches per step, same FLOPs each)
+    dense = [t for (n, k, _), t in zip(wk.ops, op_ms) if n.startswith("gemm ")]
+    d = wk.dense
+    dense_flops = 2.0 * d.tokens * d.out * d.hidden
+    achieved = dense_flops / (statistics.mean(dense) * 1e-3) / 1e12
+    roofline = {"kernel": "k_gemm_nvfp4 (dense fprop/dgrad/wgrad)", "bound": "tensor",
+                "achieved": round(achieved, 1), "peak": round(fp4_peak_sust, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / fp4_peak_sust, 4),
+                "peak_note": f"{pk['source']} sustained bf16 x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
+                "frac_of_burst": round(achieved / fp4_peak_burst, 4), "traffic": None}
+    q_dy = op_ms[3]
+    roofline_q = {"kernel": "k_amax + k_quant1d<SR> (dY 1x16 SR)", "bound": "hbm",
+                  "achieved": round(wk.ops[3][2] / (q_dy * 1e-3) / 1e9, 1), "peak": pk["hbm_gbs"],
+                  "unit": "GB/s", "frac": round(wk.ops[3][2] / (q_dy * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                  "traffic": None}
+
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        e2e = measure_e2e(wk, args.e2e_steps, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sec, desc, th = oracle_sample(args.workload, budget_s=15.0)
+        cpu = {"value": round(wk.gemm_flops / sec / 1e12, 9), "unit": "TFLOP/s", "cores": th,
+               "kind": "oracle", "sample": desc, "seconds_per_step_extrapolated": round(sec, 1)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
+        "data": "synthetic (seeded device generators; no dataset)",
+        "config": {"workload": f"{args.workload}_full_step", "dense_tokens": d.tokens, "hidden": d.hidden,
+                   "in_proj_out": d.out, "moe_tokens": wk.moe.tokens, "moe_latent": wk.moe.latent,
+                   "moe_expert_hidden": wk.moe.expert_hidden, "experts": wk.moe.experts, "topk": wk.moe.topk,
+                   "moe_rows": wk.R, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (tens of GB streamed per step); no flush"},
+        "gemm_tflops": round(wk.gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
+        "quantize_gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1),
+        "quantize_frac_hbm": round(quant_bytes / (quant_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+        "ops": ops, "roofline": roofline, "roofline_quantize": roofline_q,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk,
+        "device_status": status, "routing": {"max_vio": round(wk.routing.max_vio, 3),
+                                             "empty_experts": int((wk.routing.counts == 0).sum())},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def measure_e2e(wk: Workload, steps: int, dev):
+    """Same metric through the public API with host buffers: every step copies
+    all inputs from pinned host memory, runs the step and reads every output
+    back.  Skipped (None) when pinned host memory for it is not available."""
+    import psutil
+    import torch
+    in_bytes = sum(t.numel() * t.element_size() for t in wk.input_tensors)
+    out_bytes = sum(t.numel() * t.element_size() for t in wk.output_tensors)
+    avail = psutil.virtual_memory().available
+    if avail < 2 * (in_bytes + out_bytes):
+        return {"value": None, "unit": "TFLOP/s", "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+                "skipped": f"needs {2 * (in_bytes + out_bytes) / 1e9:.0f} GB free host memory, {avail / 1e9:.0f} GB available"}
+    host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wk.input_tensors]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wk.output_tensors]
+    for h, t in zip(host_in, wk.input_tensors):
+        h.copy_(t)
+    torch.cuda.synchronize()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(steps):
+        for h, t in zip(host_in, wk.input_tensors):
+            t.copy_(h, non_blocking=True)
+        wk.step()
+        for h, t in zip(host_out, wk.output_tensors):
+            h.copy_(t, non_blocking=True)
+    s1.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1) / steps
+    del host_in, host_out
+    return {"value": round(wk.gemm_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 2),
+            "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes, "steps": steps}
+
+
+def reference_arm(args):
+    """The CPU oracle as the reference arm: each step runs a bounded sample of
+    the workload on the host cores; value is extrapolated to the full step."""
+    times = []
+    desc, th, sec = "", 1, 0.0
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        sec, desc, th = oracle_sample(args.workload, budget_s=4.0)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    from nvfp4_precision_02_b300 import workloads as wl
+    d = wl.ULTRA_DENSE if args.workload == "ultra" else wl.SUPER_DENSE
+    m = wl.ULTRA_MOE if args.workload == "ultra" else wl.SUPER_MOE
+    R = m.tokens * m.topk
+    flops = 3 * 2.0 * d.tokens * d.out * d.hidden + 2 * 2.0 * R * m.expert_hidden * m.latent
+    value = flops / sec / 1e12
+    line = {"metric": METRIC, "value": round(value, 9), "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{args.workload}_full_step", "sample_wall_s": round(statistics.mean(times), 2)},
+            "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

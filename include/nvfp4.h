@@ -1,0 +1,249 @@
+/*
+ * nvfp4.h -- C ABI of libnvfp4.so: NVFP4 training linear layers on one
+ * B300 (sm_103a).
+ *
+ * The method (web pages summarising the Nemotron 3 Super / Ultra technical
+ * reports):
+ *   - "Nemotron 3 Super -- technical report summary" (gkm0120.cn), section 1,
+ *     pre-training table, row "training precision": NVFP4 = E2M1 elements in
+ *     16-element micro-blocks with E4M3 scaling.
+ *   - same page, "Infra design" table: NVFP4 GEMMs for fprop, dgrad and wgrad;
+ *     2D block scaling for weights, 1D block scaling for activations and
+ *     gradients; random Hadamard transforms plus stochastic rounding.
+ *   - "Nemotron 3 Ultra: Open, Efficient Mixture-of-Experts Hybrid
+ *     Mamba-Transformer Model for Agentic Reasoning" (papercache.org
+ *     translation), section 2.2: 2D block quantisation of weights, the RHT
+ *     on the inputs of wgrad, SR on gradients.
+ *   - "Nemotron 3 Super" summary (papers.lianghsun.dev), section 2.2: the
+ *     MoE routed-expert GEMMs run in NVFP4.
+ *
+ * Numerics (the pages give the format, not the formulas; these readings are
+ * fixed here and every entry point follows them bit for bit):
+ *   tensor scale  S_enc = 2688 / amax in FP32 (1 if amax == 0, FLT_MAX if the
+ *                 quotient overflows); decode scale dec = 1 / S_enc.
+ *   block scale   sf = E4M3(round-nearest-even, saturating at 448) of
+ *                 (bamax / 6) * S_enc, computed as two FP32 operations.
+ *   element       sf == 0 gives code +0; otherwise v = x * (S_enc / sf) in
+ *                 FP32, rounded to E2M1 {0,.5,1,1.5,2,3,4,6} (nearest-even,
+ *                 saturating at 6) or stochastically (below); the sign bit
+ *                 is copied from x.
+ *   SR            element e (row-major index in the quantised output) draws
+ *                 word e & 3 of Philox4x32 with 5 rounds, key = seed,
+ *                 counter = (e >> 2 as two 32-bit halves, 0, 0); with grid
+ *                 neighbours lo <= |v| < hi and p = (|v|-lo)/(hi-lo), the
+ *                 magnitude rounds up iff (word >> 8) < p * 2^24.
+ *   RHT           per column, per 16 consecutive rows: y = 0.25 * H16 * (s .* x),
+ *                 s_j = -1 where bit j of sign_mask is set, H16 the Sylvester
+ *                 Hadamard matrix, evaluated as the FP32 butterfly with strides
+ *                 1, 2, 4, 8.
+ *
+ * Layouts:
+ *   codes  uint8 [rows, cols/2], rows cols/2 bytes apart; element 2j of a
+ *          row is the low nibble of byte j, element 2j+1 the high nibble;
+ *          nibble = sign << 3 | E2M1 magnitude index.
+ *   sf     block scale (r, c) of a [rows, cols] operand (c < cols/16) sits at
+ *          byte ((r/128) * ceil(cols/64) + c/4) * 512
+ *               + (r%32)*16 + ((r%128)/32)*4 + c%4,
+ *          i.e. 128x4 atoms of 512 bytes, rows padded to 128 and scale
+ *          columns to 4; padding bytes are written as 0 by the quantisers.
+ *          nvfp4_sf_bytes() gives the size.
+ *   grouped operands: group g's rows are offsets[g] .. offsets[g+1]-1 of the
+ *          codes, and its block scales start at scale row
+ *          P_g = sum_{i<g} ceil((offsets[i+1]-offsets[i]) / 128) * 128.
+ *   batched 2D weights: entry b of a [batch, rows, cols] weight owns codes
+ *          bytes [b*rows*cols/2, ...) and sf bytes
+ *          [b*nvfp4_sf_bytes(rows, cols), ...).
+ *
+ * Ownership and errors:
+ *   The caller allocates every device buffer and owns the stream; the
+ *   library allocates no device memory.  Every call validates its
+ *   arguments on the host before launching anything and returns a status;
+ *   work is enqueued asynchronously on `stream` (NULL = legacy default
+ *   stream).  Launch failures return NVFP4_ERR_CUDA with the CUDA message in
+ *   nvfp4_last_error().  Values that live in device memory (group offsets)
+ *   cannot be checked on the host: kernels clamp them into range and record
+ *   NVFP4_DEV_* codes in a device status word read by nvfp4_device_status().
+ *   Bounded waits inside kernels that give up record NVFP4_DEV_TIMEOUT there
+ *   and return instead of hanging.
+ *   All device pointers must be 16-byte aligned; all leading dimensions are
+ *   in elements and must make every row start 16-byte aligned.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *nvfp4_stream_t;
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_NULL = 1,        /* a required pointer is NULL */
+    NVFP4_ERR_SHAPE = 2,       /* negative size, dimension not a multiple of 16 (32 for GEMM K), mismatch */
+    NVFP4_ERR_ALIGN = 3,       /* pointer or leading dimension breaks 16-byte alignment */
+    NVFP4_ERR_DEVICE = 4,      /* no CUDA device or not compute capability 10.3 */
+    NVFP4_ERR_CUDA = 5,        /* a CUDA call failed; see nvfp4_last_error() */
+    NVFP4_ERR_TIMEOUT = 6,     /* a kernel abandoned a bounded wait */
+    NVFP4_ERR_LIMIT = 7        /* a size is beyond a documented limit */
+} nvfp4_status;
+
+typedef enum { NVFP4_ROUND_RNE = 0, NVFP4_ROUND_SR = 1 } nvfp4_round;
+typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_FP32 = 1 } nvfp4_out_dtype;
+
+/* Device status word codes (bit flags, sticky until read). */
+#define NVFP4_DEV_TIMEOUT     1
+#define NVFP4_DEV_BAD_OFFSETS 2
+
+/* Largest group count of the grouped calls. */
+#define NVFP4_MAX_GROUPS 1024
+
+/* A quantised operand.  cols is the reduction (K) dimension. */
+typedef struct {
+    void    *codes;    /* device, uint8 [rows, cols/2] */
+    uint8_t *sf;       /* device, swizzled E4M3 block scales */
+    float   *amax;     /* device, FP32 amax: 1 value, or 1 per group / batch entry */
+    int64_t  rows;
+    int64_t  cols;
+} nvfp4_tensor;
+
+/* ------------------------------------------------------------- layout */
+
+/* Bytes of the swizzled block-scale buffer of a [rows, cols] operand. */
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols);
+
+/* Upper bound of the block-scale bytes of a grouped [rows, cols] operand with
+ * num_groups groups (each group may add up to 127 padding rows). */
+size_t nvfp4_sf_bytes_grouped(int64_t rows, int64_t cols, int32_t num_groups);
+
+/* Byte offset of block scale (r, c) inside the swizzled buffer. */
+int64_t nvfp4_sf_offset(int64_t r, int64_t c, int64_t cols);
+
+/* ------------------------------------------------------------- amax */
+
+/* amax[b] = max |x| over entry b of a bf16 [batch, rows, cols] tensor with
+ * row stride ld (entries rows*ld elements apart).  amax: device, batch floats,
+ * overwritten.  Inputs must be finite.  (Per-tensor FP32 scale of the
+ * recipe; the max-based scaling of "Nemotron 3 Super" summary,
+ * papers.lianghsun.dev, section 4.2.) */
+nvfp4_status nvfp4_amax(const void *x, int64_t batch, int64_t rows, int64_t cols,
+                        int64_t ld, float *amax, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------- quantisers */
+
+/* 1D (1x16) quantisation of activations (RNE) or gradients (SR) -- "Infra
+ * design" table of the Super summary; SR of gradients, Ultra report 2.2.
+ * x: bf16 [rows, cols], row stride ld; cols % 16 == 0.
+ * out: codes, sf (nvfp4_sf_bytes(rows, cols)), amax (1 float), rows, cols
+ * must equal the arguments.  amax_in (device, nullable): when given, its
+ * value is the tensor amax (and is copied to out->amax); otherwise the
+ * amax is computed first (an extra read of x).  seed is used only for SR. */
+nvfp4_status nvfp4_quantize_1d(const void *x, int64_t rows, int64_t cols, int64_t ld,
+                               nvfp4_round mode, uint64_t seed, const float *amax_in,
+                               nvfp4_tensor *out, nvfp4_stream_t stream);
+
+/* Grouped 1D quantisation of expert-sorted activations (LatentMoE routed
+ * experts in NVFP4, Super summary papers.lianghsun.dev 2.2): group g is rows
+ * offsets[g] .. offsets[g+1]-1 and has its own tensor amax (out->amax[g]).
+ * offsets: device int64 [num_groups+1], non-decreasing, offsets[0] == 0,
+ * offsets[num_groups] <= rows; empty groups allowed.  out->sf must hold
+ * nvfp4_sf_bytes_grouped(rows, cols, num_groups) bytes; block scales of
+ * group g start at scale row P_g (see Layouts).  SR index e = r*cols + c
+ * over the whole output.  amax_in: device, num_groups floats, nullable.
+ * 1 <= num_groups <= NVFP4_MAX_GROUPS. */
+nvfp4_status nvfp4_quantize_1d_grouped(const void *x, int64_t rows, int64_t cols, int64_t ld,
+                                       const int64_t *offsets, int32_t num_groups,
+                                       nvfp4_round mode, uint64_t seed, const float *amax_in,
+                                       nvfp4_tensor *out, nvfp4_stream_t stream);
+
+/* 2D (16x16) quantisation of weights, so that W and W^T quantise
+ * identically (Super summary "Infra design"; Ultra report 2.2).
+ * w: bf16 [batch, rows, cols], row stride ld, entry stride rows*ld;
+ * rows % 16 == 0, cols % 16 == 0.  Always RNE.
+ * out   (required): codes [batch][rows, cols/2], sf per entry
+ *       nvfp4_sf_bytes(rows, cols) with each tile's scale on every one of its
+ *       16 rows (GEMM-ready), amax[batch]; out->rows == rows, out->cols == cols.
+ * out_t (nullable): the transposed operand W^T -- codes [batch][cols, rows/2],
+ *       sf per entry nvfp4_sf_bytes(cols, rows); amax may be NULL (the
+ *       amax lives in out->amax); out_t->rows == cols, out_t->cols == rows.
+ * tile_sf (nullable): device uint8 [batch][rows/16, cols/16] row-major.
+ * amax_in: device, batch floats, nullable. */
+nvfp4_status nvfp4_quantize_2d(const void *w, int64_t batch, int64_t rows, int64_t cols,
+                               int64_t ld, const float *amax_in, nvfp4_tensor *out,
+                               nvfp4_tensor *out_t, uint8_t *tile_sf, nvfp4_stream_t stream);
+
+/* amax of the RHT output of x (bf16 [tokens, cols], row stride ld,
+ * tokens % 16 == 0) -> amax (device, 1 float). */
+nvfp4_status nvfp4_rht_amax(const void *x, int64_t tokens, int64_t cols, int64_t ld,
+                            uint16_t sign_mask, float *amax, nvfp4_stream_t stream);
+
+/* RHT + 1D quantisation of a wgrad input (Super summary "Infra design";
+ * Ultra report 2.2: RHT on the inputs of wgrad).  x: bf16 [tokens, cols],
+ * row stride ld, tokens % 16 == 0.  The transform runs along tokens (the
+ * wgrad K axis); the result is the TRANSPOSED operand out_t: codes
+ * [cols, tokens/2], sf nvfp4_sf_bytes(cols, tokens), amax (1 float) of the
+ * transformed values; out_t->rows == cols, out_t->cols == tokens.
+ * Use the same sign_mask for both operands of one wgrad GEMM.
+ * SR index e = c*tokens + t.  amax_in: device, nullable. */
+nvfp4_status nvfp4_rht_quantize(const void *x, int64_t tokens, int64_t cols, int64_t ld,
+                                uint16_t sign_mask, nvfp4_round mode, uint64_t seed,
+                                const float *amax_in, nvfp4_tensor *out_t,
+                                nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------- GEMMs */
+
+/* C[m, n] = alpha * sum_k a_k * sa * b_k * sb with FP32 accumulation, where
+ * alpha = dec(a->amax) * dec(b->amax) in FP32 -- the fprop / dgrad / wgrad
+ * NVFP4 GEMMs (Super summary "Infra design"; Ultra report 2.2).
+ * a: [M, K], b: [N, K] (both K-major, a->cols == b->cols == K, K % 32 == 0
+ * so that code rows are 16-byte multiples).  c: device [M, N], row stride
+ * ldc elements, bf16 (one RNE rounding of the FP32 result) or FP32.
+ * M, N >= 1 arbitrary. */
+nvfp4_status nvfp4_gemm(const nvfp4_tensor *a, const nvfp4_tensor *b, void *c, int64_t ldc,
+                        nvfp4_out_dtype c_dtype, nvfp4_stream_t stream);
+
+/* Grouped GEMM of the LatentMoE routed experts: for every group g,
+ * C[offsets[g] .. offsets[g+1]-1, :] = alpha_g * A_g * W_g^T with
+ * alpha_g = dec(a->amax[g]) * dec(b->amax[g]).  a: grouped operand from
+ * nvfp4_quantize_1d_grouped ([R, K], K % 32 == 0).  b: batched operand from
+ * nvfp4_quantize_2d with batch == num_groups, b->rows == n per expert,
+ * b->cols == K.  offsets: device int64 [num_groups+1] as for the grouped
+ * quantiser.  Rows of C outside [offsets[0], offsets[num_groups]) are not
+ * written.  c: bf16 or FP32 [R, n], row stride ldc. */
+nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int64_t *offsets, int32_t num_groups,
+                                const nvfp4_tensor *b, int64_t n, void *c, int64_t ldc,
+                                nvfp4_out_dtype c_dtype, nvfp4_stream_t stream);
+
+/* ------------------------------------------------------------- status */
+
+const char *nvfp4_status_string(nvfp4_status status);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char *nvfp4_last_error(void);
+
+/* Synchronises the current device, returns the device status word
+ * (NVFP4_DEV_* bit flags, 0 if clean) in *flags and clears it.  Returns
+ * NVFP4_ERR_TIMEOUT if NVFP4_DEV_TIMEOUT was set, NVFP4_OK otherwise. */
+nvfp4_status nvfp4_device_status(int32_t *flags);
+
+/* Number of kernels this library has launched in this process (diagnostic;
+ * counts every successful launch of every entry point). */
+uint64_t nvfp4_launch_count(void);
+
+/* Test hook: the next call to any entry point above returns `status`
+ * without launching (NVFP4_OK clears the hook).  Host-side only. */
+void nvfp4_debug_inject(nvfp4_status status);
+
+/* Test hook: launches one block that waits on a barrier nothing will
+ * complete, giving up after timeout_ns nanoseconds; the give-up is recorded
+ * as NVFP4_DEV_TIMEOUT in the device status word. */
+nvfp4_status nvfp4_debug_wait_timeout(int64_t timeout_ns, nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_H */

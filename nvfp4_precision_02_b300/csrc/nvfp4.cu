@@ -1,0 +1,522 @@
+// nvfp4.cu -- the C ABI of libnvfp4.so (declared in include/nvfp4.h).
+//
+// Host side only validates arguments, builds TMA tensor maps and launches the
+// kernels of quant.cuh and gemm.cuh on the caller's stream.  It allocates no
+// device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "nvfp4.h"
+#include "common.cuh"
+#include "quant.cuh"
+#include "gemm.cuh"
+
+using namespace nvfp4;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+std::atomic<int> g_inject{0};
+std::atomic<uint64_t> g_launches{0};
+
+nvfp4_status fail(nvfp4_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+#define NVFP4_INJECT_CHECK()                                                              \
+    do {                                                                                  \
+        const int inj = g_inject.exchange(0);                                             \
+        if (inj != 0) return fail((nvfp4_status)inj, "injected failure (test hook)");     \
+    } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+    bool checked = false;
+    bool ok = false;
+    int sms = 0;
+    bool gemm_attr = false;
+};
+DeviceInfo g_dev[64];
+std::mutex g_dev_mu;
+
+// Current device must be compute capability 10.3 (B300, sm_103a).
+nvfp4_status check_device(int* sms = nullptr, int* dev_out = nullptr) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return fail(NVFP4_ERR_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.checked) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(NVFP4_ERR_DEVICE, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+        }
+        d.ok = (prop.major == 10 && prop.minor == 3);
+        d.sms = prop.multiProcessorCount;
+        d.checked = true;
+        if (!d.ok) return fail(NVFP4_ERR_DEVICE, "device %d is sm_%d%d, this library is built for sm_103a", dev, prop.major, prop.minor);
+    }
+    if (!d.ok) return fail(NVFP4_ERR_DEVICE, "device %d is not sm_103", dev);
+    if (sms) *sms = d.sms;
+    if (dev_out) *dev_out = dev;
+    return NVFP4_OK;
+}
+
+nvfp4_status launched(const char* what) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return NVFP4_OK;
+}
+
+nvfp4_status cuda_call(cudaError_t e, const char* what) {
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(NVFP4_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    }
+    return NVFP4_OK;
+}
+
+#define NVFP4_TRY(expr)                           \
+    do {                                          \
+        const nvfp4_status st_ = (expr);          \
+        if (st_ != NVFP4_OK) return st_;          \
+    } while (0)
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Shared checks of a bf16 input [rows, cols] with row stride ld.
+// vec_rows: the kernel reads rows with 16-byte vectors (ld % 8 == 0 and a
+// 16-byte aligned base); otherwise 2-byte alignment suffices.
+nvfp4_status check_input(const void* x, int64_t rows, int64_t cols, int64_t ld, int64_t mult, const char* name,
+                         bool vec_rows = true) {
+    if (x == nullptr && rows > 0) return fail(NVFP4_ERR_NULL, "%s is NULL", name);
+    if (rows < 0 || cols < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative size", name);
+    if (cols % mult != 0) return fail(NVFP4_ERR_SHAPE, "%s: cols=%lld is not a multiple of %lld", name, (long long)cols, (long long)mult);
+    if (ld < cols) return fail(NVFP4_ERR_SHAPE, "%s: ld=%lld < cols=%lld", name, (long long)ld, (long long)cols);
+    if (vec_rows && (ld % 8 != 0 || !aligned16(x)))
+        return fail(NVFP4_ERR_ALIGN, "%s: rows must start 16-byte aligned (ld %% 8 == 0, aligned base)", name);
+    if (!vec_rows && ((uintptr_t)x & 1u)) return fail(NVFP4_ERR_ALIGN, "%s: not 2-byte aligned", name);
+    if ((rows * cols) / 8 >= (int64_t(1) << 32)) return fail(NVFP4_ERR_LIMIT, "%s: more than 2^35 elements", name);
+    return NVFP4_OK;
+}
+
+nvfp4_status check_out(const nvfp4_tensor* t, int64_t rows, int64_t cols, bool need_amax, const char* name) {
+    if (t == nullptr) return fail(NVFP4_ERR_NULL, "%s is NULL", name);
+    if (t->rows != rows || t->cols != cols)
+        return fail(NVFP4_ERR_SHAPE, "%s: shape [%lld, %lld] != expected [%lld, %lld]", name, (long long)t->rows,
+                    (long long)t->cols, (long long)rows, (long long)cols);
+    if (rows > 0 && (t->codes == nullptr || t->sf == nullptr)) return fail(NVFP4_ERR_NULL, "%s: codes/sf NULL", name);
+    if (need_amax && t->amax == nullptr) return fail(NVFP4_ERR_NULL, "%s: amax NULL", name);
+    if (!aligned16(t->codes) || !aligned16(t->sf)) return fail(NVFP4_ERR_ALIGN, "%s: codes/sf not 16-byte aligned", name);
+    return NVFP4_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2D uint8 tensor map over packed codes [rows, row_bytes] with a box of
+// {128 bytes, box_rows} and 128-byte swizzle (the tcgen05 K-major layout).
+nvfp4_status make_code_map(CUtensorMap* map, const void* codes, int64_t rows, int64_t row_bytes, int box_rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(codes), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return NVFP4_OK;
+}
+
+int quant_blocks(int64_t rows, int sms) {
+    const int64_t b = cdiv(rows, 8);
+    return (int)std::max<int64_t>(1, std::min<int64_t>(b, (int64_t)sms * 8));
+}
+
+int amax_blocks(int64_t units) {
+    return (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(units, 256 * 8), 4096));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return (size_t)sf_bytes(rows, cols);
+}
+
+size_t nvfp4_sf_bytes_grouped(int64_t rows, int64_t cols, int32_t num_groups) {
+    if (rows < 0 || cols <= 0 || num_groups <= 0) return 0;
+    return (size_t)sf_bytes(rows + 127 * (int64_t)num_groups, cols);
+}
+
+int64_t nvfp4_sf_offset(int64_t r, int64_t c, int64_t cols) { return sf_offset(r, c, cols); }
+
+const char* nvfp4_status_string(nvfp4_status s) {
+    switch (s) {
+        case NVFP4_OK: return "ok";
+        case NVFP4_ERR_NULL: return "null pointer";
+        case NVFP4_ERR_SHAPE: return "invalid shape";
+        case NVFP4_ERR_ALIGN: return "misaligned pointer or leading dimension";
+        case NVFP4_ERR_DEVICE: return "no sm_103 CUDA device";
+        case NVFP4_ERR_CUDA: return "CUDA error";
+        case NVFP4_ERR_TIMEOUT: return "kernel wait timed out";
+        case NVFP4_ERR_LIMIT: return "size beyond a documented limit";
+    }
+    return "unknown status";
+}
+
+const char* nvfp4_last_error(void) { return g_last_error; }
+
+void nvfp4_debug_inject(nvfp4_status status) { g_inject.store((int)status); }
+
+uint64_t nvfp4_launch_count(void) { return g_launches.load(); }
+
+nvfp4_status nvfp4_amax(const void* x, int64_t batch, int64_t rows, int64_t cols, int64_t ld, float* amax,
+                        nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    if (amax == nullptr) return fail(NVFP4_ERR_NULL, "amax is NULL");
+    if (batch < 1 || batch > 65535) return fail(NVFP4_ERR_SHAPE, "batch must be in [1, 65535]");
+    NVFP4_TRY(check_input(x, rows, cols, ld, 16, "x"));
+    if (((uintptr_t)amax & 3u) != 0) return fail(NVFP4_ERR_ALIGN, "amax not 4-byte aligned");
+    NVFP4_TRY(check_device());
+    NVFP4_TRY(cuda_call(cudaMemsetAsync(amax, 0, sizeof(float) * batch, stream), "memset amax"));
+    if (rows == 0 || cols == 0) return NVFP4_OK;
+    k_amax<<<dim3(amax_blocks(rows * cols / 8), (unsigned)batch), 256, 0, stream>>>(
+        (const uint16_t*)x, rows, cols, ld, rows * ld, amax);
+    return launched("k_amax");
+}
+
+nvfp4_status nvfp4_quantize_1d(const void* x, int64_t rows, int64_t cols, int64_t ld, nvfp4_round mode,
+                               uint64_t seed, const float* amax_in, nvfp4_tensor* out, nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    NVFP4_TRY(check_input(x, rows, cols, ld, 16, "x"));
+    NVFP4_TRY(check_out(out, rows, cols, true, "out"));
+    if (mode != NVFP4_ROUND_RNE && mode != NVFP4_ROUND_SR) return fail(NVFP4_ERR_SHAPE, "bad rounding mode");
+    int sms = 0;
+    NVFP4_TRY(check_device(&sms));
+    const float* am = amax_in;
+    float* copy = nullptr;
+    if (am == nullptr) {
+        NVFP4_TRY(cuda_call(cudaMemsetAsync(out->amax, 0, sizeof(float), stream), "memset amax"));
+        if (rows > 0 && cols > 0) {
+            k_amax<<<dim3(amax_blocks(rows * cols / 8), 1), 256, 0, stream>>>((const uint16_t*)x, rows, cols, ld, 0,
+                                                                               out->amax);
+            NVFP4_TRY(launched("k_amax"));
+        }
+        am = out->amax;
+    } else if (amax_in != out->amax) {
+        copy = out->amax;
+    }
+    if (rows == 0 || cols == 0) {
+        if (copy) NVFP4_TRY(cuda_call(cudaMemcpyAsync(copy, amax_in, 4, cudaMemcpyDeviceToDevice, stream), "amax copy"));
+        return NVFP4_OK;
+    }
+    const int nb = quant_blocks(rows, sms);
+    uint8_t* codes = (uint8_t*)out->codes;
+    if (mode == NVFP4_ROUND_SR)
+        k_quant1d<true, false><<<nb, 256, 0, stream>>>((const uint16_t*)x, rows, cols, ld, am, seed, codes, out->sf,
+                                                       nullptr, 0, copy);
+    else
+        k_quant1d<false, false><<<nb, 256, 0, stream>>>((const uint16_t*)x, rows, cols, ld, am, seed, codes, out->sf,
+                                                        nullptr, 0, copy);
+    NVFP4_TRY(launched("k_quant1d"));
+    if (rows % 128 != 0) {
+        k_zero_pad_rows<<<64, 256, 0, stream>>>(out->sf, rows, cols, nullptr, 0);
+        NVFP4_TRY(launched("k_zero_pad_rows"));
+    }
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_quantize_1d_grouped(const void* x, int64_t rows, int64_t cols, int64_t ld, const int64_t* offsets,
+                                       int32_t num_groups, nvfp4_round mode, uint64_t seed, const float* amax_in,
+                                       nvfp4_tensor* out, nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    NVFP4_TRY(check_input(x, rows, cols, ld, 16, "x"));
+    NVFP4_TRY(check_out(out, rows, cols, true, "out"));
+    if (offsets == nullptr) return fail(NVFP4_ERR_NULL, "offsets is NULL");
+    if (num_groups < 1 || num_groups > NVFP4_MAX_GROUPS) return fail(NVFP4_ERR_LIMIT, "num_groups must be in [1, %d]", NVFP4_MAX_GROUPS);
+    if (rows >= (int64_t(1) << 31) - 128 * (int64_t)num_groups) return fail(NVFP4_ERR_LIMIT, "rows too large");
+    if (mode != NVFP4_ROUND_RNE && mode != NVFP4_ROUND_SR) return fail(NVFP4_ERR_SHAPE, "bad rounding mode");
+    int sms = 0;
+    NVFP4_TRY(check_device(&sms));
+    const size_t tab = sizeof(int32_t) * 2 * (num_groups + 1);
+    const float* am = amax_in;
+    float* copy = nullptr;
+    if (am == nullptr) {
+        NVFP4_TRY(cuda_call(cudaMemsetAsync(out->amax, 0, sizeof(float) * num_groups, stream), "memset amax"));
+        if (rows > 0 && cols > 0) {
+            k_amax_grouped<<<quant_blocks(rows, sms), 256, tab, stream>>>((const uint16_t*)x, rows, cols, ld, offsets,
+                                                                           num_groups, out->amax);
+            NVFP4_TRY(launched("k_amax_grouped"));
+        }
+        am = out->amax;
+    } else if (amax_in != out->amax) {
+        copy = out->amax;
+    }
+    if (rows == 0 || cols == 0) {
+        if (copy)
+            NVFP4_TRY(cuda_call(cudaMemcpyAsync(copy, amax_in, 4 * num_groups, cudaMemcpyDeviceToDevice, stream), "amax copy"));
+        return NVFP4_OK;
+    }
+    const int nb = quant_blocks(rows, sms);
+    uint8_t* codes = (uint8_t*)out->codes;
+    if (mode == NVFP4_ROUND_SR)
+        k_quant1d<true, true><<<nb, 256, tab, stream>>>((const uint16_t*)x, rows, cols, ld, am, seed, codes, out->sf,
+                                                        offsets, num_groups, copy);
+    else
+        k_quant1d<false, true><<<nb, 256, tab, stream>>>((const uint16_t*)x, rows, cols, ld, am, seed, codes, out->sf,
+                                                         offsets, num_groups, copy);
+    NVFP4_TRY(launched("k_quant1d grouped"));
+    k_zero_pad_rows<<<std::min(num_groups, 256), 256, tab, stream>>>(out->sf, rows, cols, offsets, num_groups);
+    return launched("k_zero_pad_rows grouped");
+}
+
+nvfp4_status nvfp4_quantize_2d(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ld,
+                               const float* amax_in, nvfp4_tensor* out, nvfp4_tensor* out_t, uint8_t* tile_sf,
+                               nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    if (batch < 1 || batch > 65535) return fail(NVFP4_ERR_SHAPE, "batch must be in [1, 65535]");
+    NVFP4_TRY(check_input(w, rows * batch, cols, ld, 16, "w"));
+    if (rows % 16 != 0) return fail(NVFP4_ERR_SHAPE, "rows=%lld is not a multiple of 16", (long long)rows);
+    if (cdiv(rows, 64) > 65535) return fail(NVFP4_ERR_LIMIT, "rows too large");
+    NVFP4_TRY(check_out(out, rows, cols, true, "out"));
+    if (out_t != nullptr) NVFP4_TRY(check_out(out_t, cols, rows, false, "out_t"));
+    int sms = 0;
+    NVFP4_TRY(check_device(&sms));
+    const float* am = amax_in;
+    float* copy = nullptr;
+    if (am == nullptr) {
+        NVFP4_TRY(cuda_call(cudaMemsetAsync(out->amax, 0, sizeof(float) * batch, stream), "memset amax"));
+        if (rows > 0 && cols > 0) {
+            k_amax<<<dim3(amax_blocks(rows * cols / 8), (unsigned)batch), 256, 0, stream>>>((const uint16_t*)w, rows, cols,
+                                                                                          ld, rows * ld, out->amax);
+            NVFP4_TRY(launched("k_amax"));
+        }
+        am = out->amax;
+    } else if (amax_in != out->amax) {
+        copy = out->amax;
+    }
+    if (rows == 0 || cols == 0) {
+        if (copy) NVFP4_TRY(cuda_call(cudaMemcpyAsync(copy, amax_in, 4 * batch, cudaMemcpyDeviceToDevice, stream), "amax copy"));
+        return NVFP4_OK;
+    }
+    dim3 grid((unsigned)cdiv(cols, 64), (unsigned)cdiv(rows, 64), (unsigned)batch);
+    k_quant2d<<<grid, 128, 0, stream>>>((const uint16_t*)w, rows, cols, ld, am, (uint8_t*)out->codes, out->sf,
+                                        out_t ? (uint8_t*)out_t->codes : nullptr, out_t ? out_t->sf : nullptr, tile_sf,
+                                        copy);
+    NVFP4_TRY(launched("k_quant2d"));
+    const bool pad = (rows % 128) || ((cols / 16) % 4) || (out_t && ((cols % 128) || ((rows / 16) % 4)));
+    if (pad) {
+        k_quant2d_pad<<<dim3(16, (unsigned)batch), 256, 0, stream>>>(out->sf, out_t ? out_t->sf : nullptr, rows, cols);
+        NVFP4_TRY(launched("k_quant2d_pad"));
+    }
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_rht_amax(const void* x, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask, float* amax,
+                            nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    if (amax == nullptr) return fail(NVFP4_ERR_NULL, "amax is NULL");
+    NVFP4_TRY(check_input(x, tokens, cols, ld, 1, "x", false));
+    if (tokens % 16 != 0) return fail(NVFP4_ERR_SHAPE, "tokens=%lld is not a multiple of 16", (long long)tokens);
+    if (cdiv(tokens, 64) > 65535) return fail(NVFP4_ERR_LIMIT, "tokens too large");
+    NVFP4_TRY(check_device());
+    NVFP4_TRY(cuda_call(cudaMemsetAsync(amax, 0, sizeof(float), stream), "memset amax"));
+    if (tokens == 0 || cols == 0) return NVFP4_OK;
+    k_rht<0><<<dim3((unsigned)cdiv(cols, 128), (unsigned)cdiv(tokens, 64)), 128, 0, stream>>>(
+        (const uint16_t*)x, tokens, cols, ld, sign_mask, amax, 0, nullptr, nullptr, nullptr);
+    return launched("k_rht amax");
+}
+
+nvfp4_status nvfp4_rht_quantize(const void* x, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask,
+                                nvfp4_round mode, uint64_t seed, const float* amax_in, nvfp4_tensor* out_t,
+                                nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    NVFP4_TRY(check_input(x, tokens, cols, ld, 1, "x", false));
+    if (tokens % 16 != 0) return fail(NVFP4_ERR_SHAPE, "tokens=%lld is not a multiple of 16", (long long)tokens);
+    if (cdiv(tokens, 64) > 65535) return fail(NVFP4_ERR_LIMIT, "tokens too large");
+    NVFP4_TRY(check_out(out_t, cols, tokens, true, "out_t"));
+    if (mode != NVFP4_ROUND_RNE && mode != NVFP4_ROUND_SR) return fail(NVFP4_ERR_SHAPE, "bad rounding mode");
+    NVFP4_TRY(check_device());
+    const float* am = amax_in;
+    float* copy = nullptr;
+    if (am == nullptr) {
+        NVFP4_TRY(cuda_call(cudaMemsetAsync(out_t->amax, 0, sizeof(float), stream), "memset amax"));
+        if (tokens > 0 && cols > 0) {
+            k_rht<0><<<dim3((unsigned)cdiv(cols, 128), (unsigned)cdiv(tokens, 64)), 128, 0, stream>>>(
+                (const uint16_t*)x, tokens, cols, ld, sign_mask, out_t->amax, 0, nullptr, nullptr, nullptr);
+            NVFP4_TRY(launched("k_rht amax"));
+        }
+        am = out_t->amax;
+    } else if (amax_in != out_t->amax) {
+        copy = out_t->amax;
+    }
+    if (tokens == 0 || cols == 0) {
+        if (copy) NVFP4_TRY(cuda_call(cudaMemcpyAsync(copy, amax_in, 4, cudaMemcpyDeviceToDevice, stream), "amax copy"));
+        return NVFP4_OK;
+    }
+    const dim3 grid((unsigned)cdiv(cols, 128), (unsigned)cdiv(tokens, 64));
+    if (mode == NVFP4_ROUND_SR)
+        k_rht<2><<<grid, 128, 0, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask, const_cast<float*>(am), seed,
+                                           (uint8_t*)out_t->codes, out_t->sf, copy);
+    else
+        k_rht<1><<<grid, 128, 0, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask, const_cast<float*>(am), seed,
+                                           (uint8_t*)out_t->codes, out_t->sf, copy);
+    NVFP4_TRY(launched("k_rht quantize"));
+    if (cols % 128 != 0) {
+        k_zero_pad_rows<<<64, 256, 0, stream>>>(out_t->sf, cols, tokens, nullptr, 0);
+        NVFP4_TRY(launched("k_zero_pad_rows"));
+    }
+    return NVFP4_OK;
+}
+
+static nvfp4_status check_operand(const nvfp4_tensor* t, const char* name) {
+    if (t == nullptr) return fail(NVFP4_ERR_NULL, "%s is NULL", name);
+    if (t->rows < 0 || t->cols < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative size", name);
+    if (t->rows > 0 && (t->codes == nullptr || t->sf == nullptr || t->amax == nullptr))
+        return fail(NVFP4_ERR_NULL, "%s: codes/sf/amax NULL", name);
+    if (!aligned16(t->codes) || !aligned16(t->sf)) return fail(NVFP4_ERR_ALIGN, "%s: codes/sf not 16-byte aligned", name);
+    return NVFP4_OK;
+}
+
+static nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int grid,
+                                nvfp4_out_dtype dt, nvfp4_stream_t stream, int dev) {
+    const int smem = gemm_smem_bytes(p.groups);
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!g_dev[dev].gemm_attr) {
+            NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     gemm_smem_bytes(NVFP4_MAX_GROUPS)), "smem attr"));
+            NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     gemm_smem_bytes(NVFP4_MAX_GROUPS)), "smem attr"));
+            g_dev[dev].gemm_attr = true;
+        }
+    }
+    if (dt == NVFP4_OUT_FP32)
+        k_gemm_nvfp4<true><<<grid, G_THREADS, smem, stream>>>(ma, mb, p);
+    else
+        k_gemm_nvfp4<false><<<grid, G_THREADS, smem, stream>>>(ma, mb, p);
+    return launched("k_gemm_nvfp4");
+}
+
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* c, int64_t ldc, nvfp4_out_dtype c_dtype,
+                        nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    NVFP4_TRY(check_operand(a, "a"));
+    NVFP4_TRY(check_operand(b, "b"));
+    const int64_t M = a->rows, N = b->rows, K = a->cols;
+    if (b->cols != K) return fail(NVFP4_ERR_SHAPE, "a->cols=%lld != b->cols=%lld", (long long)K, (long long)b->cols);
+    if (K % 32 != 0 || K == 0) return fail(NVFP4_ERR_SHAPE, "K=%lld must be a positive multiple of 32", (long long)K);
+    if (c_dtype != NVFP4_OUT_BF16 && c_dtype != NVFP4_OUT_FP32) return fail(NVFP4_ERR_SHAPE, "bad output dtype");
+    if (ldc < N) return fail(NVFP4_ERR_SHAPE, "ldc < N");
+    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) return fail(NVFP4_ERR_LIMIT, "M or N >= 2^31");
+    if (M == 0 || N == 0) return NVFP4_OK;
+    if (c == nullptr) return fail(NVFP4_ERR_NULL, "c is NULL");
+    const int esz = c_dtype == NVFP4_OUT_FP32 ? 4 : 2;
+    if (((uintptr_t)c % esz) != 0) return fail(NVFP4_ERR_ALIGN, "c is not aligned to its element size");
+    int sms = 0, dev = 0;
+    NVFP4_TRY(check_device(&sms, &dev));
+    CUtensorMap ma, mb;
+    NVFP4_TRY(make_code_map(&ma, a->codes, M, K / 2, G_BM));
+    NVFP4_TRY(make_code_map(&mb, b->codes, N, K / 2, G_BN));
+    GemmParams p{};
+    p.M = M; p.N = N; p.K = K;
+    p.offsets = nullptr; p.groups = 1;
+    p.sfa = a->sf; p.sfb = b->sf; p.sfb_group_stride = 0;
+    p.amax_a = a->amax; p.amax_b = b->amax;
+    p.c = c; p.ldc = ldc;
+    p.vec_store = aligned16(c) && (ldc * esz) % 16 == 0;
+    const int64_t tiles = cdiv(M, G_BM) * cdiv(N, G_BN);
+    const int grid = (int)std::min<int64_t>(tiles, sms);
+    return launch_gemm(ma, mb, p, grid, c_dtype, stream, dev);
+}
+
+nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, int32_t num_groups,
+                                const nvfp4_tensor* b, int64_t n, void* c, int64_t ldc, nvfp4_out_dtype c_dtype,
+                                nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    NVFP4_TRY(check_operand(a, "a"));
+    NVFP4_TRY(check_operand(b, "b"));
+    if (offsets == nullptr) return fail(NVFP4_ERR_NULL, "offsets is NULL");
+    if (num_groups < 1 || num_groups > NVFP4_MAX_GROUPS) return fail(NVFP4_ERR_LIMIT, "num_groups must be in [1, %d]", NVFP4_MAX_GROUPS);
+    const int64_t R = a->rows, K = a->cols;
+    if (b->rows != n || b->cols != K) return fail(NVFP4_ERR_SHAPE, "b must be [n, K] per expert");
+    if (K % 32 != 0 || K == 0) return fail(NVFP4_ERR_SHAPE, "K=%lld must be a positive multiple of 32", (long long)K);
+    if (n < 1) return fail(NVFP4_ERR_SHAPE, "n must be >= 1");
+    if (c_dtype != NVFP4_OUT_BF16 && c_dtype != NVFP4_OUT_FP32) return fail(NVFP4_ERR_SHAPE, "bad output dtype");
+    if (ldc < n) return fail(NVFP4_ERR_SHAPE, "ldc < n");
+    if (R >= (int64_t(1) << 31) - 128 * (int64_t)num_groups || n * (int64_t)num_groups >= (int64_t(1) << 31))
+        return fail(NVFP4_ERR_LIMIT, "rows or experts*n >= 2^31");
+    if (R == 0) return NVFP4_OK;
+    if (c == nullptr) return fail(NVFP4_ERR_NULL, "c is NULL");
+    const int esz = c_dtype == NVFP4_OUT_FP32 ? 4 : 2;
+    if (((uintptr_t)c % esz) != 0) return fail(NVFP4_ERR_ALIGN, "c is not aligned to its element size");
+    int sms = 0, dev = 0;
+    NVFP4_TRY(check_device(&sms, &dev));
+    CUtensorMap ma, mb;
+    NVFP4_TRY(make_code_map(&ma, a->codes, R, K / 2, G_BM));
+    NVFP4_TRY(make_code_map(&mb, b->codes, n * num_groups, K / 2, G_BN));
+    GemmParams p{};
+    p.M = R; p.N = n; p.K = K;
+    p.offsets = offsets; p.groups = num_groups;
+    p.sfa = a->sf; p.sfb = b->sf; p.sfb_group_stride = sf_bytes(n, K);
+    p.amax_a = a->amax; p.amax_b = b->amax;
+    p.c = c; p.ldc = ldc;
+    p.vec_store = aligned16(c) && (ldc * esz) % 16 == 0;
+    return launch_gemm(ma, mb, p, sms, c_dtype, stream, dev);
+}
+
+nvfp4_status nvfp4_device_status(int32_t* flags) {
+    NVFP4_INJECT_CHECK();
+    if (flags == nullptr) return fail(NVFP4_ERR_NULL, "flags is NULL");
+    NVFP4_TRY(check_device());
+    NVFP4_TRY(cuda_call(cudaDeviceSynchronize(), "cudaDeviceSynchronize"));
+    int v = 0, zero = 0;
+    NVFP4_TRY(cuda_call(cudaMemcpyFromSymbol(&v, g_dev_status, sizeof(int)), "read status"));
+    NVFP4_TRY(cuda_call(cudaMemcpyToSymbol(g_dev_status, &zero, sizeof(int)), "clear status"));
+    *flags = v;
+    return (v & DEV_TIMEOUT) ? NVFP4_ERR_TIMEOUT : NVFP4_OK;
+}
+
+nvfp4_status nvfp4_debug_wait_timeout(int64_t timeout_ns, nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    if (timeout_ns <= 0 || timeout_ns > 10000000000ll) return fail(NVFP4_ERR_SHAPE, "timeout must be in (0, 10 s]");
+    NVFP4_TRY(check_device());
+    k_wait_probe<<<1, 32, 0, stream>>>((uint64_t)timeout_ns);
+    return launched("k_wait_probe");
+}
+
+}  // extern "C"

@@ -1,0 +1,204 @@
+"""GPU parity of the NVFP4 GEMMs (tcgen05 block-scaled MMA) against the FP64
+GEMM of the oracle's own dequantised operands: every output element must
+satisfy |gpu - ref| <= 1e-5 * sum_k |a_k b_k| (plus one bf16 rounding for a
+bf16 output).  The oracle quantises the same bf16 inputs itself; nothing it
+uses comes from the CUDA path."""
+import numpy as np
+import pytest
+import torch
+
+from parity import gemm_within_bound, np_u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from nvfp4_precision_02_b300 import binding, build
+    build.build()
+    binding.lib()
+    assert torch.cuda.is_available()
+    return binding
+
+
+def _rand(rows, cols, seed, std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(rows, cols, generator=g) * std).to(torch.bfloat16)
+
+
+def _oracle_ref(orc, a, w, two_d=True):
+    qa = orc.quantize_1d(a)
+    M, K = a.shape
+    N = w.shape[0]
+    A = orc.dequantize(qa, M, K)
+    if two_d:
+        qw = orc.quantize_2d(w, want_t=False)
+        W = orc.dequantize_rows(qw["codes"][0], qw["sf"], K, float(qw["amax"][0]), np.arange(N))
+    else:
+        W = orc.dequantize(orc.quantize_1d(w), N, K)
+    return orc.gemm(A, W)
+
+
+def _quant_b(B, w, two_d):
+    """Weights take 16x16 blocks when N is a multiple of 16; any N takes 1x16."""
+    if two_d:
+        return B.quantize_2d(w, want_t=False)[0]
+    return B.quantize_1d(w)
+
+
+def _check(out, ref, absum, bf16):
+    ok, worst = gemm_within_bound(out, ref, absum, bf16)
+    bad = np.argwhere(~ok)
+    assert ok.all(), f"{len(bad)} elements out of bound, worst ratio {worst:.3g}, first {bad[:5].tolist()}"
+    return worst
+
+
+SHAPES = [(256, 256, 256),    # the tiny fprop workload shape
+          (1, 1, 32), (17, 33, 64), (128, 256, 256), (129, 257, 288), (300, 520, 1024),
+          (256, 384, 96), (64, 1000, 512), (520, 130, 2048)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("fp32", [False, True])
+def test_gemm_fprop_shapes(B, orc, M, N, K, fp32):
+    a = _rand(M, K, seed=M * 31 + K)
+    w = _rand(N, K, seed=N * 17 + K + 1, std=0.02)
+    two_d = N % 16 == 0
+    qa = B.quantize_1d(a.cuda())
+    qw = _quant_b(B, w.cuda(), two_d)
+    out = B.gemm(qa, qw, out_dtype=B.OUT_FP32 if fp32 else B.OUT_BF16)
+    torch.cuda.synchronize()
+    ref, absum = _oracle_ref(orc, a, w, two_d)
+    o = out.float().cpu().numpy()
+    _check(o, ref, absum, bf16=not fp32)
+
+
+def test_tiny_fprop_workload(B, orc):
+    """256x256 A and W ~ N(0,1), seed 0: 1x16 RNE A, 16x16 W, bf16 C = A.W^T."""
+    from nvfp4_precision_02_b300 import workloads as wl
+    a, w = wl.tiny_inputs()
+    qa = B.quantize_1d(a.cuda())
+    qw, _, _ = B.quantize_2d(w.cuda(), want_t=False)
+    out = B.gemm(qa, qw)
+    out32 = B.gemm(qa, qw, out_dtype=B.OUT_FP32)
+    torch.cuda.synchronize()
+    ref, absum = _oracle_ref(orc, a, w)
+    _check(out.float().cpu().numpy(), ref, absum, bf16=True)
+    _check(out32.cpu().numpy(), ref, absum, bf16=False)
+
+
+def test_gemm_ldc_and_exact_products(B, orc):
+    """Operands with one nonzero per row whose sixth is an E4M3 value
+    dequantise exactly, so every output is one exact product: the GPU must
+    reproduce it exactly (also through a padded ldc)."""
+    K = 64
+    A = torch.zeros(16, K)
+    W = torch.zeros(16, K)
+    for i in range(16):
+        A[i, (5 * i) % K] = [6, 3, 1.5, 0.75, 9, 4.5, 7.5, -10.5][i % 8]
+        W[i, (5 * i) % K] = [12, -6, 3, 1.5, 7.5, 0.375, 24, 9][i % 8]
+    amax = torch.tensor([2688.0], device="cuda")
+    qa = B.quantize_1d(A.to(torch.bfloat16).cuda(), amax_in=amax)
+    qw = B.quantize_1d(W.to(torch.bfloat16).cuda(), amax_in=amax)
+    out = torch.full((16, 24), 7.0, device="cuda")
+    B.gemm(qa, qw, out_dtype=B.OUT_FP32, out=out[:, :16])
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert (o[:, :16] == (A.double() @ W.double().T).numpy()).all()
+    assert (o[:, 16:] == 7.0).all()                      # nothing written beyond N
+
+
+def test_dgrad_and_wgrad_operands(B, orc):
+    """dgrad: dY (SR) x W^T from the 2D quantiser's transposed copy; wgrad:
+    RHT(dY)^T (SR) x RHT(X)^T (RNE) with one shared sign mask."""
+    T, Kh, N = 256, 192, 320
+    x = _rand(T, Kh, seed=1)
+    w = _rand(N, Kh, seed=2, std=0.02)
+    dy = _rand(T, N, seed=3, std=1e-3)
+    seed, mask = 7, 0x6A35
+    # dgrad: dX[T, Kh] = dY[T, N] . W[N, Kh] -> B operand is W^T [Kh, N]
+    qdy = B.quantize_1d(dy.cuda(), mode=B.SR, seed=seed)
+    _, qwt, _ = B.quantize_2d(w.cuda(), want_t=True)
+    dx = B.gemm(qdy, qwt, out_dtype=B.OUT_FP32)
+    # wgrad: dW[N, Kh] = dY^T . X over tokens, both through the RHT
+    sdy = B.rht_quantize(dy.cuda(), mask, mode=B.SR, seed=seed ^ 0x9E3779B97F4A7C15)
+    sx = B.rht_quantize(x.cuda(), mask, mode=B.RNE)
+    dw = B.gemm(sdy, sx, out_dtype=B.OUT_FP32)
+    torch.cuda.synchronize()
+    # oracle
+    r_dy = orc.quantize_1d(dy, mode=orc.SR, seed=seed)
+    r_w = orc.quantize_2d(w)
+    A = orc.dequantize(r_dy, T, N)
+    Bt = orc.dequantize_rows(r_w["codes_t"][0], r_w["sf_t"], N, float(r_w["amax"][0]), np.arange(Kh))
+    ref, absum = orc.gemm(A, Bt)
+    _check(dx.cpu().numpy(), ref, absum, bf16=False)
+    r_sdy = orc.rht_quantize(dy, mask, mode=orc.SR, seed=seed ^ 0x9E3779B97F4A7C15)
+    r_sx = orc.rht_quantize(x, mask, mode=orc.RNE)
+    A2 = orc.dequantize(r_sdy, N, T)
+    B2 = orc.dequantize(r_sx, Kh, T)
+    ref2, absum2 = orc.gemm(A2, B2)
+    _check(dw.cpu().numpy(), ref2, absum2, bf16=False)
+    # the RHT is orthogonal: the wgrad of the transformed operands estimates dY^T X
+    exact = dy.double().T @ x.double()
+    rel = np.linalg.norm(dw.cpu().double().numpy() - exact.numpy()) / np.linalg.norm(exact.numpy())
+    assert rel < 0.25
+
+
+@pytest.mark.parametrize("fp32", [False, True])
+def test_grouped_gemm(B, orc, fp32):
+    K, n = 256, 304          # last N tile ragged; its second 128-row scale block is absent
+    offsets = np.array([0, 0, 1, 130, 130, 400, 656, 657, 800], dtype=np.int64)   # empty and 1-row groups
+    E = len(offsets) - 1
+    R = int(offsets[-1])
+    a = _rand(R, K, seed=5)
+    g = torch.Generator().manual_seed(6)
+    w = (torch.randn(E, n, K, generator=g) * 0.02 * torch.linspace(0.5, 4, E)[:, None, None]).to(torch.bfloat16)
+    off = torch.from_numpy(offsets).cuda()
+    qa = B.quantize_1d_grouped(a.cuda(), off)
+    qw, _, _ = B.quantize_2d(w.cuda(), want_t=False)
+    out = torch.full((R, n), -3.0, device="cuda",
+                     dtype=torch.float32 if fp32 else torch.bfloat16)
+    B.grouped_gemm(qa, off, qw, n, out_dtype=B.OUT_FP32 if fp32 else B.OUT_BF16, out=out)
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy()
+    ra = orc.quantize_1d_grouped(a, offsets)
+    rw = orc.quantize_2d(w, want_t=False)
+    nsf = orc.sf_bytes(n, K)
+    for e in range(E):
+        o0, o1 = offsets[e], offsets[e + 1]
+        if o1 == o0:
+            continue
+        Ae = orc.dequantize_rows(ra["codes"], ra["sf"], K, float(ra["amax"][e]), np.arange(o0, o1),
+                                 sf_row0=orc.group_sf_row(offsets, e) - int(o0))
+        We = orc.dequantize_rows(rw["codes"][e], rw["sf"][e * nsf:(e + 1) * nsf], K, float(rw["amax"][e]),
+                                 np.arange(n))
+        ref, absum = orc.gemm(Ae, We)
+        _check(o[o0:o1], ref, absum, bf16=not fp32)
+
+
+def test_grouped_gemm_leaves_rows_outside_groups(B):
+    K, n = 64, 256
+    offsets = torch.tensor([0, 100, 100], dtype=torch.int64)
+    a = _rand(160, K, seed=8).cuda()
+    w = _rand(2 * n, K, seed=9).reshape(2, n, K).cuda()
+    off = offsets.cuda()
+    qa = B.quantize_1d_grouped(a, off)
+    qw, _, _ = B.quantize_2d(w, want_t=False)
+    out = torch.full((160, n), 5.0, device="cuda", dtype=torch.float32)
+    B.grouped_gemm(qa, off, qw, n, out_dtype=B.OUT_FP32, out=out)
+    torch.cuda.synchronize()
+    assert (out[100:] == 5.0).all()
+    assert B.device_status() == 0
+
+
+def test_wait_timeout_is_reported_not_hung(B):
+    """A bounded wait that nothing completes returns and records a timeout
+    in the device status word; the context stays usable."""
+    assert B.device_status() == 0
+    B.debug_wait_timeout(50_000_000)          # 50 ms
+    assert B.device_status() & B.DEV_TIMEOUT
+    assert B.device_status() == 0             # read clears
+    x = torch.ones(16, 16, dtype=torch.bfloat16, device="cuda")
+    q = B.quantize_1d(x)
+    torch.cuda.synchronize()
+    assert np_u8(q.amax)[0] == 1.0

@@ -1,0 +1,137 @@
+"""GPU parity of the quantisers against the CPU oracle, bit for bit: packed
+codes, the whole swizzled scale buffer (padding included) and the FP32 amax.
+Shapes span several warps and CTAs, ragged row counts (not multiples of 128),
+scale-column padding (cols/16 not a multiple of 4), empty and one-row
+groups, and the degenerate all-zero tensor."""
+import numpy as np
+import pytest
+import torch
+
+from parity import np_u8, sf_rows_region
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from nvfp4_precision_02_b300 import binding, build
+    build.build()
+    binding.lib()
+    assert torch.cuda.is_available()
+    return binding
+
+
+def _x(rows, cols, seed, scale=1.0, spread=0.0):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(rows, cols, generator=g) * scale
+    if spread:
+        x = x * torch.exp(torch.rand(rows, 1, generator=g) * spread - spread / 2)
+    return x.to(torch.bfloat16)
+
+
+def _same(gpu_q, ref, rows, cols, check_amax=True):
+    assert (np_u8(gpu_q.codes).reshape(ref["codes"].shape) == ref["codes"]).all(), "codes differ"
+    assert (np_u8(gpu_q.sf) == ref["sf"]).all(), "scales differ"
+    if check_amax:
+        assert np_u8(gpu_q.amax)[0] == np.float32(ref["amax"]), "amax differs"
+
+
+SHAPES_1D = [(1, 16), (15, 32), (128, 64), (129, 1040), (300, 256), (257, 48), (1000, 2048)]
+
+
+@pytest.mark.parametrize("rows,cols", SHAPES_1D)
+@pytest.mark.parametrize("mode", [0, 1])
+def test_quantize_1d(B, orc, rows, cols, mode):
+    x = _x(rows, cols, seed=rows * 7 + cols, spread=8.0)
+    seed = 0xDEADBEEF12345 + rows
+    q = B.quantize_1d(x.cuda(), mode=mode, seed=seed)
+    torch.cuda.synchronize()
+    _same(q, orc.quantize_1d(x, mode=mode, seed=seed), rows, cols)
+
+
+def test_quantize_1d_supplied_amax_and_ld(B, orc):
+    x = _x(200, 96, seed=3)
+    big = torch.zeros(200, 128, dtype=torch.bfloat16)
+    big[:, :96] = x
+    xg = big.cuda()[:, :96]                                  # ld = 128 > cols
+    amax_in = torch.tensor([7.5], device="cuda")
+    q = B.quantize_1d(xg, mode=1, seed=9, amax_in=amax_in)
+    torch.cuda.synchronize()
+    _same(q, orc.quantize_1d(x, mode=1, seed=9, amax_in=7.5), 200, 96)
+
+
+def test_quantize_1d_zero_tensor_and_denormals(B, orc):
+    z = torch.zeros(130, 64, dtype=torch.bfloat16)
+    q = B.quantize_1d(z.cuda())
+    torch.cuda.synchronize()
+    _same(q, orc.quantize_1d(z), 130, 64)
+    assert (np_u8(q.codes) == 0).all() and (np_u8(q.sf) == 0).all()
+    # tiny (subnormal bf16) and large magnitudes in one tensor: underflowing blocks
+    x = _x(64, 64, seed=5)
+    x[:8] = (torch.randn(8, 64) * 1e-39).to(torch.bfloat16)
+    x[8:16] = (torch.randn(8, 64) * 3e4).to(torch.bfloat16)
+    for mode in (0, 1):
+        q = B.quantize_1d(x.cuda(), mode=mode, seed=1)
+        torch.cuda.synchronize()
+        _same(q, orc.quantize_1d(x, mode=mode, seed=1), 64, 64)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_quantize_1d_grouped(B, orc, mode):
+    cols = 80
+    offsets = np.array([0, 0, 5, 6, 140, 140, 400, 401, 700], dtype=np.int64)   # empty, 1-row groups
+    scales = np.array([1, 1, 3, 0.01, 1, 7, 1e-3, 2.0])
+    rows = int(offsets[-1])
+    x = (_x(rows, cols, seed=11).float() * torch.from_numpy(np.repeat(scales, np.diff(offsets))).float()[:, None]).to(torch.bfloat16)
+    off = torch.from_numpy(offsets).cuda()
+    q = B.quantize_1d_grouped(x.cuda(), off, mode=mode, seed=77)
+    torch.cuda.synchronize()
+    ref = orc.quantize_1d_grouped(x, offsets, mode=mode, seed=77)
+    assert (np_u8(q.codes) == ref["codes"]).all()
+    used = orc.group_sf_row(offsets, len(offsets) - 1)
+    assert (sf_rows_region(np_u8(q.sf), used, cols) == sf_rows_region(ref["sf"], used, cols)).all()
+    assert (np_u8(q.amax) == ref["amax"]).all()
+
+
+SHAPES_2D = [(1, 16, 16), (1, 48, 80), (1, 128, 256), (1, 144, 1040), (3, 32, 64), (2, 2688 // 8, 1024 // 8)]
+
+
+@pytest.mark.parametrize("batch,rows,cols", SHAPES_2D)
+def test_quantize_2d(B, orc, batch, rows, cols):
+    g = torch.Generator().manual_seed(rows + cols + batch)
+    w = (torch.randn(batch, rows, cols, generator=g) * 0.02 *
+         torch.exp(torch.rand(batch, rows, cols, generator=g) * 6 - 3)).to(torch.bfloat16)
+    qw, qt, tile = B.quantize_2d(w.cuda(), want_t=True, want_tile_sf=True)
+    torch.cuda.synchronize()
+    ref = orc.quantize_2d(w)
+    assert (np_u8(qw.codes).reshape(ref["codes"].shape) == ref["codes"]).all()
+    assert (np_u8(qw.sf) == ref["sf"]).all()
+    assert (np_u8(qt.codes).reshape(ref["codes_t"].shape) == ref["codes_t"]).all()
+    assert (np_u8(qt.sf) == ref["sf_t"]).all()
+    assert (np_u8(tile) == ref["tile_sf"]).all()
+    assert (np_u8(qw.amax) == ref["amax"]).all()
+
+
+@pytest.mark.parametrize("tokens,cols", [(16, 1), (64, 24), (80, 130), (1024, 300), (48, 8)])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rht_quantize(B, orc, tokens, cols, mode):
+    x = _x(tokens, cols, seed=tokens * 3 + cols, spread=4.0)
+    mask = 0xB5A3 ^ tokens
+    q = B.rht_quantize(x.cuda(), mask, mode=mode, seed=1234567)
+    a = B.rht_amax(x.cuda(), mask)
+    torch.cuda.synchronize()
+    ref = orc.rht_quantize(x, mask, mode=mode, seed=1234567)
+    _same(q, ref, cols, tokens)
+    assert np_u8(a)[0] == np.float32(ref["amax"])
+
+
+def test_amax_batched(B, orc):
+    w = _x(3 * 48, 64, seed=2).reshape(3, 48, 64)
+    a = B.amax(w.cuda())
+    torch.cuda.synchronize()
+    for b in range(3):
+        assert np_u8(a)[b] == np.float32(orc.amax(w[b]))
+
+
+def test_device_status_clean(B):
+    assert B.device_status() == 0
