@@ -367,15 +367,26 @@ def main():
     return 0
 
 
+def host_mem_available() -> int:
+    """MemAvailable of /proc/meminfo in bytes (0 if unreadable)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
 def measure_e2e(wk: Workload, steps: int, dev):
     """Same metric through the public API with host buffers: every step copies
     all inputs from pinned host memory, runs the step and reads every output
     back.  Skipped (None) when pinned host memory for it is not available."""
-    import psutil
     import torch
     in_bytes = sum(t.numel() * t.element_size() for t in wk.input_tensors)
     out_bytes = sum(t.numel() * t.element_size() for t in wk.output_tensors)
-    avail = psutil.virtual_memory().available
+    avail = host_mem_available()
     if avail < 2 * (in_bytes + out_bytes):
         return {"value": None, "unit": "TFLOP/s", "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                 "skipped": f"needs {2 * (in_bytes + out_bytes) / 1e9:.0f} GB free host memory, {avail / 1e9:.0f} GB available"}
