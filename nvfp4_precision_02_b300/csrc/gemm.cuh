@@ -9,18 +9,29 @@
 // LatentMoE routed-expert GEMM ("Nemotron 3 Super" summary,
 // papers.lianghsun.dev, section 2.2).
 //
-// Design (one CTA per SM, persistent over output tiles):
-//   tile 128 x 256, K stage 256 FP4 elements (128 B per row, 128B-swizzled
-//   TMA boxes), 4 stages of A 16 KB + B 32 KB + scales 6 KB in shared memory.
-//   warp 0      TMA producer: A and B boxes by cp.async.bulk.tensor, the scale
-//               atoms (512 B each, already in the 128x4 layout) by cp.async.bulk
-//   warp 1      allocates TMEM; one lane copies the stage's scales into TMEM
-//               (tcgen05.cp 32x128b.warpx4) and issues 4 MMAs 128x256x64
-//   warps 2..9  epilogue: tcgen05.ld the 128x256 FP32 accumulator (two warps
-//               per TMEM lane quarter, 128 columns each), release it to the
-//               MMA warp, scale by alpha, round, store rows to global memory
+// Design (one CTA per SM, persistent over output tiles of 128 x 256):
+//   K stage 256 FP4 elements (128 B per row, 128B-swizzled TMA boxes);
+//   4 stages of A 16 KB + B 32 KB + scales 6 KB in shared memory.
+//   warp 0        TMA producer: A and B boxes by cp.async.bulk.tensor, the
+//                 scale atoms (512 B each, already in the 128x4 layout) by
+//                 cp.async.bulk
+//   warp 1        allocates TMEM; one lane issues the 4 MMAs 128x256x64 of a
+//                 stage from one asm block (descriptors advanced in place)
+//   warps 2..5    scale-factor writers, one per TMEM lane quarter: when a
+//                 stage lands, each lane reads the 16 bytes it owns of every
+//                 128x4 scale atom from shared memory and writes them into
+//                 TMEM with tcgen05.st.  In every quarter, column j of an
+//                 atom's 4 columns then holds rows 32j .. 32j+31 (the same
+//                 replicated layout a 32x128b.warpx4 copy would produce),
+//                 which is where the block-scaled MMA reads its scales.
+//   warps 6..21   epilogue: four warps per TMEM lane quarter, 64 accumulator
+//                 columns each; tcgen05.ld, release the accumulator to the
+//                 MMA warp, scale by alpha, round, store to global memory.
 //   TMEM: accumulator columns 0..255; per stage 16 columns of A scales and
 //   32 columns of B scales from column 256.
+//   Moving the scales with tcgen05.st from dedicated warps keeps them off
+//   the MMA issue thread: measured on B300, a tcgen05.cp per 512-byte atom
+//   cost as much tensor time as half an MMA.
 // Every wait is bounded (DEV_TIMEOUT in the status word, then a clean exit).
 #pragma once
 
@@ -34,19 +45,22 @@ constexpr int G_BM = 128, G_BN = 256, G_BK = 256;
 constexpr int G_STAGES = 4;
 constexpr int G_A_BYTES = G_BM * G_BK / 2;                 // 16384
 constexpr int G_B_BYTES = G_BN * G_BK / 2;                 // 32768
-constexpr int G_SFA_BYTES = (G_BK / 64) * 512;             // 2048
-constexpr int G_SFB_BYTES = 2 * (G_BK / 64) * 512;         // 4096
+constexpr int G_SFA_BYTES = (G_BK / 64) * 512;             // 2048: 4 atoms of A scales
+constexpr int G_SFB_BYTES = 2 * (G_BK / 64) * 512;         // 4096: 2 row blocks x 4 atoms of B scales
 constexpr int G_STAGE_BYTES = G_A_BYTES + G_B_BYTES + G_SFA_BYTES + G_SFB_BYTES;  // 55296
-constexpr int G_THREADS = 320;
+constexpr int G_W_TMA = 0, G_W_MMA = 1, G_W_SF0 = 2, G_W_EPI0 = 6;
+constexpr int G_EPI_WARPS = 16;
+constexpr int G_THREADS = (G_W_EPI0 + G_EPI_WARPS) * 32;   // 704
 constexpr int G_TMEM_COLS = 512;
 constexpr int G_SF_COL0 = 256;
 constexpr int G_SF_COLS_PER_STAGE = 48;
 constexpr int G_BAND = 16;                                   // m-tiles per raster band
 constexpr uint64_t G_WAIT_NS = 4000000000ull;                // bounded waits: 4 s
+constexpr int G_BAR_BYTES = 256;                             // barriers, TMEM slot, abort flag
 
 // dynamic shared memory: 1 KB alignment slack, stages, barriers, tables
 __host__ __device__ constexpr int gemm_smem_bytes(int groups) {
-    return 1024 + G_STAGES * G_STAGE_BYTES + 128 + 2 * 4 * (groups + 1);
+    return 1024 + G_STAGES * G_STAGE_BYTES + G_BAR_BYTES + 2 * 4 * (groups + 1);
 }
 
 struct GemmParams {
@@ -152,9 +166,6 @@ __host__ __device__ constexpr uint32_t mxf4nvf4_idesc(int m, int n) {
     return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
 
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                        uint32_t sfb, uint32_t accumulate) {
@@ -177,8 +188,64 @@ __device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t* v) {
 }
 #undef NVFP4_R32
 
+#define NVFP4_R16(i) "=r"(v[i]), "=r"(v[i + 1]), "=r"(v[i + 2]), "=r"(v[i + 3])
+__device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t* v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15}, [%16];"
+        : NVFP4_R16(0), NVFP4_R16(4), NVFP4_R16(8), NVFP4_R16(12)
+        : "r"(taddr));
+}
+#undef NVFP4_R16
+
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+
+// Four K=64 MMAs covering one 256-wide K stage.  The shared-memory
+// descriptors advance by 32 bytes (2 in descriptor units) per MMA inside the
+// 128-byte swizzle atom; scale columns advance by 4 (A) and 8 (B).  Only the
+// first MMA may start a fresh accumulator.
+__device__ __forceinline__ void tc_mma4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                        uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        ".reg .b32 sa1, sa2, sa3, sb1, sb2, sb3;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.u32 t, 0, 0;\n\t"
+        "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+        "add.u32 sa1, %5, 4;\n\tadd.u32 sa2, %5, 8;\n\tadd.u32 sa3, %5, 12;\n\t"
+        "add.u32 sb1, %6, 8;\n\tadd.u32 sb2, %6, 16;\n\tadd.u32 sb3, %6, 24;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [sa1], [sb1], t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a2, b2, %3, [sa2], [sb2], t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a3, b3, %3, [sa3], [sb3], t;\n\t}"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+
+// tcgen05.st of 16 / 32 consecutive 32-bit columns into this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tc_st_x16(uint32_t taddr, const uint4 (&v)[4]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z), "r"(v[1].w),
+        "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y), "r"(v[3].z), "r"(v[3].w)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_st_x32(uint32_t taddr, const uint4 (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z), "r"(v[1].w),
+        "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y), "r"(v[3].z), "r"(v[3].w),
+        "r"(v[4].x), "r"(v[4].y), "r"(v[4].z), "r"(v[4].w), "r"(v[5].x), "r"(v[5].y), "r"(v[5].z), "r"(v[5].w),
+        "r"(v[6].x), "r"(v[6].y), "r"(v[6].z), "r"(v[6].w), "r"(v[7].x), "r"(v[7].y), "r"(v[7].z), "r"(v[7].w)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // ------------------------------------------------------------------ tiles
 struct TileCoord {
     int g;            // group
@@ -213,6 +280,8 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int mtiles, int ntil
     return c;
 }
 
+__device__ __forceinline__ uint4 ldg_u4(const uint8_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
 // ------------------------------------------------------------------ kernel
 template <bool OUT_FP32>
 __global__ void __launch_bounds__(G_THREADS, 1)
@@ -222,34 +291,35 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G_STAGES * G_STAGE_BYTES);
-    // bars: full[4], empty[4], acc_full, acc_empty, drain
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G_STAGES + 3);
+    // bars: full[S], empty[S], sf_full[S], acc_full, acc_empty, drain
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * G_STAGES + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int32_t* tab = reinterpret_cast<int32_t*>(smem + G_STAGES * G_STAGE_BYTES + 128);
+    int32_t* tab = reinterpret_cast<int32_t*>(smem + G_STAGES * G_STAGE_BYTES + G_BAR_BYTES);
     const int groups = p.groups;
     GroupTables gt{tab, tab + groups + 1};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + G_STAGES);
-    const uint32_t acc_full = smem_u32(bars + 2 * G_STAGES), acc_empty = acc_full + 8, drain = acc_full + 16;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + G_STAGES), sff0 = smem_u32(bars + 2 * G_STAGES);
+    const uint32_t acc_full = smem_u32(bars + 3 * G_STAGES), acc_empty = acc_full + 8, drain = acc_full + 16;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < G_STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
+            mbar_init(sff0 + 8 * s, 4);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 8);
+        mbar_init(acc_empty, G_EPI_WARPS);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == G_W_TMA && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_a)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b)) : "memory");
     }
-    if (warp == 1) {
+    if (warp == G_W_MMA) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(G_TMEM_COLS)
                      : "memory");
@@ -276,13 +346,11 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int nrb = (int)((p.N + 127) / 128);            // 128-row scale blocks of one B operand
     const int64_t b_rows_per_group = (p.offsets != nullptr) ? p.N : 0;
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+    if (warp == G_W_TMA) {
+        // ------------------------------------------------ TMA producer (A, B)
         if (lane == 0) {
             int s = 0;
-            uint32_t ph = 0;
-            int32_t issued_ph[G_STAGES];
-            for (int i = 0; i < G_STAGES; ++i) issued_ph[i] = -1;
+            uint32_t ph = 0, issued = 0, issued_ph = 0;   // per-stage bits: ever issued, parity of last issue
             bool ok = true;
             for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const TileCoord tc = decode_tile(t, mtiles, ntiles, gt.off, gt.pad, groups);
@@ -298,13 +366,14 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     const uint32_t st = smem_u32(stages + s * G_STAGE_BYTES);
                     tma_load_2d(st, &tm_a, ks * 128, tc.row0, bar);
                     tma_load_2d(st + G_A_BYTES, &tm_b, ks * 128, brow0, bar);
-                    bulk_load(st + G_A_BYTES + G_B_BYTES, p.sfa + ((int64_t)tc.mtg * katoms + 4 * ks) * 512, sfbytes, bar);
-                    bulk_load(st + G_A_BYTES + G_B_BYTES + G_SFA_BYTES,
-                              sfb_g + ((int64_t)(tc.nt * 2) * katoms + 4 * ks) * 512, sfbytes, bar);
+                    const uint32_t ssf = st + G_A_BYTES + G_B_BYTES;
+                    bulk_load(ssf, p.sfa + ((int64_t)tc.mtg * katoms + 4 * ks) * 512, sfbytes, bar);
+                    bulk_load(ssf + G_SFA_BYTES, sfb_g + ((int64_t)(tc.nt * 2) * katoms + 4 * ks) * 512, sfbytes, bar);
                     if (rb2)
-                        bulk_load(st + G_A_BYTES + G_B_BYTES + G_SFA_BYTES + 2048,
-                                  sfb_g + ((int64_t)(tc.nt * 2 + 1) * katoms + 4 * ks) * 512, sfbytes, bar);
-                    issued_ph[s] = (int32_t)ph;
+                        bulk_load(ssf + G_SFA_BYTES + 2048, sfb_g + ((int64_t)(tc.nt * 2 + 1) * katoms + 4 * ks) * 512,
+                                  sfbytes, bar);
+                    issued |= 1u << s;
+                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                     if (++s == G_STAGES) { s = 0; ph ^= 1u; }
                 }
             }
@@ -312,10 +381,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 // let every copy already issued land before the CTA exits
                 volatile int never = 0;
                 for (int i = 0; i < G_STAGES; ++i)
-                    if (issued_ph[i] >= 0) mbar_wait(full0 + 8 * i, (uint32_t)issued_ph[i], &never);
+                    if ((issued >> i) & 1u) mbar_wait(full0 + 8 * i, (issued_ph >> i) & 1u, &never);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == G_W_MMA) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = mxf4nvf4_idesc(G_BM, G_BN);
@@ -323,29 +392,26 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             uint32_t ph = 0, it = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-                const TileCoord tc = decode_tile(t, mtiles, ntiles, gt.off, gt.pad, groups);
-                const bool rb2 = (tc.nt * 2 + 1) < nrb;
-                (void)tc;
                 if (!mbar_wait(acc_empty, (it & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 for (int ks = 0; ks < kstages; ++ks) {
-                    if (!mbar_wait(full0 + 8 * s, ph, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(full0 + 8 * s, ph, abort_flag) || !mbar_wait(sff0 + 8 * s, ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     const int na = min(4, katoms - 4 * ks);
                     const uint32_t st = smem_u32(stages + s * G_STAGE_BYTES);
                     const uint32_t sfa_t = tmem + G_SF_COL0 + s * G_SF_COLS_PER_STAGE;
                     const uint32_t sfb_t = sfa_t + 16;
-                    for (int j = 0; j < na; ++j) {
-                        tc_cp_sf(sfa_t + 4 * j, smem_desc(st + G_A_BYTES + G_B_BYTES + 512 * j, 0, 128, 0));
-                        tc_cp_sf(sfb_t + 8 * j, smem_desc(st + G_A_BYTES + G_B_BYTES + G_SFA_BYTES + 512 * j, 0, 128, 0));
-                        if (rb2)
-                            tc_cp_sf(sfb_t + 8 * j + 4,
-                                     smem_desc(st + G_A_BYTES + G_B_BYTES + G_SFA_BYTES + 2048 + 512 * j, 0, 128, 0));
-                    }
-                    for (int j = 0; j < na; ++j) {
-                        const uint64_t ad = smem_desc(st + 32 * j, 16, 1024, 2);
-                        const uint64_t bd = smem_desc(st + G_A_BYTES + 32 * j, 16, 1024, 2);
-                        tc_mma(tmem, ad, bd, idesc, sfa_t + 4 * j, sfb_t + 8 * j, (ks | j) != 0 ? 1u : 0u);
+                    const uint64_t ad = smem_desc(st, 16, 1024, 2);
+                    const uint64_t bd = smem_desc(st + G_A_BYTES, 16, 1024, 2);
+                    if (na == 4) {
+                        tc_mma4(tmem, ad, bd, idesc, sfa_t, sfb_t, ks != 0 ? 1u : 0u);
+                    } else {
+                        for (int j = 0; j < na; ++j)
+                            tc_mma(tmem, ad + 2 * j, bd + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 8 * j,
+                                   (ks | j) != 0 ? 1u : 0u);
                     }
                     tc_commit(empty0 + 8 * s);
                     if (++s == G_STAGES) { s = 0; ph ^= 1u; }
@@ -358,64 +424,123 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             volatile int never = 0;
             mbar_wait(drain, 0, &never);
         }
+    } else if (warp < G_W_EPI0) {
+        // ------------------------------------------------ scale factors -> TMEM
+        // The producer lands the stage's scale atoms in shared memory next to
+        // A and B.  Lane i of every quarter copies the 16 bytes at offset 16*i
+        // of each 512-byte atom (the 4 scales of rows i, i+32, i+64, i+96) into
+        // the atom's 4 TMEM columns.  The stage's TMEM columns are free once
+        // its data has landed: the producer refilled it only after the MMAs of
+        // its previous use completed.
+        const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const TileCoord tc = decode_tile(t, mtiles, ntiles, gt.off, gt.pad, groups);
+            const bool rb2 = (tc.nt * 2 + 1) < nrb;
+            for (int ks = 0; ks < kstages; ++ks) {
+                const int na = min(4, katoms - 4 * ks);
+                if (!mbar_wait(full0 + 8 * s, ph, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint8_t* ssf = stages + s * G_STAGE_BYTES + G_A_BYTES + G_B_BYTES + lane * 16;
+                uint4 va[4], vb[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = j < na;
+                    va[j] = in ? *reinterpret_cast<const uint4*>(ssf + 512 * j) : make_uint4(0, 0, 0, 0);
+                    vb[2 * j] = in ? *reinterpret_cast<const uint4*>(ssf + G_SFA_BYTES + 512 * j) : make_uint4(0, 0, 0, 0);
+                    vb[2 * j + 1] = (in && rb2) ? *reinterpret_cast<const uint4*>(ssf + G_SFA_BYTES + 2048 + 512 * j)
+                                                : make_uint4(0, 0, 0, 0);
+                }
+                const uint32_t col = (uint32_t)(G_SF_COL0 + s * G_SF_COLS_PER_STAGE);
+                tc_st_x16(tq + col, va);
+                tc_st_x32(tq + col + 16, vb);
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sff0 + 8 * s);
+                if (++s == G_STAGES) { s = 0; ph ^= 1u; }
+            }
+        }
     } else {
         // ------------------------------------------------ epilogue
-        const int q = warp & 3;                  // TMEM lane quarter this warp may access
-        const int h = (warp - 2) >> 2;           // column half
-        const int r = q * 32 + lane;             // row inside the tile
+        const int q = warp & 3;                          // TMEM lane quarter this warp may access
+        const int chunk = (warp - G_W_EPI0) >> 2;        // 64-column chunk of the tile
+        const int r = q * 32 + lane;                     // row inside the tile
         uint32_t it = 0;
         for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++it) {
             const TileCoord tc = decode_tile(t, mtiles, ntiles, gt.off, gt.pad, groups);
             const float alpha = __fmul_rn(tensor_decode_scale(p.amax_a[tc.g]), tensor_decode_scale(p.amax_b[tc.g]));
             if (!mbar_wait(acc_full, it & 1u, abort_flag)) break;
             tc_fence_after();
-            uint32_t v[128];
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
-            tc_ld_32x32b_x32(taddr, v);
-            tc_ld_32x32b_x32(taddr + 32, v + 32);
-            tc_ld_32x32b_x32(taddr + 64, v + 64);
-            tc_ld_32x32b_x32(taddr + 96, v + 96);
-            tc_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
-            if (r < tc.rows) {
-                const int64_t row = tc.row0 + r;
-                const int64_t col0 = (int64_t)tc.nt * G_BN + h * 128;
-                if (OUT_FP32) {
-                    float* out = reinterpret_cast<float*>(p.c) + row * p.ldc + col0;
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(chunk * 64);
+            const int64_t row = tc.row0 + r;
+            const int64_t col0 = (int64_t)tc.nt * G_BN + chunk * 64;
+            if (OUT_FP32) {
+                // two 32-column halves: load, scale, store; release after the second load
+                const bool live = r < tc.rows && col0 < p.N;
+                float* out = reinterpret_cast<float*>(p.c) + row * p.ldc + col0;
 #pragma unroll
-                    for (int i = 0; i < 128; i += 4) {
-                        const float4 o = make_float4(__fmul_rn(alpha, __uint_as_float(v[i])),
-                                                     __fmul_rn(alpha, __uint_as_float(v[i + 1])),
-                                                     __fmul_rn(alpha, __uint_as_float(v[i + 2])),
-                                                     __fmul_rn(alpha, __uint_as_float(v[i + 3])));
-                        if (p.vec_store && col0 + i + 4 <= p.N) {
-                            *reinterpret_cast<float4*>(out + i) = o;
-                        } else {
-                            const float oo[4] = {o.x, o.y, o.z, o.w};
-                            for (int j = 0; j < 4; ++j)
-                                if (col0 + i + j < p.N) out[i + j] = oo[j];
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[32];
+                    tc_ld_32x32b_x32(taddr + 32 * h, v);
+                    tc_wait_ld();
+                    if (h == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty);
+                    }
+                    if (live) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const int cc = 32 * h + i;
+                            const float4 o = make_float4(__fmul_rn(alpha, __uint_as_float(v[i])),
+                                                         __fmul_rn(alpha, __uint_as_float(v[i + 1])),
+                                                         __fmul_rn(alpha, __uint_as_float(v[i + 2])),
+                                                         __fmul_rn(alpha, __uint_as_float(v[i + 3])));
+                            if (p.vec_store && col0 + cc + 4 <= p.N) {
+                                *reinterpret_cast<float4*>(out + cc) = o;
+                            } else {
+                                const float oo[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    if (col0 + cc + j < p.N) out[cc + j] = oo[j];
+                            }
                         }
                     }
-                } else {
-                    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.c) + row * p.ldc + col0;
+                }
+            } else {
+                // four 16-column pieces: load, scale, round, store; release after the last load
+                const bool live = r < tc.rows && col0 < p.N;
+                uint16_t* out = reinterpret_cast<uint16_t*>(p.c) + row * p.ldc + col0;
 #pragma unroll
-                    for (int i = 0; i < 128; i += 8) {
-                        uint32_t w[4];
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t v[16], w[8];
+                    tc_ld_32x32b_x16(taddr + 16 * h, v);
+                    tc_wait_ld();
+                    if (h == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty);
+                    }
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                                __fmul_rn(alpha, __uint_as_float(v[i + 2 * j])),
-                                __fmul_rn(alpha, __uint_as_float(v[i + 2 * j + 1])));
-                            w[j] = *reinterpret_cast<const uint32_t*>(&b2);
-                        }
-                        if (p.vec_store && col0 + i + 8 <= p.N) {
-                            *reinterpret_cast<uint4*>(out + i) = make_uint4(w[0], w[1], w[2], w[3]);
-                        } else {
-                            const uint16_t* hw = reinterpret_cast<const uint16_t*>(w);
-                            for (int j = 0; j < 8; ++j)
-                                if (col0 + i + j < p.N) reinterpret_cast<uint16_t*>(out)[i + j] = hw[j];
+                    for (int j = 0; j < 8; ++j) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(v[2 * j])),
+                                                                        __fmul_rn(alpha, __uint_as_float(v[2 * j + 1])));
+                        w[j] = *reinterpret_cast<const uint32_t*>(&b2);
+                    }
+                    if (live) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 8) {
+                            const int cc = 16 * h + i;
+                            if (p.vec_store && col0 + cc + 8 <= p.N) {
+                                *reinterpret_cast<uint4*>(out + cc) = make_uint4(w[i / 2], w[i / 2 + 1], w[i / 2 + 2], w[i / 2 + 3]);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    if (col0 + cc + j < p.N) out[cc + j] = (uint16_t)(w[(i + j) / 2] >> (16 * ((i + j) & 1)));
+                            }
                         }
                     }
                 }
@@ -425,7 +550,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == G_W_MMA) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(G_TMEM_COLS) : "memory");
     }
