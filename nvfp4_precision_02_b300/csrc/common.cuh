@@ -69,38 +69,59 @@ __device__ __forceinline__ float element_ratio(float s_enc, uint32_t sf) {
     return __fdiv_rn(s_enc, e4m3_to_float(sf));
 }
 
-// E2M1 magnitude index (0..7) of m >= 0 with round-to-nearest-even and
-// saturation: the decision points are the grid midpoints; a midpoint goes
-// to the even index (0.25->0, 0.75->1.0, 1.25->1.0, 1.75->2, 2.5->2,
-// 3.5->4, 5->4).
-__device__ __forceinline__ uint32_t e2m1_rne_mag(float m) {
-    return (uint32_t)(m > 0.25f) + (uint32_t)(m >= 0.75f) + (uint32_t)(m > 1.25f) +
-           (uint32_t)(m >= 1.75f) + (uint32_t)(m > 2.5f) + (uint32_t)(m >= 3.5f) +
-           (uint32_t)(m > 5.0f);
+// Eight E2M1 codes (round to nearest even, saturating at 6, sign copied)
+// of f[0..7], element j in nibble j, by the hardware conversion
+// cvt.rn.satfinite.e2m1x2.f32 (its first source goes to the high nibble).
+// The GPU parity tests compare it with the oracle's nearest-value search,
+// ties and signed zeros included.
+__device__ __forceinline__ uint32_t e2m1x8_rne(const float (&f)[8]) {
+    uint32_t out;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(out)
+        : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]));
+    return out;
 }
 
-// E2M1 code (sign << 3 | magnitude) of v with RNE; the sign is copied.
-__device__ __forceinline__ uint32_t e2m1_rne(float v) {
-    return ((__float_as_uint(v) >> 28) & 8u) | e2m1_rne_mag(fabsf(v));
-}
-
-// E2M1 code of v with stochastic rounding by the 32-bit word u: with grid
-// neighbours lo <= |v| < hi, p = (|v| - lo) / (hi - lo) (the gaps are powers
-// of two, so the product with the reciprocal below is the exact quotient),
-// and the magnitude rounds up iff (u >> 8) < p * 2^24.
+// E2M1 code of v with stochastic rounding by the 32-bit word u.  With grid
+// neighbours lo <= |v| < hi and p = (|v| - lo) / (hi - lo), the magnitude
+// rounds up iff (u >> 8) < p * 2^24, i.e. iff u < 256 * ceil(p * 2^24).
+// That bound is formed from the FP32 bits of |v| with integer operations:
+//   |v| in [1, 6):   lo index 2 + 2e + (mantissa >= 1/2), bound = low 22
+//                    mantissa bits << 10 (the gap is 2^(e-1));
+//   |v| in [0.5, 1): lo index 1, bound = mantissa << 9 (gap 1/2);
+//   |v| in [0, 0.5): lo index 0, bound = 256 * ceil(|v| * 2^25).
+// It equals the FP32 statement above for every finite input (checked
+// exhaustively over all FP32 bit patterns below 6 on the host).
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u) {
-    const uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
-    const float m = fabsf(v);
-    if (m >= 6.0f) return sign | 7u;
-    uint32_t c = (uint32_t)(m >= 0.5f) + (uint32_t)(m >= 1.0f) + (uint32_t)(m >= 1.5f) +
-                 (uint32_t)(m >= 2.0f) + (uint32_t)(m >= 3.0f) + (uint32_t)(m >= 4.0f);
-    // lo and 1/(hi - lo) for c = 0..6
-    const float lo = (c < 4) ? __fmul_rn((float)c, 0.5f) : (c == 4 ? 2.0f : (c == 5 ? 3.0f : 4.0f));
-    const float inv_gap = (c < 4) ? 2.0f : (c < 6 ? 1.0f : 0.5f);
-    const float p = __fmul_rn(__fsub_rn(m, lo), inv_gap);
-    const float thr = __fmul_rn(p, 16777216.0f);
-    c += (__uint2float_rn(u >> 8) < thr) ? 1u : 0u;
-    return sign | c;
+    const uint32_t bits = __float_as_uint(v);
+    const uint32_t sign = (bits >> 28) & 8u;
+    const uint32_t mb = bits & 0x7FFFFFFFu;
+    if (mb >= 0x40C00000u) return sign | 7u;                       // |v| >= 6
+    uint32_t c, thr;
+    if (mb >= 0x3F800000u) {
+        c = 2u + 2u * ((mb >> 23) - 127u) + ((mb >> 22) & 1u);
+        thr = (mb & 0x3FFFFFu) << 10;
+    } else if (mb >= 0x3F000000u) {
+        c = 1u;
+        thr = (mb & 0x7FFFFFu) << 9;
+    } else {
+        const uint32_t ef = mb >> 23;
+        uint32_t x;
+        if (mb == 0u) x = 0u;
+        else if (ef <= 101u) x = 1u;                                // |v| * 2^25 < 1
+        else {
+            const uint32_t sh = 125u - ef;
+            x = (((mb & 0x7FFFFFu) | 0x800000u) + (1u << sh) - 1u) >> sh;
+        }
+        c = 0u;
+        thr = x << 8;
+    }
+    return sign | (c + (u < thr ? 1u : 0u));
 }
 
 // ------------------------------------------------------------------ Philox

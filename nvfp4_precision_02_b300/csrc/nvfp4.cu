@@ -356,7 +356,7 @@ nvfp4_status nvfp4_rht_amax(const void* x, int64_t tokens, int64_t cols, int64_t
     NVFP4_TRY(check_device());
     NVFP4_TRY(cuda_call(cudaMemsetAsync(amax, 0, sizeof(float), stream), "memset amax"));
     if (tokens == 0 || cols == 0) return NVFP4_OK;
-    k_rht<0><<<dim3((unsigned)cdiv(cols, 128), (unsigned)cdiv(tokens, 64)), 128, 0, stream>>>(
+    k_rht<0><<<dim3((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64)), 256, 0, stream>>>(
         (const uint16_t*)x, tokens, cols, ld, sign_mask, amax, 0, nullptr, nullptr, nullptr);
     return launched("k_rht amax");
 }
@@ -376,7 +376,7 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t tokens, int64_t cols, int
     if (am == nullptr) {
         NVFP4_TRY(cuda_call(cudaMemsetAsync(out_t->amax, 0, sizeof(float), stream), "memset amax"));
         if (tokens > 0 && cols > 0) {
-            k_rht<0><<<dim3((unsigned)cdiv(cols, 128), (unsigned)cdiv(tokens, 64)), 128, 0, stream>>>(
+            k_rht<0><<<dim3((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64)), 256, 0, stream>>>(
                 (const uint16_t*)x, tokens, cols, ld, sign_mask, out_t->amax, 0, nullptr, nullptr, nullptr);
             NVFP4_TRY(launched("k_rht amax"));
         }
@@ -388,12 +388,12 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t tokens, int64_t cols, int
         if (copy) NVFP4_TRY(cuda_call(cudaMemcpyAsync(copy, amax_in, 4, cudaMemcpyDeviceToDevice, stream), "amax copy"));
         return NVFP4_OK;
     }
-    const dim3 grid((unsigned)cdiv(cols, 128), (unsigned)cdiv(tokens, 64));
+    const dim3 grid((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64));
     if (mode == NVFP4_ROUND_SR)
-        k_rht<2><<<grid, 128, 0, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask, const_cast<float*>(am), seed,
+        k_rht<2><<<grid, 256, 0, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask, const_cast<float*>(am), seed,
                                            (uint8_t*)out_t->codes, out_t->sf, copy);
     else
-        k_rht<1><<<grid, 128, 0, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask, const_cast<float*>(am), seed,
+        k_rht<1><<<grid, 256, 0, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask, const_cast<float*>(am), seed,
                                            (uint8_t*)out_t->codes, out_t->sf, copy);
     NVFP4_TRY(launched("k_rht quantize"));
     if (cols % 128 != 0) {

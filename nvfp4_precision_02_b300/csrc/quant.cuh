@@ -228,24 +228,23 @@ template <bool SR>
 __device__ __forceinline__ uint32_t encode8(const uint4 v, float ratio, bool zero, uint64_t seed,
                                             uint64_t e0) {
     if (zero) return 0u;
-    float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                  bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+    const float f[8] = {__fmul_rn(bf16_lo(v.x), ratio), __fmul_rn(bf16_hi(v.x), ratio),
+                        __fmul_rn(bf16_lo(v.y), ratio), __fmul_rn(bf16_hi(v.y), ratio),
+                        __fmul_rn(bf16_lo(v.z), ratio), __fmul_rn(bf16_hi(v.z), ratio),
+                        __fmul_rn(bf16_lo(v.w), ratio), __fmul_rn(bf16_hi(v.w), ratio)};
+    if (!SR) return e2m1x8_rne(f);
+    const uint4 w0 = sr_words(seed, e0 >> 2);
+    const uint4 w1 = sr_words(seed, (e0 >> 2) + 1);
+    const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     uint32_t out = 0;
-    if (SR) {
-        const uint4 w0 = sr_words(seed, e0 >> 2);
-        const uint4 w1 = sr_words(seed, (e0 >> 2) + 1);
-        const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) out |= e2m1_sr(__fmul_rn(f[j], ratio), w[j]) << (4 * j);
-    } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) out |= e2m1_rne(__fmul_rn(f[j], ratio)) << (4 * j);
-    }
+    for (int j = 0; j < 8; ++j) out |= e2m1_sr(f[j], w[j]) << (4 * j);
     return out;
 }
 
 // One warp walks a contiguous range of rows; in each row lane pairs own
-// 16-element blocks (lane 2j: first 8 elements, lane 2j+1: last 8).
+// 16-element blocks (lane 2j: first 8 elements, lane 2j+1: last 8), four
+// 16-byte loads per lane in flight.
 // x: bf16 [rows, cols] (row stride ld); codes [rows, cols/2]; sf swizzled.
 // amax: 1 value (or one per group when GROUPED).  SR index e = r*cols + c.
 template <bool SR, bool GROUPED>
@@ -262,6 +261,7 @@ __global__ void __launch_bounds__(256) k_quant1d(const uint16_t* __restrict__ x,
         const int n = GROUPED ? groups : 1;
         for (int i = threadIdx.x; i < n; i += blockDim.x) amax_copy[i] = amax[i];
     }
+    constexpr int U = 4;                               // 16-byte units per lane per step
     const int lane = threadIdx.x & 31;
     const int upr = (int)(cols >> 3);
     const int64_t nc = cols >> 4, pc = ((nc + 3) >> 2) << 2;
@@ -286,31 +286,29 @@ __global__ void __launch_bounds__(256) k_quant1d(const uint16_t* __restrict__ x,
         const int64_t sr = GROUPED ? sf_row0 + (r - g_begin) : r;
         const uint16_t* row = x + r * ld;
         uint8_t* crow = codes + r * (cols >> 1);
-        for (int base = 0; base < upr; base += 64) {
-            uint4 v[2];
-            bool ok[2];
+        for (int base = 0; base < upr; base += 32 * U) {
+            uint4 v[U];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < U; ++i) {
                 const int u = base + i * 32 + lane;
-                ok[i] = u < upr;
-                v[i] = ok[i] ? __ldg(reinterpret_cast<const uint4*>(row + u * 8)) : make_uint4(0, 0, 0, 0);
+                v[i] = u < upr ? __ldg(reinterpret_cast<const uint4*>(row + u * 8)) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < U; ++i) {
                 const int u = base + i * 32 + lane;
                 uint32_t m = absmax_bits(v[i], 0u);
                 m = max(m & 0xFFFFu, m >> 16);
                 m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
                 const float bamax = __uint_as_float(m << 16);
-                const uint32_t s = block_scale(bamax, s_enc);
-                const float ratio = s ? element_ratio(s_enc, s) : 0.0f;
-                if (ok[i]) {
-                    const uint32_t packed = encode8<SR>(v[i], ratio, s == 0, seed,
+                const uint32_t sc = block_scale(bamax, s_enc);
+                const float ratio = sc ? element_ratio(s_enc, sc) : 0.0f;
+                if (u < upr) {
+                    const uint32_t packed = encode8<SR>(v[i], ratio, sc == 0, seed,
                                                         (uint64_t)r * (uint64_t)cols + (uint64_t)u * 8);
                     *reinterpret_cast<uint32_t*>(crow + u * 4) = packed;
                     if ((lane & 1) == 0) {
                         const int64_t c = u >> 1;
-                        sf[sf_offset(sr, c, cols)] = (uint8_t)s;
+                        sf[sf_offset(sr, c, cols)] = (uint8_t)sc;
                         if (c == nc - 1)
                             for (int64_t cc = nc; cc < pc; ++cc) sf[sf_offset(sr, cc, cols)] = 0;
                     }
@@ -355,82 +353,120 @@ __global__ void __launch_bounds__(256) k_zero_pad_rows(uint8_t* __restrict__ sf,
 }
 
 // ------------------------------------------------------------------ 2D quantise
-// CTA tile 64x64 of one batch entry; 128 threads; sub-tile s = tid/8 (4x4 of
-// 16x16 tiles); thread k = tid%8 of a sub-tile owns its rows 2k, 2k+1 (for
-// W) and its columns 2k, 2k+1 (for W^T).
+// In-register transpose of an 8x8 block of nibbles: a[n] holds row n (column
+// k in nibble k); afterwards a[k] holds column k (row n in nibble n).  Three
+// stages swap 1x1, 2x2 and 4x4 sub-blocks across the diagonal.
+__device__ __forceinline__ void transpose8x8_nibbles(uint32_t (&a)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        const uint32_t t = ((a[i] >> 4) ^ a[i + 1]) & 0x0F0F0F0Fu;
+        a[i + 1] ^= t;
+        a[i] ^= t << 4;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i += 4)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t t = ((a[i + j] >> 8) ^ a[i + j + 2]) & 0x00FF00FFu;
+            a[i + j + 2] ^= t;
+            a[i + j] ^= t << 8;
+        }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t t = ((a[j] >> 16) ^ a[j + 4]) & 0x0000FFFFu;
+        a[j + 4] ^= t;
+        a[j] ^= t << 16;
+    }
+}
+
+// CTA = 64x64 block of one batch entry (blockIdx.z), 4 warps.  Warp w owns
+// rows 16w .. 16w+15 of the block: a 16x64 strip of four 16x16 tiles.  Lane l
+// loads four 16-byte vectors: row (l >> 3) + 4i, columns 8*(l & 7) .. +7, so
+// the lanes of a tile are those with equal (l & 7) >> 1 and the tile amax is
+// three xor-shuffles away.  W codes and the W rows' scales (4 tiles = 4
+// contiguous scale bytes per row) are stored straight from registers; for
+// W^T the code words go through shared memory and 64 threads each transpose
+// one 8x8 nibble block, so that every W^T row receives 32 contiguous bytes.
 __global__ void __launch_bounds__(128) k_quant2d(const uint16_t* __restrict__ w, int64_t rows,
                                                  int64_t cols, int64_t ld, const float* __restrict__ amax,
                                                  uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                                                  uint8_t* __restrict__ codes_t, uint8_t* __restrict__ sf_t,
                                                  uint8_t* __restrict__ tile_sf, float* __restrict__ amax_copy) {
-    __shared__ __align__(16) uint16_t tile[64][72];
+    __shared__ uint32_t s_cw[64][9];        // code words [row of the block][8-column group] (+1 pad)
+    __shared__ uint32_t s_sc[4][4];         // tile scales [warp][tile]
     const int b = blockIdx.z;
     const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
     const uint16_t* wb = w + (int64_t)b * rows * ld;
-    const int tid = threadIdx.x;
-    if (amax_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) amax_copy[b] = amax[b];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (amax_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) amax_copy[b] = amax[b];
+    const int64_t rs = r0 + 16 * warp;                  // first row of this warp's strip
+    const bool rows_ok = rs < rows;                     // rows % 16 == 0: a strip is all in or all out
+    const int c8 = lane & 7;
+    const bool col_ok = c0 + 8 * c8 < cols;             // cols % 16 == 0: 8-column groups are all in or out
+    uint4 v[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int i = tid + 128 * j;
-        const int rr = i >> 3, cc = (i & 7) * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r0 + rr < rows && c0 + cc < cols)
-            v = __ldg(reinterpret_cast<const uint4*>(wb + (r0 + rr) * ld + c0 + cc));
-        *reinterpret_cast<uint4*>(&tile[rr][cc]) = v;
+    for (int i = 0; i < 4; ++i) {
+        const int64_t rr = rs + (lane >> 3) + 4 * i;
+        v[i] = (rows_ok && col_ok) ? __ldg(reinterpret_cast<const uint4*>(wb + rr * ld + c0 + 8 * c8))
+                                   : make_uint4(0, 0, 0, 0);
     }
-    __syncthreads();
-    const int st = tid >> 3, k = tid & 7;
-    const int sr = (st >> 2) * 16, sc = (st & 3) * 16;        // sub-tile origin in the CTA tile
-    const bool valid = (r0 + sr < rows) && (c0 + sc < cols);   // dims are multiples of 16
     uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int j = 0; j < 16; ++j) m = max(m, (uint32_t)(tile[sr + 2 * k + i][sc + j] & 0x7FFFu));
+    for (int i = 0; i < 4; ++i) m = absmax_bits(v[i], m);
+    m = max(m & 0xFFFFu, m >> 16);
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-    if (!valid) return;
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
     const float s_enc = tensor_encode_scale(amax[b]);
-    const uint32_t s = block_scale(__uint_as_float(m << 16), s_enc);
-    const float ratio = s ? element_ratio(s_enc, s) : 0.0f;
-    const int64_t ti = (r0 + sr) >> 4, tj = (c0 + sc) >> 4;
+    const uint32_t sc = block_scale(__uint_as_float(m << 16), s_enc);
+    const float ratio = sc ? element_ratio(s_enc, sc) : 0.0f;
+    uint32_t cw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cw[i] = encode8<false>(v[i], ratio, sc == 0, 0, 0);
+    // scales of the strip's four tiles (tile t is held by lane 2t)
+    const uint32_t word = __shfl_sync(0xFFFFFFFFu, sc, 0) | (__shfl_sync(0xFFFFFFFFu, sc, 2) << 8) |
+                          (__shfl_sync(0xFFFFFFFFu, sc, 4) << 16) | (__shfl_sync(0xFFFFFFFFu, sc, 6) << 24);
     const int64_t ebytes = rows * cols / 2;
-    // W rows
+    if (rows_ok) {
+        uint8_t* cb = codes + b * ebytes;
+        if (col_ok) {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int rr = sr + 2 * k + i;
-        uint32_t lo = 0, hi = 0;
-        if (s) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                lo |= e2m1_rne(__fmul_rn(__uint_as_float((uint32_t)tile[rr][sc + j] << 16), ratio)) << (4 * j);
-                hi |= e2m1_rne(__fmul_rn(__uint_as_float((uint32_t)tile[rr][sc + 8 + j] << 16), ratio)) << (4 * j);
+            for (int i = 0; i < 4; ++i) {
+                const int64_t rr = rs + (lane >> 3) + 4 * i;
+                *reinterpret_cast<uint32_t*>(cb + rr * (cols / 2) + (c0 + 8 * c8) / 2) = cw[i];
             }
         }
-        const int64_t gr = r0 + rr;
-        *reinterpret_cast<uint2*>(codes + b * ebytes + gr * (cols / 2) + (c0 + sc) / 2) = make_uint2(lo, hi);
-        sf[b * sf_bytes(rows, cols) + sf_offset(gr, tj, cols)] = (uint8_t)s;
+        if (lane < 16)
+            *reinterpret_cast<uint32_t*>(sf + b * sf_bytes(rows, cols) + sf_offset(rs + lane, c0 / 16, cols)) = word;
+        if (tile_sf != nullptr && lane < 8 && (lane & 1) == 0 && col_ok)
+            tile_sf[(int64_t)b * (rows / 16) * (cols / 16) + (rs / 16) * (cols / 16) + c0 / 16 + (lane >> 1)] = (uint8_t)sc;
     }
-    // W^T rows (columns of W)
-    if (codes_t != nullptr) {
+    if (codes_t == nullptr) return;
+    // ---- W^T: stage the code words, transpose 8x8 nibble blocks
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int cc = sc + 2 * k + i;
-            uint32_t lo = 0, hi = 0;
-            if (s) {
+    for (int i = 0; i < 4; ++i) s_cw[16 * warp + (lane >> 3) + 4 * i][c8] = cw[i];
+    if (lane < 4) s_sc[warp][lane] = rows_ok ? (word >> (8 * lane)) & 0xFFu : 0u;
+    __syncthreads();
+    if (threadIdx.x >= 64) return;
+    const int ng = threadIdx.x & 7, kg = threadIdx.x >> 3;     // rows 8ng.., columns 8kg..
+    uint32_t a[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    lo |= e2m1_rne(__fmul_rn(__uint_as_float((uint32_t)tile[sr + j][cc] << 16), ratio)) << (4 * j);
-                    hi |= e2m1_rne(__fmul_rn(__uint_as_float((uint32_t)tile[sr + 8 + j][cc] << 16), ratio)) << (4 * j);
-                }
-            }
-            const int64_t gc = c0 + cc;
-            *reinterpret_cast<uint2*>(codes_t + b * ebytes + gc * (rows / 2) + (r0 + sr) / 2) = make_uint2(lo, hi);
-            sf_t[b * sf_bytes(cols, rows) + sf_offset(gc, ti, rows)] = (uint8_t)s;
-        }
+    for (int j = 0; j < 8; ++j) a[j] = s_cw[8 * ng + j][kg];
+    transpose8x8_nibbles(a);
+    const bool n_ok = r0 + 8 * ng < rows;
+    uint8_t* ctb = codes_t + b * ebytes;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int64_t kk = c0 + 8 * kg + k;                    // W^T row = W column
+        if (n_ok && kk < cols) *reinterpret_cast<uint32_t*>(ctb + kk * (rows / 2) + (r0 + 8 * ng) / 2) = a[k];
     }
-    if (tile_sf != nullptr && k == 0) tile_sf[(int64_t)b * (rows / 16) * (cols / 16) + ti * (cols / 16) + tj] = (uint8_t)s;
+    // W^T row c0 + t: the scales of the block's four row tiles are 4 contiguous bytes
+    const int64_t kk = c0 + threadIdx.x;
+    if (kk < cols) {
+        const int tj = threadIdx.x >> 4;
+        const uint32_t tw = s_sc[0][tj] | (s_sc[1][tj] << 8) | (s_sc[2][tj] << 16) | (s_sc[3][tj] << 24);
+        *reinterpret_cast<uint32_t*>(sf_t + b * sf_bytes(cols, rows) + sf_offset(kk, r0 / 16, rows)) = tw;
+    }
 }
 
 // Padding of the 2D scale buffers (per batch entry: blockIdx.y).
@@ -463,31 +499,59 @@ __device__ __forceinline__ void rht16(float (&x)[16], uint32_t sign_mask) {
     for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(x[i], 0.25f);
 }
 
-// One thread = one channel c and 4 consecutive 16-token chunks (64 tokens).
+// CTA = 64 tokens x 256 channels, 256 threads.  The tile is staged in
+// shared memory with 16-byte loads (element loads when rows are not 16-byte
+// aligned); thread t then owns channel c0 + t and the tile's four 16-token
+// chunks.
 // MODE 0: amax of the transform (amax must be zero on entry).
 // MODE 1/2: transform + quantise (RNE / SR) into the transposed operand
 // [cols, tokens]: codes_t [cols, tokens/2], sf_t for [cols, tokens].
 template <int MODE>
-__global__ void __launch_bounds__(128) k_rht(const uint16_t* __restrict__ x, int64_t tokens,
+__global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int64_t tokens,
                                              int64_t cols, int64_t ld, uint32_t sign_mask,
                                              float* __restrict__ amax, uint64_t seed,
                                              uint8_t* __restrict__ codes_t, uint8_t* __restrict__ sf_t,
                                              float* __restrict__ amax_copy) {
-    const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t t0 = (int64_t)blockIdx.y * 64;
-    if (MODE != 0 && amax_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    __shared__ __align__(16) uint16_t tile[64][256 + 8];
+    const int64_t c0 = (int64_t)blockIdx.x * 256, t0 = (int64_t)blockIdx.y * 64;
+    const int tid = threadIdx.x;
+    if (MODE != 0 && amax_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
         amax_copy[0] = amax[0];
-    const bool active = c < cols;
     const int64_t left16 = (tokens - t0) >> 4;
     const int nchunks = left16 < 4 ? (int)left16 : 4;
+    const int ntok = 16 * nchunks;
+    const bool vec = ((ld & 7) == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+    // ---- stage 64 x 256 bf16 (zeros outside the tensor)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int i = tid + 256 * k;
+        const int rr = i >> 5, cc = (i & 31) * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        const int64_t gc = c0 + cc;
+        if (rr < ntok && gc < cols) {
+            const uint16_t* src = x + (t0 + rr) * ld + gc;
+            if (vec && gc + 8 <= cols) {
+                v = __ldg(reinterpret_cast<const uint4*>(src));
+            } else {
+                uint16_t e[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) e[j] = (gc + j < cols) ? __ldg(src + j) : (uint16_t)0;
+                v = make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16),
+                               e[4] | ((uint32_t)e[5] << 16), e[6] | ((uint32_t)e[7] << 16));
+            }
+        }
+        *reinterpret_cast<uint4*>(&tile[rr][cc]) = v;
+    }
+    __syncthreads();
+    const int64_t c = c0 + tid;
+    const bool active = c < cols;
     if (MODE == 0) {
         float m = 0.0f;
         if (active) {
             for (int j = 0; j < nchunks; ++j) {
                 float v[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    v[i] = __uint_as_float((uint32_t)__ldg(x + (t0 + 16 * j + i) * ld + c) << 16);
+                for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[16 * j + i][tid] << 16);
                 rht16(v, sign_mask);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
@@ -500,42 +564,39 @@ __global__ void __launch_bounds__(128) k_rht(const uint16_t* __restrict__ x, int
     const float s_enc = tensor_encode_scale(amax[0]);
     uint32_t packed[4][2];
     uint32_t sfw = 0;
-    for (int j = 0; j < nchunks; ++j) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        packed[j][0] = packed[j][1] = 0u;
+        if (j >= nchunks) continue;
         float v[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            v[i] = __uint_as_float((uint32_t)__ldg(x + (t0 + 16 * j + i) * ld + c) << 16);
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[16 * j + i][tid] << 16);
         rht16(v, sign_mask);
         float bamax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(v[i]));
-        const uint32_t s = block_scale(bamax, s_enc);
-        sfw |= s << (8 * j);
-        uint32_t lo = 0, hi = 0;
-        if (s) {
-            const float ratio = element_ratio(s_enc, s);
-            if (MODE == 2) {
-                const uint64_t e0 = (uint64_t)c * (uint64_t)tokens + (uint64_t)(t0 + 16 * j);
+        const uint32_t sc = block_scale(bamax, s_enc);
+        sfw |= sc << (8 * j);
+        if (sc == 0) continue;
+        const float ratio = element_ratio(s_enc, sc);
+        float f[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 w = sr_words(seed, (e0 >> 2) + q);
-                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(v[i], ratio);
+        if (MODE == 2) {
+            const uint64_t e0 = (uint64_t)c * (uint64_t)tokens + (uint64_t)(t0 + 16 * j);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t code = e2m1_sr(__fmul_rn(v[4 * q + i], ratio), ws[i]);
-                        if (q < 2) lo |= code << (4 * (4 * q + i)); else hi |= code << (4 * (4 * (q - 2) + i));
-                    }
-                }
-            } else {
+            for (int q = 0; q < 4; ++q) {
+                const uint4 wd = sr_words(seed, (e0 >> 2) + q);
+                const uint32_t ws[4] = {wd.x, wd.y, wd.z, wd.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    lo |= e2m1_rne(__fmul_rn(v[i], ratio)) << (4 * i);
-                    hi |= e2m1_rne(__fmul_rn(v[8 + i], ratio)) << (4 * i);
-                }
+                for (int i = 0; i < 4; ++i) packed[j][q >> 1] |= e2m1_sr(f[4 * q + i], ws[i]) << (4 * (4 * (q & 1) + i));
             }
+        } else {
+            const float lo[8] = {f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]};
+            const float hi[8] = {f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]};
+            packed[j][0] = e2m1x8_rne(lo);
+            packed[j][1] = e2m1x8_rne(hi);
         }
-        packed[j][0] = lo;
-        packed[j][1] = hi;
     }
     uint8_t* crow = codes_t + c * (tokens >> 1) + (t0 >> 1);
     const int64_t sfc = t0 >> 4;

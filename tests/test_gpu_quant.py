@@ -135,3 +135,28 @@ def test_amax_batched(B, orc):
 
 def test_device_status_clean(B):
     assert B.device_status() == 0
+
+
+def test_quantize_1d_ties_signed_zeros_saturation(B, orc):
+    """Blocks whose largest magnitude is 6 under a tensor amax of 2688 get
+    scale 1.0 and element multiplier 1, so every value below reaches the E2M1
+    rounding unchanged: the seven ties of the grid, negative values that
+    round to zero (code 0x8), -0, and values beyond 6 that saturate."""
+    rows = [
+        [6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.1, -0.25, -5, 5.5, 0.5, 1.0, -0.0, -6],
+        [6, -0.75, -1.25, -1.75, -2.5, -3.5, -0.0001, 0.0001, -3, 4.5, 2.75, -0.3, 0.2, 1.4, -1.6, 6],
+        [-6, 0.2499, 0.2501, 0.7499, 0.7501, 4.999, 5.001, -5.001, -0.2501, 3.49, 3.51, 1.74, 1.76, 0, 0, 0],
+    ]
+    x = torch.tensor(rows, dtype=torch.float32).repeat(5, 2).to(torch.bfloat16)   # 15 x 32
+    amax_in = torch.tensor([2688.0], device="cuda")
+    for mode in (0, 1):
+        q = B.quantize_1d(x.cuda(), mode=mode, seed=5, amax_in=amax_in)
+        torch.cuda.synchronize()
+        _same(q, orc.quantize_1d(x, mode=mode, seed=5, amax_in=2688.0), 15, 32)
+    # 2D tiles and the transposed copy take the same conversion
+    w = torch.tensor(rows, dtype=torch.float32).repeat(6, 1)[:16].to(torch.bfloat16)    # 16 x 16
+    qw, qt, _ = B.quantize_2d(w.cuda(), want_t=True, amax_in=amax_in)
+    torch.cuda.synchronize()
+    ref = orc.quantize_2d(w, amax_in=[2688.0])
+    assert (np_u8(qw.codes).reshape(ref["codes"].shape) == ref["codes"]).all()
+    assert (np_u8(qt.codes).reshape(ref["codes_t"].shape) == ref["codes_t"]).all()
