@@ -90,60 +90,65 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float (&f)[8]) {
 // E2M1 code of v with stochastic rounding by the 32-bit word u.  With grid
 // neighbours lo <= |v| < hi and p = (|v| - lo) / (hi - lo), the magnitude
 // rounds up iff (u >> 8) < p * 2^24, i.e. iff u < 256 * ceil(p * 2^24).
-// That bound is formed from the FP32 bits of |v| with integer operations:
-//   |v| in [1, 6):   lo index 2 + 2e + (mantissa >= 1/2), bound = low 22
-//                    mantissa bits << 10 (the gap is 2^(e-1));
-//   |v| in [0.5, 1): lo index 1, bound = mantissa << 9 (gap 1/2);
-//   |v| in [0, 0.5): lo index 0, bound = 256 * ceil(|v| * 2^25).
-// It equals the FP32 statement above for every finite input (checked
-// exhaustively over all FP32 bit patterns below 6 on the host).
+// Branch-free integer form on the FP32 bits mb of |v|:
+//   |v| in [1, 6):   the grid step is bit 22 of mb; adding (~u >> 10) to the
+//                    22 bits below it carries into bit 22 exactly when
+//                    (u >> 10) < those bits, and the carried value's bits
+//                    22..30 give the code: (mb + (~u >> 10)) >> 22, minus 252;
+//   |v| in [0.5, 1): the step is the exponent: (mb + (~u >> 9)) >> 23, minus 125;
+//   |v| in [0, 0.5): up iff u < 256 * ceil(|v| * 2^25), the ceiling taken by
+//                    a rounding-up shift of the significand.
+// It equals the FP32 statement above at both sides of every threshold for
+// every FP32 bit pattern (checked exhaustively on the host); the decision is
+// monotone in u, so that covers all words.
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u) {
     const uint32_t bits = __float_as_uint(v);
-    const uint32_t sign = (bits >> 28) & 8u;
     const uint32_t mb = bits & 0x7FFFFFFFu;
-    if (mb >= 0x40C00000u) return sign | 7u;                       // |v| >= 6
-    uint32_t c, thr;
-    if (mb >= 0x3F800000u) {
-        c = 2u + 2u * ((mb >> 23) - 127u) + ((mb >> 22) & 1u);
-        thr = (mb & 0x3FFFFFu) << 10;
-    } else if (mb >= 0x3F000000u) {
-        c = 1u;
-        thr = (mb & 0x7FFFFFu) << 9;
-    } else {
-        const uint32_t ef = mb >> 23;
-        uint32_t x;
-        if (mb == 0u) x = 0u;
-        else if (ef <= 101u) x = 1u;                                // |v| * 2^25 < 1
-        else {
-            const uint32_t sh = 125u - ef;
-            x = (((mb & 0x7FFFFFu) | 0x800000u) + (1u << sh) - 1u) >> sh;
-        }
-        c = 0u;
-        thr = x << 8;
-    }
-    return sign | (c + (u < thr ? 1u : 0u));
+    const uint32_t nu = ~u;
+    const uint32_t c_hi = ((mb + (nu >> 10)) >> 22) - 252u;
+    const uint32_t c_mid = ((mb + (nu >> 9)) >> 23) - 125u;
+    const uint32_t ef = mb >> 23;
+    const uint32_t sh = (uint32_t)min(max(125 - (int)ef, 0), 31);
+    const uint32_t sig = (mb & 0x7FFFFFu) | (ef != 0u ? 0x800000u : 0u);
+    const uint32_t x = (sig + (1u << sh) - 1u) >> sh;              // ceil(|v| * 2^25) < 2^24
+    const uint32_t c_lo = u < (x << 8) ? 1u : 0u;
+    uint32_t c = mb >= 0x3F800000u ? c_hi : (mb >= 0x3F000000u ? c_mid : c_lo);
+    c = mb >= 0x40C00000u ? 7u : c;                                 // |v| >= 6 saturates
+    return ((bits >> 28) & 8u) | c;
 }
 
 // ------------------------------------------------------------------ Philox
-// Philox4x32 with R rounds (Salmon et al., SC'11): per round two 32x32->64
-// products of counter words 0 and 2, words recombined with the key; the key
-// advances by the Weyl constants between rounds.
-template <int R>
-__device__ __forceinline__ uint4 philox4x32(uint4 c, uint2 k) {
+// Philox4x32 with 5 rounds (Salmon et al., SC'11): per round two 32x32->64
+// products of counter words 0 and 2, words recombined with the round key;
+// the key advances by the Weyl constants between rounds.  The round keys
+// depend on the seed only and are formed once per thread.
+struct PhiloxKeys {
+    uint32_t k0[5], k1[5];
+};
+
+__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
+    PhiloxKeys k;
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        if (r > 0) { k.x += 0x9E3779B9u; k.y += 0xBB67AE85u; }
-        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+    for (int r = 0; r < 5; ++r) {
+        k.k0[r] = a;
+        k.k1[r] = b;
+        a += 0x9E3779B9u;
+        b += 0xBB67AE85u;
     }
-    return c;
+    return k;
 }
 
-// Four random words for output elements 4q .. 4q+3 under seed.
-__device__ __forceinline__ uint4 sr_words(uint64_t seed, uint64_t q) {
-    return philox4x32<5>(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u),
-                         make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+// Four random words for output elements 4q .. 4q+3: counter (q, 0, 0).
+__device__ __forceinline__ uint4 sr_words(const PhiloxKeys& k, uint64_t q) {
+    uint4 c = make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u);
+#pragma unroll
+    for (int r = 0; r < 5; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k.k0[r], lo1, hi0 ^ c.w ^ k.k1[r], lo0);
+    }
+    return c;
 }
 
 // ------------------------------------------------------------------ layout

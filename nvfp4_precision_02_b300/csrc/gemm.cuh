@@ -26,7 +26,13 @@
 //                 which is where the block-scaled MMA reads its scales.
 //   warps 6..21   epilogue: four warps per TMEM lane quarter, 64 accumulator
 //                 columns each; tcgen05.ld, release the accumulator to the
-//                 MMA warp, scale by alpha, round, store to global memory.
+//                 MMA warp, scale by alpha, round, store.  bf16 output goes
+//                 through a 2 KB 64B-swizzled staging buffer per warp and
+//                 TMA stores of 32 x 32 boxes (a warp's direct stores would
+//                 touch 32 rows per instruction); FP32 output, and rows past
+//                 the end of an expert, are stored directly.
+//   The TMA-store epilogue uses 3 stages (the staging takes the fourth's
+//   space); it is chosen for bf16 outputs of GEMMs with K < 8192.
 //   TMEM: accumulator columns 0..255; per stage 16 columns of A scales and
 //   32 columns of B scales from column 256.
 //   Moving the scales with tcgen05.st from dedicated warps keeps them off
@@ -42,7 +48,6 @@
 namespace nvfp4 {
 
 constexpr int G_BM = 128, G_BN = 256, G_BK = 256;
-constexpr int G_STAGES = 4;
 constexpr int G_A_BYTES = G_BM * G_BK / 2;                 // 16384
 constexpr int G_B_BYTES = G_BN * G_BK / 2;                 // 32768
 constexpr int G_SFA_BYTES = (G_BK / 64) * 512;             // 2048: 4 atoms of A scales
@@ -58,10 +63,29 @@ constexpr int G_BAND = 16;                                   // m-tiles per rast
 constexpr uint64_t G_WAIT_NS = 4000000000ull;                // bounded waits: 4 s
 constexpr int G_BAR_BYTES = 256;                             // barriers, TMEM slot, abort flag
 
-// dynamic shared memory: 1 KB alignment slack, stages, barriers, tables
-__host__ __device__ constexpr int gemm_smem_bytes(int groups) {
-    return 1024 + G_STAGES * G_STAGE_BYTES + G_BAR_BYTES + 2 * 4 * (groups + 1);
+constexpr int G_STORE_WARP_BYTES = 2048;                     // bf16 staging of one epilogue warp: 32 x 32
+
+// Shared-memory layout of one CTA (after 1 KB alignment): the stage ring,
+// the bf16 store staging (TMA-store epilogue only), barriers, group tables.
+// The TMA-store epilogue gives up one stage for the 32 KB staging: it pays
+// when K is short (the epilogue of a tile is then as long as its mainloop),
+// while long-K GEMMs keep four stages and store directly.
+template <bool TMA_STORE>
+struct GemmLayout {
+    static constexpr int STAGES = TMA_STORE ? 3 : 4;
+    static constexpr int STORE_OFF = STAGES * G_STAGE_BYTES;
+    static constexpr int STORE_BYTES = TMA_STORE ? G_EPI_WARPS * G_STORE_WARP_BYTES : 0;
+    static constexpr int BAR_OFF = STORE_OFF + STORE_BYTES;
+    static constexpr int TAB_OFF = BAR_OFF + G_BAR_BYTES;
+};
+
+// dynamic shared memory: 1 KB alignment slack, layout, group tables
+__host__ __device__ constexpr int gemm_smem_bytes(bool tma_store, int groups) {
+    return 1024 + (tma_store ? GemmLayout<true>::TAB_OFF : GemmLayout<false>::TAB_OFF) + 2 * 4 * (groups + 1);
 }
+
+// K below which a bf16 GEMM takes the TMA-store epilogue.
+constexpr int64_t G_TMA_STORE_MAX_K = 8192;
 
 struct GemmParams {
     int64_t M;                  // rows of A (dense) / total rows R (grouped)
@@ -141,6 +165,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// TMA store of a box from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -283,18 +321,23 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int mtiles, int ntil
 __device__ __forceinline__ uint4 ldg_u4(const uint8_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
 // ------------------------------------------------------------------ kernel
-template <bool OUT_FP32>
+// OUT_FP32: FP32 output (stored directly); otherwise bf16.  TMA_STORE (bf16
+// only): the output leaves through tm_c (rows 16-byte aligned).
+template <bool OUT_FP32, bool TMA_STORE>
 __global__ void __launch_bounds__(G_THREADS, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                 const GemmParams p) {
+                 const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
+    static_assert(!(OUT_FP32 && TMA_STORE), "the TMA-store epilogue is bf16 only");
+    using L = GemmLayout<TMA_STORE>;
+    constexpr int G_STAGES = L::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G_STAGES * G_STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
     // bars: full[S], empty[S], sf_full[S], acc_full, acc_empty, drain
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * G_STAGES + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int32_t* tab = reinterpret_cast<int32_t*>(smem + G_STAGES * G_STAGE_BYTES + G_BAR_BYTES);
+    int32_t* tab = reinterpret_cast<int32_t*>(smem + L::TAB_OFF);
     const int groups = p.groups;
     GroupTables gt{tab, tab + groups + 1};
 
@@ -318,6 +361,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     if (warp == G_W_TMA && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_a)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b)) : "memory");
+        if (TMA_STORE) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_c)) : "memory");
     }
     if (warp == G_W_MMA) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -511,41 +555,70 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     }
                 }
             } else {
-                // four 16-column pieces: load, scale, round, store; release after the last load
-                const bool live = r < tc.rows && col0 < p.N;
-                uint16_t* out = reinterpret_cast<uint16_t*>(p.c) + row * p.ldc + col0;
+                // two 32-column halves: load, scale, round; release after the second load.
+                // A half whose 32 rows all belong to the tile goes out as one TMA
+                // store box (32 x 32 bf16) from this warp's 64B-swizzled staging
+                // buffer; other rows are stored directly.
+                const bool rows_full = TMA_STORE && (q * 32 + 31) < tc.rows;
+                const uint32_t stage_buf = smem_u32(smem + L::STORE_OFF + (warp - G_W_EPI0) * G_STORE_WARP_BYTES);
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    uint32_t v[16], w[8];
-                    tc_ld_32x32b_x16(taddr + 16 * h, v);
-                    tc_wait_ld();
-                    if (h == 3) {
-                        tc_fence_before();
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        uint32_t v[16];
+                        tc_ld_32x32b_x16(taddr + 32 * h + 16 * k, v);
+                        tc_wait_ld();
+                        if (h == 1 && k == 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(acc_empty);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(v[2 * j])),
+                                                                            __fmul_rn(alpha, __uint_as_float(v[2 * j + 1])));
+                            w[8 * k + j] = *reinterpret_cast<const uint32_t*>(&b2);
+                        }
+                    }
+                    const int64_t cstart = col0 + 32 * h;
+                    if (cstart >= p.N) continue;
+                    if (rows_full) {
+                        // the staging buffer is free once the previous box has been read
+                        if (lane == 0) bulk_wait_read0();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty);
-                    }
+                        // row `lane`, 16-byte chunk j at lane*64 + 16*(j ^ ((lane >> 1) & 3))
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(v[2 * j])),
-                                                                        __fmul_rn(alpha, __uint_as_float(v[2 * j + 1])));
-                        w[j] = *reinterpret_cast<const uint32_t*>(&b2);
-                    }
-                    if (live) {
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t addr = stage_buf + lane * 64 + 16 * (j ^ ((lane >> 1) & 3));
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * j]),
+                                         "r"(w[4 * j + 1]), "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tm_c, stage_buf, (int32_t)cstart, (int32_t)(tc.row0 + q * 32));
+                            bulk_commit();
+                        }
+                    } else if (r < tc.rows) {
+                        uint16_t* out = reinterpret_cast<uint16_t*>(p.c) + row * p.ldc + cstart;
 #pragma unroll
-                        for (int i = 0; i < 16; i += 8) {
-                            const int cc = 16 * h + i;
-                            if (p.vec_store && col0 + cc + 8 <= p.N) {
-                                *reinterpret_cast<uint4*>(out + cc) = make_uint4(w[i / 2], w[i / 2 + 1], w[i / 2 + 2], w[i / 2 + 3]);
+                        for (int i = 0; i < 32; i += 8) {
+                            if (p.vec_store && cstart + i + 8 <= p.N) {
+                                *reinterpret_cast<uint4*>(out + i) = make_uint4(w[i / 2], w[i / 2 + 1], w[i / 2 + 2], w[i / 2 + 3]);
                             } else {
 #pragma unroll
                                 for (int j = 0; j < 8; ++j)
-                                    if (col0 + cc + j < p.N) out[cc + j] = (uint16_t)(w[(i + j) / 2] >> (16 * ((i + j) & 1)));
+                                    if (cstart + i + j < p.N) out[i + j] = (uint16_t)(w[(i + j) / 2] >> (16 * ((i + j) & 1)));
                             }
                         }
                     }
                 }
             }
         }
+        // every TMA store of this warp has finished before the CTA exits
+        if (TMA_STORE && lane == 0) bulk_wait0();
     }
 
     tc_fence_before();

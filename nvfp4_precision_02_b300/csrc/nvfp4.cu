@@ -412,24 +412,51 @@ static nvfp4_status check_operand(const nvfp4_tensor* t, const char* name) {
     return NVFP4_OK;
 }
 
-static nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int grid,
-                                nvfp4_out_dtype dt, nvfp4_stream_t stream, int dev) {
-    const int smem = gemm_smem_bytes(p.groups);
+static nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                                const GemmParams& p, int grid, nvfp4_out_dtype dt, bool tma_store,
+                                nvfp4_stream_t stream, int dev) {
+    const bool f32 = dt == NVFP4_OUT_FP32;
+    const int smem = gemm_smem_bytes(tma_store, p.groups);
     {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         if (!g_dev[dev].gemm_attr) {
-            NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     gemm_smem_bytes(NVFP4_MAX_GROUPS)), "smem attr"));
-            NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     gemm_smem_bytes(NVFP4_MAX_GROUPS)), "smem attr"));
+            NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     gemm_smem_bytes(false, NVFP4_MAX_GROUPS)), "smem attr"));
+            NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     gemm_smem_bytes(true, NVFP4_MAX_GROUPS)), "smem attr"));
+            NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     gemm_smem_bytes(false, NVFP4_MAX_GROUPS)), "smem attr"));
             g_dev[dev].gemm_attr = true;
         }
     }
-    if (dt == NVFP4_OUT_FP32)
-        k_gemm_nvfp4<true><<<grid, G_THREADS, smem, stream>>>(ma, mb, p);
+    if (f32)
+        k_gemm_nvfp4<true, false><<<grid, G_THREADS, smem, stream>>>(ma, mb, mc, p);
+    else if (tma_store)
+        k_gemm_nvfp4<false, true><<<grid, G_THREADS, smem, stream>>>(ma, mb, mc, p);
     else
-        k_gemm_nvfp4<false><<<grid, G_THREADS, smem, stream>>>(ma, mb, p);
+        k_gemm_nvfp4<false, false><<<grid, G_THREADS, smem, stream>>>(ma, mb, mc, p);
     return launched("k_gemm_nvfp4");
+}
+
+// Store tensor map of a bf16 output [rows, n] with row stride ldc: boxes of
+// 32 x 32 elements (64-byte rows) with 64-byte swizzle.  Only built when C
+// rows are 16-byte aligned; otherwise the kernel stores directly.
+static nvfp4_status make_store_map(CUtensorMap* map, void* c, int64_t rows, int64_t n, int64_t ldc, bool* enabled) {
+    std::memset(map, 0, sizeof(*map));
+    *enabled = false;
+    if (!aligned16(c) || (ldc * 2) % 16 != 0) return NVFP4_OK;
+    auto fn = encode_fn();
+    if (fn == nullptr) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldc * 2)};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled (store) failed (%d)", (int)r);
+    *enabled = true;
+    return NVFP4_OK;
 }
 
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* c, int64_t ldc, nvfp4_out_dtype c_dtype,
@@ -459,9 +486,13 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* c, i
     p.amax_a = a->amax; p.amax_b = b->amax;
     p.c = c; p.ldc = ldc;
     p.vec_store = aligned16(c) && (ldc * esz) % 16 == 0;
+    CUtensorMap mc;
+    bool tma_store = false;
+    std::memset(&mc, 0, sizeof(mc));
+    if (c_dtype == NVFP4_OUT_BF16 && K < G_TMA_STORE_MAX_K) NVFP4_TRY(make_store_map(&mc, c, M, N, ldc, &tma_store));
     const int64_t tiles = cdiv(M, G_BM) * cdiv(N, G_BN);
     const int grid = (int)std::min<int64_t>(tiles, sms);
-    return launch_gemm(ma, mb, p, grid, c_dtype, stream, dev);
+    return launch_gemm(ma, mb, mc, p, grid, c_dtype, tma_store, stream, dev);
 }
 
 nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, int32_t num_groups,
@@ -496,7 +527,11 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, i
     p.amax_a = a->amax; p.amax_b = b->amax;
     p.c = c; p.ldc = ldc;
     p.vec_store = aligned16(c) && (ldc * esz) % 16 == 0;
-    return launch_gemm(ma, mb, p, sms, c_dtype, stream, dev);
+    CUtensorMap mc;
+    bool tma_store = false;
+    std::memset(&mc, 0, sizeof(mc));
+    if (c_dtype == NVFP4_OUT_BF16 && K < G_TMA_STORE_MAX_K) NVFP4_TRY(make_store_map(&mc, c, R, n, ldc, &tma_store));
+    return launch_gemm(ma, mb, mc, p, sms, c_dtype, tma_store, stream, dev);
 }
 
 nvfp4_status nvfp4_device_status(int32_t* flags) {

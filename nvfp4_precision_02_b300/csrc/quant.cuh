@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(256) k_amax_grouped(const uint16_t* __restrict
 // ------------------------------------------------------------------ 1D quantise
 // Encode the 8 elements of one half-block (lane pair = one 16-element block).
 template <bool SR>
-__device__ __forceinline__ uint32_t encode8(const uint4 v, float ratio, bool zero, uint64_t seed,
+__device__ __forceinline__ uint32_t encode8(const uint4 v, float ratio, bool zero, const PhiloxKeys& key,
                                             uint64_t e0) {
     if (zero) return 0u;
     const float f[8] = {__fmul_rn(bf16_lo(v.x), ratio), __fmul_rn(bf16_hi(v.x), ratio),
@@ -233,8 +233,8 @@ __device__ __forceinline__ uint32_t encode8(const uint4 v, float ratio, bool zer
                         __fmul_rn(bf16_lo(v.z), ratio), __fmul_rn(bf16_hi(v.z), ratio),
                         __fmul_rn(bf16_lo(v.w), ratio), __fmul_rn(bf16_hi(v.w), ratio)};
     if (!SR) return e2m1x8_rne(f);
-    const uint4 w0 = sr_words(seed, e0 >> 2);
-    const uint4 w1 = sr_words(seed, (e0 >> 2) + 1);
+    const uint4 w0 = sr_words(key, e0 >> 2);
+    const uint4 w1 = sr_words(key, (e0 >> 2) + 1);
     const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     uint32_t out = 0;
 #pragma unroll
@@ -270,6 +270,7 @@ __global__ void __launch_bounds__(256) k_quant1d(const uint16_t* __restrict__ x,
     int g = 0;
     int32_t g_begin = 0, g_end = (int32_t)rows, sf_row0 = 0;
     float s_enc = GROUPED ? 1.0f : tensor_encode_scale(amax[0]);
+    const PhiloxKeys key = philox_keys(seed);
     bool have_g = false;
     for (int64_t r = r0; r < r1; ++r) {
         if (GROUPED) {
@@ -303,7 +304,7 @@ __global__ void __launch_bounds__(256) k_quant1d(const uint16_t* __restrict__ x,
                 const uint32_t sc = block_scale(bamax, s_enc);
                 const float ratio = sc ? element_ratio(s_enc, sc) : 0.0f;
                 if (u < upr) {
-                    const uint32_t packed = encode8<SR>(v[i], ratio, sc == 0, seed,
+                    const uint32_t packed = encode8<SR>(v[i], ratio, sc == 0, key,
                                                         (uint64_t)r * (uint64_t)cols + (uint64_t)u * 8);
                     *reinterpret_cast<uint32_t*>(crow + u * 4) = packed;
                     if ((lane & 1) == 0) {
@@ -421,8 +422,9 @@ __global__ void __launch_bounds__(128) k_quant2d(const uint16_t* __restrict__ w,
     const uint32_t sc = block_scale(__uint_as_float(m << 16), s_enc);
     const float ratio = sc ? element_ratio(s_enc, sc) : 0.0f;
     uint32_t cw[4];
+    const PhiloxKeys no_key{};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) cw[i] = encode8<false>(v[i], ratio, sc == 0, 0, 0);
+    for (int i = 0; i < 4; ++i) cw[i] = encode8<false>(v[i], ratio, sc == 0, no_key, 0);
     // scales of the strip's four tiles (tile t is held by lane 2t)
     const uint32_t word = __shfl_sync(0xFFFFFFFFu, sc, 0) | (__shfl_sync(0xFFFFFFFFu, sc, 2) << 8) |
                           (__shfl_sync(0xFFFFFFFFu, sc, 4) << 16) | (__shfl_sync(0xFFFFFFFFu, sc, 6) << 24);
@@ -562,6 +564,7 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
     }
     if (!active) return;
     const float s_enc = tensor_encode_scale(amax[0]);
+    const PhiloxKeys key = philox_keys(seed);
     uint32_t packed[4][2];
     uint32_t sfw = 0;
 #pragma unroll
@@ -586,7 +589,7 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
             const uint64_t e0 = (uint64_t)c * (uint64_t)tokens + (uint64_t)(t0 + 16 * j);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const uint4 wd = sr_words(seed, (e0 >> 2) + q);
+                const uint4 wd = sr_words(key, (e0 >> 2) + q);
                 const uint32_t ws[4] = {wd.x, wd.y, wd.z, wd.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) packed[j][q >> 1] |= e2m1_sr(f[4 * q + i], ws[i]) << (4 * (4 * (q & 1) + i));

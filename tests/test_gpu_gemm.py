@@ -55,7 +55,8 @@ def _check(out, ref, absum, bf16):
 
 SHAPES = [(256, 256, 256),    # the tiny fprop workload shape
           (1, 1, 32), (17, 33, 64), (128, 256, 256), (129, 257, 288), (300, 520, 1024),
-          (256, 384, 96), (64, 1000, 512), (520, 130, 2048)]
+          (256, 384, 96), (64, 1000, 512), (520, 130, 2048),
+          (136, 264, 8192)]   # K >= 8192: the four-stage epilogue with direct bf16 stores
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
