@@ -176,6 +176,26 @@ nvfp4_status nvfp4_quantize_2d(const void *w, int64_t batch, int64_t rows, int64
                                int64_t ld, const float *amax_in, nvfp4_tensor *out,
                                nvfp4_tensor *out_t, uint8_t *tile_sf, nvfp4_stream_t stream);
 
+/* Bytes of device workspace nvfp4_quantize_2d_fused needs for `batch`
+ * entries (16-byte multiple). */
+size_t nvfp4_quantize_2d_fused_workspace(int64_t batch);
+
+/* The same W result as nvfp4_quantize_2d with amax_in == NULL and out_t ==
+ * NULL (per-entry amax, W codes and GEMM-ready scales, optional tile scales)
+ * for batched weights whose entries fit in L2, such as the LatentMoE expert
+ * weights (2D block scaling of weights, Super summary "Infra design").  One
+ * cooperative launch computes each entry's amax and quantises the entry while
+ * it is still in L2, so HBM is read once instead of twice.  The transposed
+ * copy is not produced (use nvfp4_quantize_2d for W^T).
+ * workspace: device, caller-allocated, at least
+ * nvfp4_quantize_2d_fused_workspace(batch) bytes, 16-byte aligned; the call
+ * zeroes and uses it (per-entry arrival counters), so calls sharing one
+ * workspace must not overlap on the GPU.  out->amax receives the amaxes.
+ * Other arguments as for nvfp4_quantize_2d. */
+nvfp4_status nvfp4_quantize_2d_fused(const void *w, int64_t batch, int64_t rows, int64_t cols, int64_t ld,
+                                     void *workspace, size_t workspace_bytes, nvfp4_tensor *out,
+                                     uint8_t *tile_sf, nvfp4_stream_t stream);
+
 /* amax of the RHT output of x (bf16 [tokens, cols], row stride ld,
  * tokens % 16 == 0) -> amax (device, 1 float). */
 nvfp4_status nvfp4_rht_amax(const void *x, int64_t tokens, int64_t cols, int64_t ld,

@@ -3,8 +3,8 @@
 Usage:
   python -m nvfp4_precision_02_b300.cases <op> [--workload super|ultra] [--iters N]
 
-<op> is one of: amax, quant1d_rne, quant1d_sr, quant2d, rht_sr, gemm_fprop, gemm_dgrad,
-gemm_wgrad, grouped_up, grouped_down.  The inputs of the op are generated on the device and
+<op> is one of: amax, quant1d_rne, quant1d_sr, quant2d, quant2d_moe, quant2d_moe_fused, rht_sr,
+gemm_fprop, gemm_dgrad, gemm_wgrad, grouped_up, grouped_down.  The inputs of the op are generated on the device and
 its operands quantised once; the op itself is then launched `iters` times back to back, so
 a profiler can skip the set-up launches and capture the op alone (for example with
 `ncu -k regex:<kernel> -s 1 -c 1`).  It prints the mean CUDA-event time per launch.
@@ -19,8 +19,8 @@ import torch
 from . import binding as B
 from . import workloads as wl
 
-OPS = ["amax", "quant1d_rne", "quant1d_sr", "quant2d", "rht_sr", "gemm_fprop", "gemm_dgrad",
-       "gemm_wgrad", "grouped_up", "grouped_down"]
+OPS = ["amax", "quant1d_rne", "quant1d_sr", "quant2d", "quant2d_moe", "quant2d_moe_fused", "rht_sr",
+       "gemm_fprop", "gemm_dgrad", "gemm_wgrad", "grouped_up", "grouped_down"]
 
 
 def prepare(op: str, which: str, dev):
@@ -44,6 +44,13 @@ def prepare(op: str, which: str, dev):
         w = wl.normal_bf16((N, K), 0.02, wl.SEEDS[which + "_w"], dev)
         qw, qwt = B.empty_qtensor(N, K, dev), B.empty_qtensor(K, N, dev)
         return lambda: B.quantize_2d(w, want_t=True, out=qw, out_t=qwt)
+    if op in ("quant2d_moe", "quant2d_moe_fused"):
+        w = wl.batched_normal_bf16(m.experts, m.expert_hidden, m.latent, 0.02, wl.SEEDS[which + "_moe_w"], dev)
+        qw = B.empty_qtensor(m.expert_hidden, m.latent, dev, batch=m.experts, n_amax=m.experts)
+        if op == "quant2d_moe":
+            return lambda: B.quantize_2d(w, want_t=False, out=qw)
+        ws = torch.empty(B.quantize_2d_fused_workspace(m.experts), dtype=torch.uint8, device=dev)
+        return lambda: B.quantize_2d_fused(w, workspace=ws, out=qw)
     if op.startswith("gemm_"):
         ins = wl.dense_inputs(d, which, device=dev)
         x, w, dy = ins["x"], ins["w"], ins["dy"]

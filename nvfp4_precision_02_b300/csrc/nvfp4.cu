@@ -346,6 +346,50 @@ nvfp4_status nvfp4_quantize_2d(const void* w, int64_t batch, int64_t rows, int64
     return NVFP4_OK;
 }
 
+size_t nvfp4_quantize_2d_fused_workspace(int64_t batch) {
+    if (batch < 1) return 0;
+    return (size_t)(((batch + 1) * 4 + 15) / 16 * 16);
+}
+
+nvfp4_status nvfp4_quantize_2d_fused(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ld,
+                                     void* workspace, size_t workspace_bytes, nvfp4_tensor* out, uint8_t* tile_sf,
+                                     nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    if (batch < 1 || batch > 65535) return fail(NVFP4_ERR_SHAPE, "batch must be in [1, 65535]");
+    NVFP4_TRY(check_input(w, rows * batch, cols, ld, 16, "w"));
+    if (rows % 16 != 0) return fail(NVFP4_ERR_SHAPE, "rows=%lld is not a multiple of 16", (long long)rows);
+    NVFP4_TRY(check_out(out, rows, cols, true, "out"));
+    if (workspace == nullptr) return fail(NVFP4_ERR_NULL, "workspace is NULL");
+    if (!aligned16(workspace)) return fail(NVFP4_ERR_ALIGN, "workspace not 16-byte aligned");
+    if (workspace_bytes < nvfp4_quantize_2d_fused_workspace(batch))
+        return fail(NVFP4_ERR_SHAPE, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                    nvfp4_quantize_2d_fused_workspace(batch));
+    int sms = 0, dev = 0;
+    NVFP4_TRY(check_device(&sms, &dev));
+    NVFP4_TRY(cuda_call(cudaMemsetAsync(out->amax, 0, sizeof(float) * batch, stream), "memset amax"));
+    if (rows == 0 || cols == 0) return NVFP4_OK;
+    NVFP4_TRY(cuda_call(cudaMemsetAsync(workspace, 0, (size_t)(batch + 1) * 4, stream), "memset workspace"));
+    int per_sm = 0;
+    NVFP4_TRY(cuda_call(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant2d_fused, 128, 0), "occupancy"));
+    if (per_sm < 1) return fail(NVFP4_ERR_CUDA, "fused 2D quantiser cannot be resident");
+    const int64_t items = 2 * batch * (rows / 16) * cdiv(cols, Q2F_COLS);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)per_sm * sms));
+    const uint16_t* wp = (const uint16_t*)w;
+    float* am = out->amax;
+    uint32_t* cnt = (uint32_t*)workspace;
+    uint8_t* codes = (uint8_t*)out->codes;
+    uint8_t* sf = out->sf;
+    void* args[] = {&wp, &batch, &rows, &cols, &ld, &am, &cnt, &codes, &sf, &tile_sf};
+    NVFP4_TRY(cuda_call(cudaLaunchCooperativeKernel((const void*)k_quant2d_fused, dim3(grid), dim3(128), args, 0, stream),
+                        "k_quant2d_fused launch"));
+    NVFP4_TRY(launched("k_quant2d_fused"));
+    if ((rows % 128) || ((cols / 16) % 4)) {
+        k_quant2d_pad<<<dim3(16, (unsigned)batch), 256, 0, stream>>>(out->sf, nullptr, rows, cols);
+        NVFP4_TRY(launched("k_quant2d_pad"));
+    }
+    return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_rht_amax(const void* x, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask, float* amax,
                             nvfp4_stream_t stream) {
     NVFP4_INJECT_CHECK();

@@ -380,37 +380,29 @@ __device__ __forceinline__ void transpose8x8_nibbles(uint32_t (&a)[8]) {
     }
 }
 
-// CTA = 64x64 block of one batch entry (blockIdx.z), 4 warps.  Warp w owns
-// rows 16w .. 16w+15 of the block: a 16x64 strip of four 16x16 tiles.  Lane l
-// loads four 16-byte vectors: row (l >> 3) + 4i, columns 8*(l & 7) .. +7, so
-// the lanes of a tile are those with equal (l & 7) >> 1 and the tile amax is
-// three xor-shuffles away.  W codes and the W rows' scales (4 tiles = 4
-// contiguous scale bytes per row) are stored straight from registers; for
-// W^T the code words go through shared memory and 64 threads each transpose
-// one 8x8 nibble block, so that every W^T row receives 32 contiguous bytes.
-__global__ void __launch_bounds__(128) k_quant2d(const uint16_t* __restrict__ w, int64_t rows,
-                                                 int64_t cols, int64_t ld, const float* __restrict__ amax,
-                                                 uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-                                                 uint8_t* __restrict__ codes_t, uint8_t* __restrict__ sf_t,
-                                                 uint8_t* __restrict__ tile_sf, float* __restrict__ amax_copy) {
-    __shared__ uint32_t s_cw[64][9];        // code words [row of the block][8-column group] (+1 pad)
-    __shared__ uint32_t s_sc[4][4];         // tile scales [warp][tile]
-    const int b = blockIdx.z;
-    const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
-    const uint16_t* wb = w + (int64_t)b * rows * ld;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (amax_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) amax_copy[b] = amax[b];
-    const int64_t rs = r0 + 16 * warp;                  // first row of this warp's strip
-    const bool rows_ok = rs < rows;                     // rows % 16 == 0: a strip is all in or all out
-    const int c8 = lane & 7;
-    const bool col_ok = c0 + 8 * c8 < cols;             // cols % 16 == 0: 8-column groups are all in or out
-    uint4 v[4];
+// One warp's 16x64 strip (rows rs .. rs+15, columns c0 .. c0+63, four 16x16
+// tiles) of batch entry b: loads, tile amax, scales, W codes and the W rows'
+// scale words.  Returns the four code words and the strip's scale word (tile
+// t in byte t) for the W^T stage.  Lane l handles row (l >> 3) + 4i,
+// columns 8*(l & 7) .. +7.
+__device__ __forceinline__ void quant2d_strip_load(const uint16_t* __restrict__ wb, int64_t rows, int64_t cols,
+                                                   int64_t ld, int64_t rs, int64_t c0, uint4 (&v)[4]) {
+    const int lane = threadIdx.x & 31, c8 = lane & 7;
+    const bool ok = rs < rows && c0 + 8 * c8 < cols;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int64_t rr = rs + (lane >> 3) + 4 * i;
-        v[i] = (rows_ok && col_ok) ? __ldg(reinterpret_cast<const uint4*>(wb + rr * ld + c0 + 8 * c8))
-                                   : make_uint4(0, 0, 0, 0);
+        v[i] = ok ? __ldg(reinterpret_cast<const uint4*>(wb + rr * ld + c0 + 8 * c8)) : make_uint4(0, 0, 0, 0);
     }
+}
+
+__device__ __forceinline__ void quant2d_strip_encode(const uint4 (&v)[4], int64_t rows, int64_t cols, int64_t b,
+                                                     int64_t rs, int64_t c0, float s_enc, uint8_t* __restrict__ codes,
+                                                     uint8_t* __restrict__ sf, uint8_t* __restrict__ tile_sf,
+                                                     uint32_t (&cw)[4], uint32_t& word) {
+    const int lane = threadIdx.x & 31, c8 = lane & 7;
+    const bool rows_ok = rs < rows;                     // rows % 16 == 0: a strip is all in or all out
+    const bool col_ok = c0 + 8 * c8 < cols;             // cols % 16 == 0: 8-column groups are all in or out
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) m = absmax_bits(v[i], m);
@@ -418,56 +410,216 @@ __global__ void __launch_bounds__(128) k_quant2d(const uint16_t* __restrict__ w,
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-    const float s_enc = tensor_encode_scale(amax[b]);
     const uint32_t sc = block_scale(__uint_as_float(m << 16), s_enc);
     const float ratio = sc ? element_ratio(s_enc, sc) : 0.0f;
-    uint32_t cw[4];
     const PhiloxKeys no_key{};
 #pragma unroll
     for (int i = 0; i < 4; ++i) cw[i] = encode8<false>(v[i], ratio, sc == 0, no_key, 0);
     // scales of the strip's four tiles (tile t is held by lane 2t)
-    const uint32_t word = __shfl_sync(0xFFFFFFFFu, sc, 0) | (__shfl_sync(0xFFFFFFFFu, sc, 2) << 8) |
-                          (__shfl_sync(0xFFFFFFFFu, sc, 4) << 16) | (__shfl_sync(0xFFFFFFFFu, sc, 6) << 24);
-    const int64_t ebytes = rows * cols / 2;
-    if (rows_ok) {
-        uint8_t* cb = codes + b * ebytes;
-        if (col_ok) {
+    word = __shfl_sync(0xFFFFFFFFu, sc, 0) | (__shfl_sync(0xFFFFFFFFu, sc, 2) << 8) |
+           (__shfl_sync(0xFFFFFFFFu, sc, 4) << 16) | (__shfl_sync(0xFFFFFFFFu, sc, 6) << 24);
+    if (!rows_ok) return;
+    uint8_t* cb = codes + b * (rows * cols / 2);
+    if (col_ok) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int64_t rr = rs + (lane >> 3) + 4 * i;
-                *reinterpret_cast<uint32_t*>(cb + rr * (cols / 2) + (c0 + 8 * c8) / 2) = cw[i];
-            }
+        for (int i = 0; i < 4; ++i) {
+            const int64_t rr = rs + (lane >> 3) + 4 * i;
+            *reinterpret_cast<uint32_t*>(cb + rr * (cols / 2) + (c0 + 8 * c8) / 2) = cw[i];
         }
-        if (lane < 16)
-            *reinterpret_cast<uint32_t*>(sf + b * sf_bytes(rows, cols) + sf_offset(rs + lane, c0 / 16, cols)) = word;
-        if (tile_sf != nullptr && lane < 8 && (lane & 1) == 0 && col_ok)
-            tile_sf[(int64_t)b * (rows / 16) * (cols / 16) + (rs / 16) * (cols / 16) + c0 / 16 + (lane >> 1)] = (uint8_t)sc;
     }
+    if (lane < 16)
+        *reinterpret_cast<uint32_t*>(sf + b * sf_bytes(rows, cols) + sf_offset(rs + lane, c0 / 16, cols)) = word;
+    if (tile_sf != nullptr && lane < 8 && (lane & 1) == 0 && col_ok)
+        tile_sf[b * (rows / 16) * (cols / 16) + (rs / 16) * (cols / 16) + c0 / 16 + (lane >> 1)] = (uint8_t)sc;
+}
+
+// One 64x64 block (rows r0.., columns c0..) of batch entry b, by 4 warps
+// (128 threads): warp w quantises the strip of rows r0 + 16w (as above); for
+// W^T the code words go through shared memory and 64 threads each transpose
+// one 8x8 nibble block, so that every W^T row receives 32 contiguous bytes.
+// Every thread of the block must call it.
+struct Quant2dSmem {
+    uint32_t cw[64][9];     // code words [row of the block][8-column group] (+1 pad)
+    uint32_t sc[4][4];      // tile scales [warp][tile]
+};
+
+__device__ __forceinline__ void quant2d_block(const uint16_t* __restrict__ wb, int64_t rows, int64_t cols,
+                                              int64_t ld, int64_t b, int64_t r0, int64_t c0, float s_enc,
+                                              uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                              uint8_t* __restrict__ codes_t, uint8_t* __restrict__ sf_t,
+                                              uint8_t* __restrict__ tile_sf, Quant2dSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t rs = r0 + 16 * warp;
+    const bool rows_ok = rs < rows;
+    const int c8 = lane & 7;
+    uint4 v[4];
+    quant2d_strip_load(wb, rows, cols, ld, rs, c0, v);
+    uint32_t cw[4], word;
+    quant2d_strip_encode(v, rows, cols, b, rs, c0, s_enc, codes, sf, tile_sf, cw, word);
+    const int64_t ebytes = rows * cols / 2;
     if (codes_t == nullptr) return;
     // ---- W^T: stage the code words, transpose 8x8 nibble blocks
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s_cw[16 * warp + (lane >> 3) + 4 * i][c8] = cw[i];
-    if (lane < 4) s_sc[warp][lane] = rows_ok ? (word >> (8 * lane)) & 0xFFu : 0u;
+    for (int i = 0; i < 4; ++i) sm.cw[16 * warp + (lane >> 3) + 4 * i][c8] = cw[i];
+    if (lane < 4) sm.sc[warp][lane] = rows_ok ? (word >> (8 * lane)) & 0xFFu : 0u;
     __syncthreads();
-    if (threadIdx.x >= 64) return;
-    const int ng = threadIdx.x & 7, kg = threadIdx.x >> 3;     // rows 8ng.., columns 8kg..
-    uint32_t a[8];
+    if (threadIdx.x < 64) {
+        const int ng = threadIdx.x & 7, kg = threadIdx.x >> 3;     // rows 8ng.., columns 8kg..
+        uint32_t a[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) a[j] = s_cw[8 * ng + j][kg];
-    transpose8x8_nibbles(a);
-    const bool n_ok = r0 + 8 * ng < rows;
-    uint8_t* ctb = codes_t + b * ebytes;
+        for (int j = 0; j < 8; ++j) a[j] = sm.cw[8 * ng + j][kg];
+        transpose8x8_nibbles(a);
+        const bool n_ok = r0 + 8 * ng < rows;
+        uint8_t* ctb = codes_t + b * ebytes;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int64_t kk = c0 + 8 * kg + k;                    // W^T row = W column
-        if (n_ok && kk < cols) *reinterpret_cast<uint32_t*>(ctb + kk * (rows / 2) + (r0 + 8 * ng) / 2) = a[k];
+        for (int k = 0; k < 8; ++k) {
+            const int64_t kk = c0 + 8 * kg + k;                    // W^T row = W column
+            if (n_ok && kk < cols) *reinterpret_cast<uint32_t*>(ctb + kk * (rows / 2) + (r0 + 8 * ng) / 2) = a[k];
+        }
+        // W^T row c0 + t: the scales of the block's four row tiles are 4 contiguous bytes
+        const int64_t kk = c0 + threadIdx.x;
+        if (kk < cols) {
+            const int tj = threadIdx.x >> 4;
+            const uint32_t tw = sm.sc[0][tj] | (sm.sc[1][tj] << 8) | (sm.sc[2][tj] << 16) | (sm.sc[3][tj] << 24);
+            *reinterpret_cast<uint32_t*>(sf_t + b * sf_bytes(cols, rows) + sf_offset(kk, r0 / 16, rows)) = tw;
+        }
     }
-    // W^T row c0 + t: the scales of the block's four row tiles are 4 contiguous bytes
-    const int64_t kk = c0 + threadIdx.x;
-    if (kk < cols) {
-        const int tj = threadIdx.x >> 4;
-        const uint32_t tw = s_sc[0][tj] | (s_sc[1][tj] << 8) | (s_sc[2][tj] << 16) | (s_sc[3][tj] << 24);
-        *reinterpret_cast<uint32_t*>(sf_t + b * sf_bytes(cols, rows) + sf_offset(kk, r0 / 16, rows)) = tw;
+    __syncthreads();                                    // shared staging free for the next block
+}
+
+// CTA = one 64x64 block (blockIdx.x: columns, blockIdx.y: rows, blockIdx.z:
+// batch entry) with the entry's amax already known.
+__global__ void __launch_bounds__(128) k_quant2d(const uint16_t* __restrict__ w, int64_t rows,
+                                                 int64_t cols, int64_t ld, const float* __restrict__ amax,
+                                                 uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                 uint8_t* __restrict__ codes_t, uint8_t* __restrict__ sf_t,
+                                                 uint8_t* __restrict__ tile_sf, float* __restrict__ amax_copy) {
+    __shared__ Quant2dSmem sm;
+    const int64_t b = blockIdx.z;
+    if (amax_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) amax_copy[b] = amax[b];
+    quant2d_block(w + b * rows * ld, rows, cols, ld, b, (int64_t)blockIdx.y * 64, (int64_t)blockIdx.x * 64,
+                  tensor_encode_scale(amax[b]), codes, sf, codes_t, sf_t, tile_sf, sm);
+}
+
+// ------------------------------------------------------------------ fused 2D
+// Per-entry amax and 2D quantisation of a batched weight [batch, rows, cols]
+// (W codes and scales; no W^T) in one launch that reads every element from
+// HBM once: the second read of an entry, for the codes, hits L2.  Work items
+// are pieces of 16 rows x up to 1024 columns of one entry, either "amax" (max
+// |w| over the piece, merged into amax[e] with an atomic max, then counted in
+// counters[e]) or "quantise" (wait until counters[e] holds all of entry e's
+// pieces, then quantise the piece with amax[e]).  Items run in the fixed
+// order
+//     A(0) A(1) | A(2) Q(0) | A(3) Q(1) | ... | A(batch-1) Q(batch-3) | Q(batch-2) Q(batch-1)
+// (A(j) / Q(j): all amax / quantise items of entry j; a lag of two entries),
+// CTA c taking items c, c + grid, c + 2*grid, ...  With about 1.2 k CTAs
+// resident and 32 KB pieces, the data between an amax read and its re-read
+// stays well inside the 126 MB L2, and the lag lets the amax items of an
+// entry finish before its quantise items come up.  A quantise item waits
+// only on amax items earlier in the order and the launch is cooperative
+// (every CTA resident), so the waits end; each is bounded anyway: the first
+// to give up records DEV_TIMEOUT and raises counters[batch] (the abort word),
+// after which no item waits any more.  amax[batch] and counters[batch + 1]
+// must be zero on entry.
+constexpr int Q2F_LAG = 2;
+constexpr int64_t Q2F_COLS = 1024;
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(128, 8) k_quant2d_fused(const uint16_t* __restrict__ w, int64_t batch, int64_t rows,
+                                                          int64_t cols, int64_t ld, float* __restrict__ amax,
+                                                          uint32_t* __restrict__ counters,
+                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                          uint8_t* __restrict__ tile_sf) {
+    __shared__ uint32_t s_red[4];
+    __shared__ float s_amax;
+    const int64_t ncc = (cols + Q2F_COLS - 1) / Q2F_COLS;      // column pieces per strip
+    const int64_t np = (rows / 16) * ncc;                        // pieces per entry
+    const int64_t lag = batch < Q2F_LAG ? batch : Q2F_LAG;
+    const int64_t head = lag * np;
+    const int64_t mid = (batch - lag) * 2 * np;
+    const int64_t items = 2 * batch * np;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        bool is_amax;
+        int64_t e, pc;
+        if (it < head) {
+            is_amax = true; e = it / np; pc = it % np;
+        } else if (it - head < mid) {
+            const int64_t i2 = it - head, j = lag + i2 / (2 * np), k = i2 % (2 * np);
+            is_amax = k < np;
+            e = is_amax ? j : j - lag;
+            pc = is_amax ? k : k - np;
+        } else {
+            const int64_t i3 = it - head - mid;
+            is_amax = false; e = (batch - lag) + i3 / np; pc = i3 % np;
+        }
+        const uint16_t* wb = w + e * rows * ld;
+        const int64_t rs = (pc / ncc) * 16;
+        const int64_t cb = (pc % ncc) * Q2F_COLS;
+        const int64_t cn = min(Q2F_COLS, cols - cb);
+        if (is_amax) {
+            const uint32_t upr = (uint32_t)(cn >> 3);
+            const uint32_t units = 16u * upr;
+            const uint16_t* base = wb + rs * ld + cb;
+            uint32_t acc = 0;
+            uint32_t u = threadIdx.x;
+            for (; u + 3 * 128 < units; u += 4 * 128) {
+                uint4 v[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t ui = u + 128 * i;
+                    v[i] = __ldg(reinterpret_cast<const uint4*>(base + (ui / upr) * ld + (ui % upr) * 8));
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc = absmax_bits(v[i], acc);
+            }
+            for (; u < units; u += 128)
+                acc = absmax_bits(__ldg(reinterpret_cast<const uint4*>(base + (u / upr) * ld + (u % upr) * 8)), acc);
+            uint32_t mbits = __float_as_uint(bits_to_amax(acc));
+            mbits = __reduce_max_sync(0xFFFFFFFFu, mbits);
+            if (lane == 0) s_red[warp] = mbits;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                const uint32_t mm = max(max(s_red[0], s_red[1]), max(s_red[2], s_red[3]));
+                if (mm != 0u) atomicMax(reinterpret_cast<unsigned int*>(amax + e), mm);
+                __threadfence();
+                atomicAdd(counters + e, 1u);
+            }
+            __syncthreads();
+        } else {
+            if (threadIdx.x == 0) {
+                const uint64_t t0 = globaltimer_ns();
+                bool ok = true;
+                while (ld_acquire_u32(counters + e) < (uint32_t)np) {
+                    __nanosleep(128);
+                    if (ld_acquire_u32(counters + batch) != 0u) { ok = false; break; }
+                    if (globaltimer_ns() - t0 > 4000000000ull) {
+                        raise_status(DEV_TIMEOUT);
+                        atomicExch(counters + batch, 1u);
+                        ok = false;
+                        break;
+                    }
+                }
+                s_amax = ok ? *reinterpret_cast<volatile float*>(amax + e) : -1.0f;
+            }
+            __syncthreads();
+            const float am = s_amax;
+            __syncthreads();
+            if (am < 0.0f) continue;                            // gave up waiting (recorded)
+            const float s_enc = tensor_encode_scale(am);
+            // warp w takes the 64-column blocks w, w + 4, ... of the piece
+            for (int64_t c0 = cb + 64 * warp; c0 < cb + cn; c0 += 256) {
+                uint4 v[4];
+                quant2d_strip_load(wb, rows, cols, ld, rs, c0, v);
+                uint32_t cw[4], word;
+                quant2d_strip_encode(v, rows, cols, e, rs, c0, s_enc, codes, sf, tile_sf, cw, word);
+            }
+        }
     }
 }
 

@@ -85,6 +85,9 @@ def test_other_entry_points_validation(L):
     assert L.nvfp4_grouped_gemm(ctypes.byref(a), None, 4, ctypes.byref(b), 48, FAKE, 48, 0, None) == 1
     assert L.nvfp4_grouped_gemm(ctypes.byref(a), FAKE, 2000, ctypes.byref(b), 48, FAKE, 48, 0, None) == 7
     assert L.nvfp4_quantize_1d_grouped(FAKE, 64, 32, 32, FAKE, 0, 0, 0, None, ctypes.byref(_t(64, 32)), None) == 7
+    assert L.nvfp4_quantize_2d_fused(FAKE, 2, 32, 32, 32, None, 64, ctypes.byref(_t(32, 32)), None, None) == 1
+    assert L.nvfp4_quantize_2d_fused(FAKE, 2, 32, 32, 32, FAKE, 4, ctypes.byref(_t(32, 32)), None, None) == 2
+    assert L.nvfp4_quantize_2d_fused_workspace(512) == 2064
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")

@@ -160,3 +160,24 @@ def test_quantize_1d_ties_signed_zeros_saturation(B, orc):
     ref = orc.quantize_2d(w, amax_in=[2688.0])
     assert (np_u8(qw.codes).reshape(ref["codes"].shape) == ref["codes"]).all()
     assert (np_u8(qt.codes).reshape(ref["codes_t"].shape) == ref["codes_t"]).all()
+
+
+@pytest.mark.parametrize("batch,rows,cols", [(1, 48, 80), (2, 144, 1040), (5, 320, 256), (3, 64, 64),
+                                             (7, 2688 // 8, 1024 // 8), (4, 16, 3072)])
+def test_quantize_2d_fused(B, orc, batch, rows, cols):
+    """One-pass (amax in the same cooperative launch) 2D quantisation gives
+    the oracle's bytes, for one entry and several, one 16-row strip per entry
+    and many, and a column count that leaves a partial 256-column sweep."""
+    g = torch.Generator().manual_seed(batch * 1000 + rows + cols)
+    w = (torch.randn(batch, rows, cols, generator=g) * 0.02 *
+         torch.exp(torch.rand(batch, 1, 1, generator=g) * 6 - 3)).to(torch.bfloat16)
+    ws = torch.full((B.quantize_2d_fused_workspace(batch),), 0xAB, dtype=torch.uint8, device="cuda")
+    for _ in range(2):   # the call re-zeroes its workspace
+        qw, tile = B.quantize_2d_fused(w.cuda(), want_tile_sf=True, workspace=ws)
+        torch.cuda.synchronize()
+        ref = orc.quantize_2d(w, want_t=False)
+        assert (np_u8(qw.amax) == ref["amax"]).all()
+        assert (np_u8(qw.codes).reshape(ref["codes"].shape) == ref["codes"]).all()
+        assert (np_u8(qw.sf) == ref["sf"]).all()
+        assert (np_u8(tile) == ref["tile_sf"]).all()
+    assert B.device_status() == 0
