@@ -196,6 +196,27 @@ nvfp4_status nvfp4_quantize_2d_fused(const void *w, int64_t batch, int64_t rows,
                                      void *workspace, size_t workspace_bytes, nvfp4_tensor *out,
                                      uint8_t *tile_sf, nvfp4_stream_t stream);
 
+/* Largest batch of nvfp4_quantize_2d_fused_static. */
+#define NVFP4_STATIC_MAX_BATCH 4096
+
+/* nvfp4_quantize_2d_fused without a caller workspace, for callers that cannot
+ * allocate device memory at the point of the call: code whose device memory
+ * is owned by another allocator that has no workspace to lend, or a loop that
+ * must not call cudaMalloc (it can synchronise the device and take locks).
+ * The per-entry counters live in a fixed array inside the library
+ * ((NVFP4_STATIC_MAX_BATCH + 4) * 4 bytes, held by every GPU that loads the
+ * library until the process exits); the call allocates nothing.
+ * batch > NVFP4_STATIC_MAX_BATCH returns NVFP4_ERR_LIMIT.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.
+ * Every call zeroes and reuses the same array, so two calls that overlap on
+ * the GPU (other streams, other host threads) race and corrupt each other.
+ * Other arguments and results as for nvfp4_quantize_2d_fused.  The pages
+ * have no counterpart of this entry point: it only changes where scratch
+ * memory comes from. */
+nvfp4_status nvfp4_quantize_2d_fused_static(const void *w, int64_t batch, int64_t rows, int64_t cols, int64_t ld,
+                                            nvfp4_tensor *out, uint8_t *tile_sf, nvfp4_stream_t stream);
+
 /* amax of the RHT output of x (bf16 [tokens, cols], row stride ld,
  * tokens % 16 == 0) -> amax (device, 1 float). */
 nvfp4_status nvfp4_rht_amax(const void *x, int64_t tokens, int64_t cols, int64_t ld,

@@ -23,12 +23,15 @@ OUT_BF16, OUT_FP32 = 0, 1
 DEV_TIMEOUT, DEV_BAD_OFFSETS = 1, 2
 MAX_GROUPS = 1024
 
+STATIC_MAX_BATCH = 4096
+
 STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_NULL", 2: "NVFP4_ERR_SHAPE", 3: "NVFP4_ERR_ALIGN",
           4: "NVFP4_ERR_DEVICE", 5: "NVFP4_ERR_CUDA", 6: "NVFP4_ERR_TIMEOUT", 7: "NVFP4_ERR_LIMIT"}
 
 EXPORTS = ["nvfp4_sf_bytes", "nvfp4_sf_bytes_grouped", "nvfp4_sf_offset", "nvfp4_amax",
            "nvfp4_quantize_1d", "nvfp4_quantize_1d_grouped", "nvfp4_quantize_2d",
-           "nvfp4_quantize_2d_fused_workspace", "nvfp4_quantize_2d_fused", "nvfp4_rht_amax",
+           "nvfp4_quantize_2d_fused_workspace", "nvfp4_quantize_2d_fused", "nvfp4_quantize_2d_fused_static",
+           "nvfp4_rht_amax",
            "nvfp4_rht_quantize", "nvfp4_gemm", "nvfp4_grouped_gemm", "nvfp4_status_string",
            "nvfp4_last_error", "nvfp4_device_status", "nvfp4_launch_count", "nvfp4_debug_inject",
            "nvfp4_debug_wait_timeout"]
@@ -70,6 +73,7 @@ def lib():
             "nvfp4_quantize_2d": (st, [P, i64, i64, i64, i64, P, TP, TP, P, P]),
             "nvfp4_quantize_2d_fused_workspace": (ctypes.c_size_t, [i64]),
             "nvfp4_quantize_2d_fused": (st, [P, i64, i64, i64, i64, P, ctypes.c_size_t, TP, P, P]),
+            "nvfp4_quantize_2d_fused_static": (st, [P, i64, i64, i64, i64, TP, P, P]),
             "nvfp4_rht_amax": (st, [P, i64, i64, i64, ctypes.c_uint16, P, P]),
             "nvfp4_rht_quantize": (st, [P, i64, i64, i64, ctypes.c_uint16, ctypes.c_int, u64, P, TP, P]),
             "nvfp4_gemm": (st, [TP, TP, P, i64, ctypes.c_int, P]),
@@ -226,6 +230,24 @@ def quantize_2d_fused(w: torch.Tensor, want_tile_sf: bool = False, workspace: Op
     _check(lib().nvfp4_quantize_2d_fused(_ptr(w3), batch, rows, cols, w3.stride(1), _ptr(workspace),
                                          workspace.numel() * workspace.element_size(), ctypes.byref(co),
                                          _ptr(tile), _stream(stream)))
+    return out, tile
+
+
+def quantize_2d_fused_static(w: torch.Tensor, want_tile_sf: bool = False, out: Optional[QTensor] = None,
+                             stream=None):
+    """quantize_2d_fused with the library's own fixed scratch instead of a
+    workspace (for callers that cannot allocate at the call); at most
+    STATIC_MAX_BATCH entries, and calls must not overlap on the GPU."""
+    w3 = w.unsqueeze(0) if w.dim() == 2 else w
+    batch, rows, cols = w3.shape
+    assert w3.dtype == torch.bfloat16 and w3.stride(2) == 1 and (batch == 1 or w3.stride(0) == rows * w3.stride(1))
+    dev = w.device
+    if out is None:
+        out = empty_qtensor(rows, cols, dev, batch=batch, n_amax=batch)
+    tile = torch.empty(batch, rows // 16, cols // 16, dtype=torch.uint8, device=dev) if want_tile_sf else None
+    co = out.c()
+    _check(lib().nvfp4_quantize_2d_fused_static(_ptr(w3), batch, rows, cols, w3.stride(1), ctypes.byref(co),
+                                                _ptr(tile), _stream(stream)))
     return out, tile
 
 

@@ -390,6 +390,40 @@ nvfp4_status nvfp4_quantize_2d_fused(const void* w, int64_t batch, int64_t rows,
     return NVFP4_OK;
 }
 
+// ------------------------------------------------------------------ allocation-free variant
+// Counter scratch of nvfp4_quantize_2d_fused_static: one word per batch entry
+// plus the abort word, in a fixed array that every GPU loading this library
+// holds until the process exits.  Host code must not pass the symbol itself
+// to a kernel (on the host it only names a stand-in); the device address is
+// looked up once per device with that device current.
+static __device__ __align__(256) uint32_t g_q2f_static_scratch[NVFP4_STATIC_MAX_BATCH + 4];
+
+namespace {
+uint32_t* g_static_scratch_ptr[64] = {};
+}
+
+nvfp4_status nvfp4_quantize_2d_fused_static(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ld,
+                                            nvfp4_tensor* out, uint8_t* tile_sf, nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    if (batch > NVFP4_STATIC_MAX_BATCH)
+        return fail(NVFP4_ERR_LIMIT, "batch=%lld exceeds the %d entries of the static scratch; use nvfp4_quantize_2d_fused "
+                    "with a workspace", (long long)batch, NVFP4_STATIC_MAX_BATCH);
+    int sms = 0, dev = 0;
+    NVFP4_TRY(check_device(&sms, &dev));
+    uint32_t* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (g_static_scratch_ptr[dev] == nullptr) {
+            void* p = nullptr;
+            NVFP4_TRY(cuda_call(cudaGetSymbolAddress(&p, g_q2f_static_scratch), "cudaGetSymbolAddress(static scratch)"));
+            g_static_scratch_ptr[dev] = static_cast<uint32_t*>(p);
+        }
+        scratch = g_static_scratch_ptr[dev];
+    }
+    return nvfp4_quantize_2d_fused(w, batch, rows, cols, ld, scratch, sizeof(g_q2f_static_scratch), out, tile_sf,
+                                   stream);
+}
+
 nvfp4_status nvfp4_rht_amax(const void* x, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask, float* amax,
                             nvfp4_stream_t stream) {
     NVFP4_INJECT_CHECK();
