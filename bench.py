@@ -20,7 +20,9 @@ bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -39,7 +41,7 @@ FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense FP4 : BF16 tensor throughput on
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=["ultra", "super"], default="ultra")
@@ -47,6 +49,46 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
+
+
+# Sources of the dense GEMM kernel; the ncu traffic figure committed under
+# profiles/ is only reported while they are unchanged since its capture.
+GEMM_SOURCES = ("nvfp4_precision_02_b300/csrc/gemm.cuh", "nvfp4_precision_02_b300/csrc/common.cuh",
+                "nvfp4_precision_02_b300/csrc/nvfp4.cu")
+
+
+def source_hash(paths=GEMM_SOURCES) -> str:
+    h = hashlib.sha256()
+    for f in paths:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(summary: str):
+    """DRAM bytes per launch from a committed ncu summary (lines
+    `dram_bytes_per_launch: N` and `kernel_source_sha256: H`), or None when the
+    summary is missing or the kernel sources changed after the capture."""
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    b = re.search(r"dram_bytes_per_launch:\s*(\d+)", text)
+    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    if not b or not h or h.group(1) != source_hash():
+        return None
+    return int(b.group(1))
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def peaks():
@@ -200,10 +242,11 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 def oracle_sample(which: str, budget_s: float):
-    """Time the oracle on a bounded slice of every op of the step and
-    extrapolate by element / multiply-add counts.  Returns (seconds per full
-    step, description, threads)."""
-    import numpy as np
+    """Time the oracle on bounded slices of every op of the step and
+    extrapolate by element / multiply-add counts.  Each op is timed once on a
+    small slice, then once on a slice sized to take about budget_s / 5
+    seconds, which gives the reported rate.  Returns (seconds per full step,
+    description, threads)."""
     import torch
     import oracle as orc
     from nvfp4_precision_02_b300 import workloads as wl
@@ -213,26 +256,53 @@ def oracle_sample(which: str, budget_s: float):
     T, K, N = d.tokens, d.hidden, d.out
     R = m.tokens * m.topk
     E, L, Hh = m.experts, m.latent, m.expert_hidden
-    scale = max(0.05, min(1.0, budget_s / 20.0))
-    rows = max(16, int(256 * scale)) // 16 * 16
     g = torch.Generator().manual_seed(0)
-    xs = (torch.randn(rows, K, generator=g)).to(torch.bfloat16)
-    dys = (torch.randn(rows, N, generator=g) * 1e-3).to(torch.bfloat16)
-    per = {}
-    t0 = time.perf_counter(); qx = orc.quantize_1d(xs); per["q1d_rne"] = (time.perf_counter() - t0) / xs.numel()
-    t0 = time.perf_counter(); orc.quantize_1d(dys, orc.SR, 7); per["q1d_sr"] = (time.perf_counter() - t0) / dys.numel()
-    t0 = time.perf_counter(); orc.quantize_2d(xs[:, :K]); per["q2d"] = (time.perf_counter() - t0) / xs.numel()
-    t0 = time.perf_counter(); orc.rht_quantize(dys, 0x1234, orc.SR, 9); per["rht"] = (time.perf_counter() - t0) / dys.numel()
-    mm = max(8, int(64 * scale))
-    A = orc.dequantize(qx, rows, K)[:mm]
-    Bm = orc.dequantize(qx, rows, K)[:mm]
-    t0 = time.perf_counter(); orc.gemm(A, Bm); per["gemm_mac"] = (time.perf_counter() - t0) / (mm * mm * K)
+    target = budget_s / 5.0
+
+    def timed(fn, units):
+        t0 = time.perf_counter()
+        fn()
+        return (time.perf_counter() - t0), units
+
+    def grow(make, n0, nmax, power=1):
+        dt, _ = make(n0)
+        n = int(n0 * (target / max(dt, 1e-4)) ** (1.0 / power))
+        n = max(n0, min(nmax, n // 16 * 16))
+        dt, units = make(n)
+        return dt / units, n
+
+    def q_op(kind):
+        def make(rows):
+            if kind == "q1d_rne":
+                x = torch.randn(rows, K, generator=g).to(torch.bfloat16)
+                return timed(lambda: orc.quantize_1d(x), x.numel())
+            if kind == "q2d":
+                x = torch.randn(rows, K, generator=g).to(torch.bfloat16)
+                return timed(lambda: orc.quantize_2d(x), x.numel())
+            x = (torch.randn(rows, N, generator=g) * 1e-3).to(torch.bfloat16)
+            if kind == "q1d_sr":
+                return timed(lambda: orc.quantize_1d(x, orc.SR, 7), x.numel())
+            return timed(lambda: orc.rht_quantize(x, 0x1234, orc.SR, 9), x.numel())
+        return make
+
+    per, sizes = {}, {}
+    for kind in ("q1d_rne", "q1d_sr", "q2d", "rht"):
+        per[kind], sizes[kind] = grow(q_op(kind), 64, T)
+
+    def gemm_make(mm):
+        A = torch.randn(mm, K, generator=g, dtype=torch.float64).numpy()
+        Bm = torch.randn(mm, K, generator=g, dtype=torch.float64).numpy()
+        return timed(lambda: orc.gemm(A, Bm), mm * mm * K)
+
+    per["gemm_mac"], mm = grow(gemm_make, 32, 4096, power=2)
     elems = {"q1d_rne": T * K + R * L + R * Hh, "q1d_sr": T * N, "q2d": N * K + 2 * E * Hh * L,
              "rht": T * N + T * K}
     macs = T * N * K * 3 + 2 * R * Hh * L
     sec = sum(per[k] * v for k, v in elems.items()) + per["gemm_mac"] * macs
-    desc = (f"oracle on {rows} rows of X [.,{K}] and dY [.,{N}] (1D RNE/SR, 2D, RHT) and a {mm}x{mm}x{K} "
-            f"FP64 GEMM; per-element and per-multiply-add times extrapolated to the full step")
+    desc = (f"oracle on {sizes['q1d_rne']}/{sizes['q1d_sr']}/{sizes['q2d']}/{sizes['rht']} rows of the step's "
+            f"X [.,{K}] / dY [.,{N}] for 1D RNE / 1D SR / 2D / RHT+SR and a {mm}x{mm}x{K} FP64 GEMM, each slice "
+            f"sized to take about {target:.1f} s; per-element and per-multiply-add times extrapolated to the "
+            f"full step")
     return sec, desc, orc.num_threads()
 
 
@@ -291,11 +361,7 @@ def main():
         torch.distributed.barrier()
     launches = B.launch_count() - launches0
     clk = clocks.stop()
-    total_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
     ms_step = total_ms / args.steps
     op_ms = [statistics.median(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps))
              for i in range(nops)]
@@ -316,16 +382,19 @@ def main():
         else:
             ops[n] = {"ms": round(t, 4), "gbs": round(w / (t * 1e-3) / 1e9, 1),
                       "frac_hbm": round(w / (t * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
-    # dominant kernel: the dense GEMM (three launches per step, same FLOPs each)
-    dense = [t for (n, k, _), t in zip(wk.ops, op_ms) if n.startswith("gemm ")]
-    d = wk.dense
-    dense_flops = 2.0 * d.tokens * d.out * d.hidden
-    achieved = dense_flops / (statistics.mean(dense) * 1e-3) / 1e12
-    roofline = {"kernel": "k_gemm_nvfp4 (dense fprop/dgrad/wgrad)", "bound": "tensor",
+    # dominant kernel: k_gemm_nvfp4; its roofline is given for the fprop launch
+    fprop_i = [n for n, _, _ in wk.ops].index("gemm fprop")
+    fprop_flops = wk.ops[fprop_i][2]
+    achieved = fprop_flops / (op_ms[fprop_i] * 1e-3) / 1e12
+    traffic = profiled_traffic(f"k_gemm_nvfp4_fprop_{args.workload}.md")
+    roofline = {"kernel": "k_gemm_nvfp4 (fprop launch)", "bound": "tensor",
                 "achieved": round(achieved, 1), "peak": round(fp4_peak_sust, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / fp4_peak_sust, 4),
                 "peak_note": f"{pk['source']} sustained bf16 x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
-                "frac_of_burst": round(achieved / fp4_peak_burst, 4), "traffic": None}
+                "frac_of_burst": round(achieved / fp4_peak_burst, 4),
+                "traffic": traffic, "traffic_unit": "bytes per launch (ncu dram read + write)",
+                "algorithmic_bytes": int(0.5625 * (wk.dense.tokens + wk.dense.out) * wk.dense.hidden
+                                         + 2 * wk.dense.tokens * wk.dense.out)}
     q_dy = op_ms[3]
     roofline_q = {"kernel": "k_amax + k_quant1d<SR> (dY 1x16 SR)", "bound": "hbm",
                   "achieved": round(wk.ops[3][2] / (q_dy * 1e-3) / 1e9, 1), "peak": pk["hbm_gbs"],
@@ -347,11 +416,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
         "data": "synthetic (seeded device generators; no dataset)",
-        "config": {"workload": f"{args.workload}_full_step", "dense_tokens": d.tokens, "hidden": d.hidden,
-                   "in_proj_out": d.out, "moe_tokens": wk.moe.tokens, "moe_latent": wk.moe.latent,
-                   "moe_expert_hidden": wk.moe.expert_hidden, "experts": wk.moe.experts, "topk": wk.moe.topk,
-                   "moe_rows": wk.R, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (tens of GB streamed per step); no flush"},
+        "config": workload_config(args.workload, d, wk.moe, wk.R, world),
         "gemm_tflops": round(wk.gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
         "quantize_gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1),
         "quantize_frac_hbm": round(quant_bytes / (quant_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
@@ -414,30 +479,44 @@ def measure_e2e(wk: Workload, steps: int, dev):
 
 def reference_arm(args):
     """The CPU oracle as the reference arm: each step runs a bounded sample of
-    the workload on the host cores; value is extrapolated to the full step."""
-    times = []
-    desc, th, sec = "", 1, 0.0
+    the workload on the host cores (sized so the whole run stays within a few
+    minutes); value is the full step's GEMM FLOPs over the extrapolated time
+    of a full step, averaged over the timed steps."""
+    budget = max(0.5, min(4.0, 120.0 / max(1, args.steps + args.warmup)))
+    secs, walls = [], []
+    desc, th = "", 1
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        sec, desc, th = oracle_sample(args.workload, budget_s=4.0)
+        sec, desc, th = oracle_sample(args.workload, budget_s=budget)
         if i >= args.warmup:
-            times.append(time.perf_counter() - t0)
+            secs.append(sec)
+            walls.append(time.perf_counter() - t0)
     from nvfp4_precision_02_b300 import workloads as wl
     d = wl.ULTRA_DENSE if args.workload == "ultra" else wl.SUPER_DENSE
     m = wl.ULTRA_MOE if args.workload == "ultra" else wl.SUPER_MOE
     R = m.tokens * m.topk
     flops = 3 * 2.0 * d.tokens * d.out * d.hidden + 2 * 2.0 * R * m.expert_hidden * m.latent
+    sec = statistics.mean(secs)
     value = flops / sec / 1e12
+    config = workload_config(args.workload, d, m, R, 1)
+    config["sample_wall_s_per_step"] = round(statistics.mean(walls), 2)
     line = {"metric": METRIC, "value": round(value, 9), "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 1),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
-            "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"{args.workload}_full_step", "sample_wall_s": round(statistics.mean(times), 2)},
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference", "config": config,
             "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": th, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def workload_config(which, d, m, rows, world):
+    return {"workload": f"{which}_full_step", "dense_tokens": d.tokens, "hidden": d.hidden,
+            "in_proj_out": d.out, "moe_tokens": m.tokens, "moe_latent": m.latent,
+            "moe_expert_hidden": m.expert_hidden, "experts": m.experts, "topk": m.topk,
+            "moe_rows": rows, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (tens of GB streamed per step); no flush"}
 
 
 if __name__ == "__main__":
