@@ -284,6 +284,56 @@ __device__ __forceinline__ void tc_st_x32(uint32_t taddr, const uint4 (&v)[8]) {
 }
 
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// Lane/chunk exchange for coalesced row stores.  On entry lane l holds 32
+// words of row l of a 32-row block (chunk c = words 4c .. 4c+3, 16 bytes).
+// Three xor-shuffle stages swap lane bits 2..4 with chunk bits 0..2; on exit
+// chunk x of lane L holds chunk (L >> 2) of row 4x + (L & 3), so the warp's
+// 16-byte store of chunk x writes four whole 128-byte row segments instead of
+// 16 bytes in each of 32 rows (8x fewer L1 wavefronts).
+__device__ __forceinline__ void rows_to_segments(uint32_t (&w)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const int m = 1 << i;
+        const bool up = (lane >> (2 + i)) & 1;
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+            if (x & m) continue;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t send = up ? w[4 * x + j] : w[4 * (x | m) + j];
+                const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, 4 << i);
+                if (up) w[4 * x + j] = recv;
+                else w[4 * (x | m) + j] = recv;
+            }
+        }
+    }
+}
+
+// Store a 32-row x 16-chunk block after rows_to_segments: chunk x of lane L
+// goes to row row_base + 4x + (L & 3), byte offset 16 * (L >> 2) past
+// col_ptr_base (rows ldc_bytes apart).  Rows at or beyond rows_valid and
+// bytes at or beyond bytes_valid (of the 128-byte segment) are skipped.
+__device__ __forceinline__ void store_segments(const uint32_t (&w)[32], uint8_t* base, int64_t ldc_bytes,
+                                               int rows_valid, int bytes_valid) {
+    const int lane = threadIdx.x & 31;
+    const int cb = 16 * (lane >> 2);
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+        const int rr = 4 * x + (lane & 3);
+        if (rr >= rows_valid) continue;
+        uint8_t* dst = base + (int64_t)rr * ldc_bytes + cb;
+        if (cb + 16 <= bytes_valid) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+        } else if (cb < bytes_valid) {
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+                if (cb + 2 * b < bytes_valid)
+                    *reinterpret_cast<uint16_t*>(dst + 2 * b) = (uint16_t)(w[4 * x + b / 2] >> (16 * (b & 1)));
+        }
+    }
+}
+
 // ------------------------------------------------------------------ tiles
 struct TileCoord {
     int g;            // group
@@ -524,7 +574,6 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             if (OUT_FP32) {
                 // two 32-column halves: load, scale, store; release after the second load
                 const bool live = r < tc.rows && col0 < p.N;
-                float* out = reinterpret_cast<float*>(p.c) + row * p.ldc + col0;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t v[32];
@@ -535,31 +584,28 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(acc_empty);
                     }
-                    if (live) {
+                    const int64_t cstart = col0 + 32 * h;
+                    if (cstart >= p.N) continue;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            const int cc = 32 * h + i;
-                            const float4 o = make_float4(__fmul_rn(alpha, __uint_as_float(v[i])),
-                                                         __fmul_rn(alpha, __uint_as_float(v[i + 1])),
-                                                         __fmul_rn(alpha, __uint_as_float(v[i + 2])),
-                                                         __fmul_rn(alpha, __uint_as_float(v[i + 3])));
-                            if (p.vec_store && col0 + cc + 4 <= p.N) {
-                                *reinterpret_cast<float4*>(out + cc) = o;
-                            } else {
-                                const float oo[4] = {o.x, o.y, o.z, o.w};
+                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[i])));
+                    if (p.vec_store) {
+                        // rows of this warp: tc.row0 + 32q .. ; 32 columns = 128 bytes per row
+                        rows_to_segments(v);
+                        store_segments(v, reinterpret_cast<uint8_t*>(reinterpret_cast<float*>(p.c) + (tc.row0 + q * 32) * p.ldc + cstart),
+                                       p.ldc * 4, tc.rows - q * 32, (int)(p.N - cstart >= 32 ? 128 : (p.N - cstart) * 4));
+                    } else if (live) {
+                        float* out = reinterpret_cast<float*>(p.c) + row * p.ldc + cstart;
 #pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    if (col0 + cc + j < p.N) out[cc + j] = oo[j];
-                            }
-                        }
+                        for (int i = 0; i < 32; ++i)
+                            if (cstart + i < p.N) out[i] = __uint_as_float(v[i]);
                     }
                 }
-            } else {
+            } else if (TMA_STORE) {
                 // two 32-column halves: load, scale, round; release after the second load.
                 // A half whose 32 rows all belong to the tile goes out as one TMA
                 // store box (32 x 32 bf16) from this warp's 64B-swizzled staging
                 // buffer; other rows are stored directly.
-                const bool rows_full = TMA_STORE && (q * 32 + 31) < tc.rows;
+                const bool rows_full = (q * 32 + 31) < tc.rows;
                 const uint32_t stage_buf = smem_u32(smem + L::STORE_OFF + (warp - G_W_EPI0) * G_STORE_WARP_BYTES);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -605,7 +651,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                         uint16_t* out = reinterpret_cast<uint16_t*>(p.c) + row * p.ldc + cstart;
 #pragma unroll
                         for (int i = 0; i < 32; i += 8) {
-                            if (p.vec_store && cstart + i + 8 <= p.N) {
+                            if (cstart + i + 8 <= p.N) {
                                 *reinterpret_cast<uint4*>(out + i) = make_uint4(w[i / 2], w[i / 2 + 1], w[i / 2 + 2], w[i / 2 + 3]);
                             } else {
 #pragma unroll
@@ -614,6 +660,38 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                             }
                         }
                     }
+                }
+            } else {
+                // 64 columns in four 16-column pieces: load, scale, round; release
+                // after the last load; then whole 128-byte row segments per store
+                uint32_t w[32];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t v[16];
+                    tc_ld_32x32b_x16(taddr + 16 * h, v);
+                    tc_wait_ld();
+                    if (h == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(v[2 * j])),
+                                                                        __fmul_rn(alpha, __uint_as_float(v[2 * j + 1])));
+                        w[8 * h + j] = *reinterpret_cast<const uint32_t*>(&b2);
+                    }
+                }
+                if (col0 >= p.N) continue;
+                if (p.vec_store) {
+                    rows_to_segments(w);
+                    store_segments(w, reinterpret_cast<uint8_t*>(reinterpret_cast<uint16_t*>(p.c) + (tc.row0 + q * 32) * p.ldc + col0),
+                                   p.ldc * 2, tc.rows - q * 32, (int)(p.N - col0 >= 64 ? 128 : (p.N - col0) * 2));
+                } else if (r < tc.rows) {
+                    uint16_t* out = reinterpret_cast<uint16_t*>(p.c) + row * p.ldc + col0;
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        if (col0 + i < p.N) out[i] = (uint16_t)(w[i / 2] >> (16 * (i & 1)));
                 }
             }
         }
