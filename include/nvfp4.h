@@ -204,7 +204,7 @@ nvfp4_status nvfp4_quantize_2d_fused(const void *w, int64_t batch, int64_t rows,
  * is owned by another allocator that has no workspace to lend, or a loop that
  * must not call cudaMalloc (it can synchronise the device and take locks).
  * The per-entry counters live in a fixed array inside the library
- * ((NVFP4_STATIC_MAX_BATCH + 4) * 4 bytes, held by every GPU that loads the
+ * ((NVFP4_STATIC_MAX_BATCH + 8) * 4 bytes, held by every GPU that loads the
  * library until the process exits); the call allocates nothing.
  * batch > NVFP4_STATIC_MAX_BATCH returns NVFP4_ERR_LIMIT.  The first call on
  * a device looks up the array's device address (cudaGetSymbolAddress) with

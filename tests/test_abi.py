@@ -88,6 +88,7 @@ def test_other_entry_points_validation(L):
     assert L.nvfp4_quantize_2d_fused(FAKE, 2, 32, 32, 32, None, 64, ctypes.byref(_t(32, 32)), None, None) == 1
     assert L.nvfp4_quantize_2d_fused(FAKE, 2, 32, 32, 32, FAKE, 4, ctypes.byref(_t(32, 32)), None, None) == 2
     assert L.nvfp4_quantize_2d_fused_workspace(512) == 2064
+    assert L.nvfp4_quantize_2d_fused_workspace(5) == 48
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
