@@ -154,8 +154,8 @@ class Workload:
             ("gemm wgrad", "tensor", gem(N, K, T)),
             ("quantize_2d W_up, W_down (amax+W)", "hbm", 4.5625 * 2 * E * Hh * L),
             ("quantize_1d_grouped A", "hbm", 4.5625 * R * L),
-            ("grouped_gemm up", "tensor", gem(R, Hh, L)),
-            ("quantize_1d_grouped H", "hbm", 4.5625 * R * Hh),
+            ("grouped_gemm up (+ per-expert amax of H)", "tensor", gem(R, Hh, L)),
+            ("quantize_1d_grouped H (amax from the GEMM)", "hbm", 2.5625 * R * Hh),
             ("grouped_gemm down", "tensor", gem(R, L, Hh)),
         ]
         self.gemm_flops = sum(w_ for _, k, w_ in self.ops if k == "tensor")
@@ -178,8 +178,9 @@ class Workload:
         B.quantize_2d(self.w_up, want_t=False, out=self.qwu)
         B.quantize_2d(self.w_down, want_t=False, out=self.qwd); mk(8)
         B.quantize_1d_grouped(self.a, self.offsets, B.RNE, 0, out=self.qa); mk(9)
-        B.grouped_gemm(self.qa, self.offsets, self.qwu, self.moe.expert_hidden, B.OUT_BF16, out=self.h); mk(10)
-        B.quantize_1d_grouped(self.h, self.offsets, B.RNE, 0, out=self.qh); mk(11)
+        B.grouped_gemm(self.qa, self.offsets, self.qwu, self.moe.expert_hidden, B.OUT_BF16, out=self.h,
+                       c_amax=self.qh.amax); mk(10)
+        B.quantize_1d_grouped(self.h, self.offsets, B.RNE, 0, amax_in=self.qh.amax, out=self.qh); mk(11)
         B.grouped_gemm(self.qh, self.offsets, self.qwd, self.moe.latent, B.OUT_BF16, out=self.o); mk(12)
 
 

@@ -184,9 +184,13 @@ size_t nvfp4_quantize_2d_fused_workspace(int64_t batch);
  * NULL (per-entry amax, W codes and GEMM-ready scales, optional tile scales)
  * for batched weights whose entries fit in L2, such as the LatentMoE expert
  * weights (2D block scaling of weights, Super summary "Infra design").  One
- * cooperative launch computes each entry's amax and quantises the entry while
- * it is still in L2, so HBM is read once instead of twice.  The transposed
- * copy is not produced (use nvfp4_quantize_2d for W^T).
+ * cooperative launch computes each entry's amax and then quantises the entry,
+ * re-reading it about one entry plus two items per warp later so that the
+ * second read can hit L2.  Whether it does depends on the L2 keeping that
+ * window: for the LatentMoE expert weights on B300 most of the second read
+ * still came from HBM and the two-launch nvfp4_quantize_2d was faster, so
+ * this entry point is an alternative, not the default.  The transposed copy
+ * is not produced (use nvfp4_quantize_2d for W^T).
  * workspace: device, caller-allocated, at least
  * nvfp4_quantize_2d_fused_workspace(batch) bytes, 16-byte aligned; the call
  * zeroes and uses it (per-entry arrival counters), so calls sharing one
@@ -243,9 +247,13 @@ nvfp4_status nvfp4_rht_quantize(const void *x, int64_t tokens, int64_t cols, int
  * a: [M, K], b: [N, K] (both K-major, a->cols == b->cols == K, K % 32 == 0
  * so that code rows are 16-byte multiples).  c: device [M, N], row stride
  * ldc elements, bf16 (one RNE rounding of the FP32 result) or FP32.
- * M, N >= 1 arbitrary. */
+ * M, N >= 1 arbitrary.  c_amax (device, 1 float, nullable): receives
+ * max |c| over the written outputs (of the stored bf16 values for a bf16 c),
+ * the tensor amax a following quantisation of c can take as amax_in instead
+ * of reading c again; it is zeroed by the call (left untouched when M or N
+ * is 0). */
 nvfp4_status nvfp4_gemm(const nvfp4_tensor *a, const nvfp4_tensor *b, void *c, int64_t ldc,
-                        nvfp4_out_dtype c_dtype, nvfp4_stream_t stream);
+                        nvfp4_out_dtype c_dtype, float *c_amax, nvfp4_stream_t stream);
 
 /* Grouped GEMM of the LatentMoE routed experts: for every group g,
  * C[offsets[g] .. offsets[g+1]-1, :] = alpha_g * A_g * W_g^T with
@@ -254,10 +262,13 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor *a, const nvfp4_tensor *b, void *c, i
  * nvfp4_quantize_2d with batch == num_groups, b->rows == n per expert,
  * b->cols == K.  offsets: device int64 [num_groups+1] as for the grouped
  * quantiser.  Rows of C outside [offsets[0], offsets[num_groups]) are not
- * written.  c: bf16 or FP32 [R, n], row stride ldc. */
+ * written.  c: bf16 or FP32 [R, n], row stride ldc.  c_amax (device,
+ * num_groups floats, nullable): per-group max |c| over the written outputs
+ * (the amax_in of a following grouped quantisation of c), zeroed by the
+ * call. */
 nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int64_t *offsets, int32_t num_groups,
                                 const nvfp4_tensor *b, int64_t n, void *c, int64_t ldc,
-                                nvfp4_out_dtype c_dtype, nvfp4_stream_t stream);
+                                nvfp4_out_dtype c_dtype, float *c_amax, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------- status */
 

@@ -76,8 +76,8 @@ def lib():
             "nvfp4_quantize_2d_fused_static": (st, [P, i64, i64, i64, i64, TP, P, P]),
             "nvfp4_rht_amax": (st, [P, i64, i64, i64, ctypes.c_uint16, P, P]),
             "nvfp4_rht_quantize": (st, [P, i64, i64, i64, ctypes.c_uint16, ctypes.c_int, u64, P, TP, P]),
-            "nvfp4_gemm": (st, [TP, TP, P, i64, ctypes.c_int, P]),
-            "nvfp4_grouped_gemm": (st, [TP, P, i32, TP, i64, P, i64, ctypes.c_int, P]),
+            "nvfp4_gemm": (st, [TP, TP, P, i64, ctypes.c_int, P, P]),
+            "nvfp4_grouped_gemm": (st, [TP, P, i32, TP, i64, P, i64, ctypes.c_int, P, P]),
             "nvfp4_status_string": (ctypes.c_char_p, [st]),
             "nvfp4_last_error": (ctypes.c_char_p, []),
             "nvfp4_device_status": (st, [ctypes.POINTER(ctypes.c_int32)]),
@@ -270,28 +270,31 @@ def rht_quantize(x: torch.Tensor, sign_mask: int, mode: int = RNE, seed: int = 0
 
 
 def gemm(a: QTensor, b: QTensor, out_dtype: int = OUT_BF16, out: Optional[torch.Tensor] = None,
-         stream=None) -> torch.Tensor:
-    """C[M, N] = alpha * A[M, K] . B[N, K]^T (both quantised, K-major)."""
+         stream=None, c_amax: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """C[M, N] = alpha * A[M, K] . B[N, K]^T (both quantised, K-major); c_amax
+    (float32 [1], optional) receives max |C|."""
     M, N = a.rows, b.rows
     if out is None:
         out = torch.empty(M, N, dtype=torch.float32 if out_dtype == OUT_FP32 else torch.bfloat16,
                           device=a.codes.device)
     ca, cb = a.c(), b.c()
     _check(lib().nvfp4_gemm(ctypes.byref(ca), ctypes.byref(cb), _ptr(out), out.stride(0), out_dtype,
-                            _stream(stream)))
+                            _ptr(c_amax), _stream(stream)))
     return out
 
 
 def grouped_gemm(a: QTensor, offsets: torch.Tensor, b: QTensor, n: int, out_dtype: int = OUT_BF16,
-                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Per expert g: C[o_g:o_{g+1}] = alpha_g * A_g . W_g^T; b is the batched [E, n, K] weight."""
+                 out: Optional[torch.Tensor] = None, stream=None,
+                 c_amax: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Per expert g: C[o_g:o_{g+1}] = alpha_g * A_g . W_g^T; b is the batched [E, n, K] weight;
+    c_amax (float32 [groups], optional) receives each group's max |C|."""
     groups = offsets.numel() - 1
     if out is None:
         out = torch.empty(a.rows, n, dtype=torch.float32 if out_dtype == OUT_FP32 else torch.bfloat16,
                           device=a.codes.device)
     ca, cb = a.c(), b.c()
     _check(lib().nvfp4_grouped_gemm(ctypes.byref(ca), _ptr(offsets), groups, ctypes.byref(cb), n, _ptr(out),
-                                    out.stride(0), out_dtype, _stream(stream)))
+                                    out.stride(0), out_dtype, _ptr(c_amax), _stream(stream)))
     return out
 
 

@@ -100,6 +100,7 @@ struct GemmParams {
     const float* amax_b;        // [groups]
     void* c;
     int64_t ldc;
+    float* c_amax;              // nullable: max |C| over the written outputs, per group (zeroed by the host)
     bool vec_store;             // rows of C start 16-byte aligned: vector stores
 };
 
@@ -284,6 +285,30 @@ __device__ __forceinline__ void tc_st_x32(uint32_t taddr, const uint4 (&v)[8]) {
 }
 
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// Largest |x| over the first `valid` bf16 values packed two per word in w[0..N)
+// (element 2j in the low half of word j), as the 15 magnitude bits.
+template <int N>
+__device__ __forceinline__ uint32_t bf16_absmax(const uint32_t (&w)[N], int valid) {
+    uint32_t acc = 0;
+    if (valid >= 2 * N) {
+#pragma unroll
+        for (int j = 0; j < N; ++j) acc = __vmaxu2(acc, w[j] & 0x7FFF7FFFu);
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            if (2 * j < valid) acc = max(acc, w[j] & 0x7FFFu);
+            if (2 * j + 1 < valid) acc = max(acc, (w[j] >> 16) & 0x7FFFu);
+        }
+    }
+    return max(acc & 0xFFFFu, acc >> 16);
+}
+
+// Merge a warp's largest output magnitude (non-negative FP32 bits) into *dst.
+__device__ __forceinline__ void warp_amax_to(float* dst, uint32_t fbits) {
+    fbits = __reduce_max_sync(0xFFFFFFFFu, fbits);
+    if ((threadIdx.x & 31) == 0 && fbits != 0u) atomicMax(reinterpret_cast<unsigned int*>(dst), fbits);
+}
+
 // Lane/chunk exchange for coalesced row stores.  On entry lane l holds 32
 // words of row l of a 32-row block (chunk c = words 4c .. 4c+3, 16 bytes).
 // Three xor-shuffle stages swap lane bits 2..4 with chunk bits 0..2; on exit
@@ -586,6 +611,15 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     }
                     const int64_t cstart = col0 + 32 * h;
                     if (cstart >= p.N) continue;
+                    if (p.c_amax != nullptr) {
+                        // rounding is monotone, so max |alpha x| = alpha max |x|
+                        const int valid = r < tc.rows ? (int)(p.N - cstart >= 32 ? 32 : p.N - cstart) : 0;
+                        float m = 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            m = fmaxf(m, i < valid ? fabsf(__uint_as_float(v[i])) : 0.0f);
+                        warp_amax_to(p.c_amax + tc.g, __float_as_uint(__fmul_rn(alpha, m)));
+                    }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[i])));
                     if (p.vec_store) {
@@ -629,6 +663,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     }
                     const int64_t cstart = col0 + 32 * h;
                     if (cstart >= p.N) continue;
+                    if (p.c_amax != nullptr) {
+                        const int valid = r < tc.rows ? (int)(p.N - cstart >= 32 ? 32 : p.N - cstart) : 0;
+                        warp_amax_to(p.c_amax + tc.g, bf16_absmax(w, valid) << 16);
+                    }
                     if (rows_full) {
                         // the staging buffer is free once the previous box has been read
                         if (lane == 0) bulk_wait_read0();
@@ -683,6 +721,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     }
                 }
                 if (col0 >= p.N) continue;
+                if (p.c_amax != nullptr) {
+                    const int valid = r < tc.rows ? (int)(p.N - col0 >= 64 ? 64 : p.N - col0) : 0;
+                    warp_amax_to(p.c_amax + tc.g, bf16_absmax(w, valid) << 16);
+                }
                 if (p.vec_store) {
                     rows_to_segments(w);
                     store_segments(w, reinterpret_cast<uint8_t*>(reinterpret_cast<uint16_t*>(p.c) + (tc.row0 + q * 32) * p.ldc + col0),

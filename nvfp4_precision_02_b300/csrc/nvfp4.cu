@@ -47,7 +47,6 @@ struct DeviceInfo {
     bool ok = false;
     int sms = 0;
     bool gemm_attr = false;
-    bool q2f_attr = false;
 };
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
@@ -349,10 +348,8 @@ nvfp4_status nvfp4_quantize_2d(const void* w, int64_t batch, int64_t rows, int64
 
 size_t nvfp4_quantize_2d_fused_workspace(int64_t batch) {
     if (batch < 1) return 0;
-    // per-entry counters, the abort word and a spare word, the 64-bit item
-    // queue at the next 8-byte boundary, rounded up to 16 bytes
-    const int64_t queue_off = ((batch + 2) * 4 + 7) & ~int64_t(7);
-    return (size_t)((queue_off + 8 + 15) / 16 * 16);
+    // per-entry counters, the abort word and a spare word, rounded up to 16 bytes
+    return (size_t)(((batch + 2) * 4 + 15) / 16 * 16);
 }
 
 nvfp4_status nvfp4_quantize_2d_fused(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ld,
@@ -373,39 +370,21 @@ nvfp4_status nvfp4_quantize_2d_fused(const void* w, int64_t batch, int64_t rows,
     NVFP4_TRY(cuda_call(cudaMemsetAsync(out->amax, 0, sizeof(float) * batch, stream), "memset amax"));
     if (rows == 0 || cols == 0) return NVFP4_OK;
     NVFP4_TRY(cuda_call(cudaMemsetAsync(workspace, 0, nvfp4_quantize_2d_fused_workspace(batch), stream), "memset workspace"));
-    // bf16 [batch * rows, cols] with row stride ld, read in boxes of 256 columns x 16 rows
-    CUtensorMap tm;
-    {
-        auto fn = encode_fn();
-        if (fn == nullptr) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-        cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows * batch)};
-        cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-        cuuint32_t box[2] = {(cuuint32_t)Q2F_BOX_COLS, 16u};
-        cuuint32_t estr[2] = {1u, 1u};
-        const CUresult r = fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled (weights) failed (%d)", (int)r);
-    }
-    {
-        std::lock_guard<std::mutex> lk(g_dev_mu);
-        if (!g_dev[dev].q2f_attr) {
-            NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_quant2d_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, Q2F_SMEM),
-                                "smem attr"));
-            g_dev[dev].q2f_attr = true;
-        }
-    }
+    if ((rows / 16) * cdiv(cols, Q2F_ITEM_COLS) > (int64_t)0x7FFFFFFF)
+        return fail(NVFP4_ERR_LIMIT, "an entry of %lld x %lld is too large", (long long)rows, (long long)cols);
     int per_sm = 0;
-    NVFP4_TRY(cuda_call(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant2d_fused, Q2F_THREADS, Q2F_SMEM), "occupancy"));
+    NVFP4_TRY(cuda_call(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant2d_fused, Q2F_THREADS, 0), "occupancy"));
     if (per_sm < 1) return fail(NVFP4_ERR_CUDA, "fused 2D quantiser cannot be resident");
-    const int64_t items = 2 * batch * (rows / 16) * cdiv(cols, Q2F_COLS);
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)per_sm * sms));
+    // every block must be resident (cooperative launch); a small problem takes fewer warps
+    const int64_t items = batch * (rows / 16) * cdiv(cols, Q2F_ITEM_COLS);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(items, Q2F_THREADS / 32), (int64_t)per_sm * sms));
+    const uint16_t* wp = (const uint16_t*)w;
     float* am = out->amax;
     uint32_t* cnt = (uint32_t*)workspace;
     uint8_t* codes = (uint8_t*)out->codes;
     uint8_t* sf = out->sf;
-    void* args[] = {&tm, &batch, &rows, &cols, &am, &cnt, &codes, &sf, &tile_sf};
-    NVFP4_TRY(cuda_call(cudaLaunchCooperativeKernel((const void*)k_quant2d_fused, dim3(grid), dim3(Q2F_THREADS), args, Q2F_SMEM, stream),
+    void* args[] = {&wp, &batch, &rows, &cols, &ld, &am, &cnt, &codes, &sf, &tile_sf};
+    NVFP4_TRY(cuda_call(cudaLaunchCooperativeKernel((const void*)k_quant2d_fused, dim3(grid), dim3(Q2F_THREADS), args, 0, stream),
                         "k_quant2d_fused launch"));
     NVFP4_TRY(launched("k_quant2d_fused"));
     if ((rows % 128) || ((cols / 16) % 4)) {
@@ -563,7 +542,7 @@ static nvfp4_status make_store_map(CUtensorMap* map, void* c, int64_t rows, int6
 }
 
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* c, int64_t ldc, nvfp4_out_dtype c_dtype,
-                        nvfp4_stream_t stream) {
+                        float* c_amax, nvfp4_stream_t stream) {
     NVFP4_INJECT_CHECK();
     NVFP4_TRY(check_operand(a, "a"));
     NVFP4_TRY(check_operand(b, "b"));
@@ -588,7 +567,12 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* c, i
     p.sfa = a->sf; p.sfb = b->sf; p.sfb_group_stride = 0;
     p.amax_a = a->amax; p.amax_b = b->amax;
     p.c = c; p.ldc = ldc;
+    p.c_amax = c_amax;
     p.vec_store = aligned16(c) && (ldc * esz) % 16 == 0;
+    if (c_amax != nullptr) {
+        if (((uintptr_t)c_amax & 3u) != 0) return fail(NVFP4_ERR_ALIGN, "c_amax not 4-byte aligned");
+        NVFP4_TRY(cuda_call(cudaMemsetAsync(c_amax, 0, sizeof(float), stream), "memset c_amax"));
+    }
     CUtensorMap mc;
     bool tma_store = false;
     std::memset(&mc, 0, sizeof(mc));
@@ -600,7 +584,7 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* c, i
 
 nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, int32_t num_groups,
                                 const nvfp4_tensor* b, int64_t n, void* c, int64_t ldc, nvfp4_out_dtype c_dtype,
-                                nvfp4_stream_t stream) {
+                                float* c_amax, nvfp4_stream_t stream) {
     NVFP4_INJECT_CHECK();
     NVFP4_TRY(check_operand(a, "a"));
     NVFP4_TRY(check_operand(b, "b"));
@@ -629,7 +613,12 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, i
     p.sfa = a->sf; p.sfb = b->sf; p.sfb_group_stride = sf_bytes(n, K);
     p.amax_a = a->amax; p.amax_b = b->amax;
     p.c = c; p.ldc = ldc;
+    p.c_amax = c_amax;
     p.vec_store = aligned16(c) && (ldc * esz) % 16 == 0;
+    if (c_amax != nullptr) {
+        if (((uintptr_t)c_amax & 3u) != 0) return fail(NVFP4_ERR_ALIGN, "c_amax not 4-byte aligned");
+        NVFP4_TRY(cuda_call(cudaMemsetAsync(c_amax, 0, sizeof(float) * num_groups, stream), "memset c_amax"));
+    }
     CUtensorMap mc;
     bool tma_store = false;
     std::memset(&mc, 0, sizeof(mc));

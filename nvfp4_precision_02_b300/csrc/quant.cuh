@@ -504,33 +504,34 @@ __global__ void __launch_bounds__(128) k_quant2d(const uint16_t* __restrict__ w,
 
 // ------------------------------------------------------------------ fused 2D
 // Per-entry amax and 2D quantisation of a batched weight [batch, rows, cols]
-// (W codes and scales; no W^T) in one launch that reads every element from
-// HBM once: the second read of an entry, for the codes, hits L2.  Work items
-// are pieces of 16 rows x up to 1024 columns of one entry, either "amax" (max
-// |w| over the piece, merged into amax[e] with an atomic max, then counted in
-// counters[e]) or "quantise" (wait until counters[e] holds all of entry e's
-// pieces, then quantise the piece with amax[e]).  Items run in the fixed
-// order
-//     A(0) A(1) | A(2) Q(0) | A(3) Q(1) | ... | A(batch-1) Q(batch-3) | Q(batch-2) Q(batch-1)
-// (A(j) / Q(j): all amax / quantise items of entry j; a lag of two entries),
-// CTA c taking items c, c + grid, c + 2*grid, ...  A CTA double-buffers its
-// pieces in shared memory: while it reduces or quantises one piece, the TMA
-// engine already loads its next one (four 256 x 16 boxes), so every CTA keeps
-// a piece in flight.  A quantise item waits only on amax items earlier in the
-// order and the launch is cooperative (every CTA resident), so the waits end;
-// each is bounded anyway: the first to give up records DEV_TIMEOUT and raises
-// counters[batch] (the abort word), after which no item waits any more.
-// Items are handed out by a queue (a 64-bit word at the first 8-byte boundary
-// after counters[batch + 1], atomically incremented) rather than a fixed stride, so that a slow CTA does not hold
-// back the items after it; a CTA takes its next item before it processes the
-// current one and keeps that piece loading meanwhile.
-// amax[batch] and counters[batch + 2] must be zero on entry.
-constexpr int Q2F_LAG = 2;
+// (W codes and scales; no W^T) in one launch, reading each element twice
+// within a short window so that the second read, for the codes, can hit L2.
+// Measured on B300 with the LatentMoE expert weights (5.5 and 21 MB per
+// entry), most second reads still missed L2 and this launch took 1.3x the
+// time of the two-launch amax + quantise path, which the step therefore uses.
+//
+// Work is split into items of 16 rows x Q2F_ITEM_COLS columns (16x64 strips
+// of 16x16 tiles) of one entry; entry e holds items e*ipe .. (e+1)*ipe - 1.
+// Every warp works alone (no block barrier anywhere): warp w of the W warps
+// of the grid takes slots w, w + W, w + 2W, ...; slot s is first the amax
+// item s (max |w| over the item) and then the quantise item s - lag, with
+// lag = ipe + 2W.  A warp keeps the running max and item count of the entry
+// it is reducing in registers and publishes them (one atomic max into
+// amax[e], then one atomic add into counters[e]) when it moves to another
+// entry.  A quantise item of entry e first waits until counters[e] == ipe.
+// Every amax item of entry e sits in a slot at least 2W before the first
+// quantise item of e, so in the steady state the wait finds the entry
+// complete (a margin of W/2 or W/4 made warps wait and ran 1.2-2.7x slower),
+// and about one entry plus 2W items pass between the two reads.  The waits cannot deadlock: a quantise item of entry e waits only on
+// publications that come before any quantise item of an entry >= e in their
+// warp's order, and the launch is cooperative (every warp resident).  Each
+// wait is bounded anyway: the first to give up records DEV_TIMEOUT and raises
+// counters[batch] (the abort word), after which every warp stops.
+// amax[batch] and counters[batch + 1] must be zero on entry.
 constexpr int Q2F_THREADS = 256;
-constexpr int64_t Q2F_COLS = 1024;                 // columns of a piece
-constexpr int Q2F_BOX_COLS = 256;                  // TMA box: 256 columns x 16 rows
-constexpr int Q2F_PIECE_BYTES = 16 * Q2F_COLS * 2; // 32 KB
-constexpr int Q2F_SMEM = 2 * Q2F_PIECE_BYTES + 1024 + 64;
+constexpr int Q2F_STRIPS = 4;                        // 64-column strips of an item
+constexpr int64_t Q2F_ITEM_COLS = 64 * Q2F_STRIPS;
+constexpr uint64_t Q2F_WAIT_NS = 4000000000ull;
 
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
     uint32_t v;
@@ -538,185 +539,88 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
     return v;
 }
 
-struct Q2fItem {
-    bool is_amax;
-    int64_t e, rs, cb, cn;       // entry, first row, first column, columns
-};
-
-__device__ __forceinline__ Q2fItem q2f_item(int64_t it, int64_t batch, int64_t rows, int64_t cols) {
-    const int64_t ncc = (cols + Q2F_COLS - 1) / Q2F_COLS;
-    const int64_t np = (rows / 16) * ncc;
-    const int64_t lag = batch < Q2F_LAG ? batch : Q2F_LAG;
-    const int64_t head = lag * np, mid = (batch - lag) * 2 * np;
-    Q2fItem r;
-    int64_t pc;
-    if (it < head) {
-        r.is_amax = true; r.e = it / np; pc = it % np;
-    } else if (it - head < mid) {
-        const int64_t i2 = it - head, j = lag + i2 / (2 * np), k = i2 % (2 * np);
-        r.is_amax = k < np;
-        r.e = r.is_amax ? j : j - lag;
-        pc = r.is_amax ? k : k - np;
-    } else {
-        const int64_t i3 = it - head - mid;
-        r.is_amax = false; r.e = (batch - lag) + i3 / np; pc = i3 % np;
-    }
-    r.rs = (pc / ncc) * 16;
-    r.cb = (pc % ncc) * Q2F_COLS;
-    r.cn = min(Q2F_COLS, cols - r.cb);
-    return r;
-}
-
-// tm_w: bf16 [batch * rows, cols] (row stride ld), box 256 x 16, no swizzle.
-__global__ void __launch_bounds__(Q2F_THREADS) k_quant2d_fused(const __grid_constant__ CUtensorMap tm_w, int64_t batch,
-                                                       int64_t rows, int64_t cols, float* __restrict__ amax,
-                                                       uint32_t* __restrict__ counters,
-                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
-                                                       uint8_t* __restrict__ tile_sf) {
-    extern __shared__ uint8_t q2f_raw[];
-    uint8_t* buf = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q2f_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(buf + 2 * Q2F_PIECE_BYTES);   // full[2]
-    __shared__ uint32_t s_red[Q2F_THREADS / 32];
-    __shared__ float s_amax;
-    __shared__ long long s_next;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t items = 2 * batch * (rows / 16) * ((cols + Q2F_COLS - 1) / Q2F_COLS);
-    unsigned long long* queue =
-        reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(counters) + (((batch + 2) * 4 + 7) & ~int64_t(7)));
-    const uint32_t full0 = (uint32_t)__cvta_generic_to_shared(bars);
-    if (threadIdx.x == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(full0) : "memory");
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(full0 + 8) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    __syncthreads();
-    // thread 0 loads item `it` into buffer `b` (four boxes; out-of-range columns read as zero)
-    auto issue = [&](int64_t it, int b) {
-        const Q2fItem w = q2f_item(it, batch, rows, cols);
-        const uint32_t bar = full0 + 8 * b;
-        const int nbox = (int)((w.cn + Q2F_BOX_COLS - 1) / Q2F_BOX_COLS);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                     "r"((uint32_t)(nbox * 16 * Q2F_BOX_COLS * 2))
-                     : "memory");
-        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(buf + b * Q2F_PIECE_BYTES);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // earlier generic reads of this buffer
-        for (int k = 0; k < nbox; ++k)
-            asm volatile(
-                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst + k * 16 * Q2F_BOX_COLS * 2),
-                "l"(reinterpret_cast<uint64_t>(&tm_w)), "r"((int32_t)(w.cb + k * Q2F_BOX_COLS)),
-                "r"((int32_t)(w.e * rows + w.rs)), "r"(bar)
-                : "memory");
+__global__ void __launch_bounds__(Q2F_THREADS, 2) k_quant2d_fused(const uint16_t* __restrict__ w, int64_t batch,
+                                                                  int64_t rows, int64_t cols, int64_t ld,
+                                                                  float* __restrict__ amax,
+                                                                  uint32_t* __restrict__ counters,
+                                                                  uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                                  uint8_t* __restrict__ tile_sf) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (Q2F_THREADS / 32);
+    const int64_t wid = (int64_t)blockIdx.x * (Q2F_THREADS / 32) + (threadIdx.x >> 5);
+    const int64_t ncc = (cols + Q2F_ITEM_COLS - 1) / Q2F_ITEM_COLS;
+    const int64_t ipe = (rows / 16) * ncc;
+    const int64_t na = batch * ipe;
+    const int64_t lag = ipe + 2 * nw;
+    int64_t red_e = -1;              // entry being reduced
+    uint32_t red_acc = 0, red_n = 0; // its running max (two bf16 magnitudes) and item count
+    int64_t ready_e = -1;            // entry whose amax this warp has seen complete
+    float s_enc = 0.0f;
+    auto publish = [&]() {
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, max(red_acc & 0xFFFFu, red_acc >> 16));
+        if (lane == 0) {
+            if (m != 0u) atomicMax(reinterpret_cast<unsigned int*>(amax + red_e), m << 16);
+            __threadfence();
+            atomicAdd(counters + red_e, red_n);
+        }
     };
-    uint32_t issued[2] = {0u, 0u};                              // loads issued per buffer (thread 0)
-    if (threadIdx.x == 0) {
-        const long long first = (long long)atomicAdd(queue, 1ull);
-        s_next = first;
-        if (first < items) { issue(first, 0); issued[0] = 1; }
-    }
-    __syncthreads();
-    uint32_t li = 0;                                            // local item count
-    bool abort_all = false;
-    for (int64_t it = s_next; it < items; ++li) {
-        const int b = li & 1;
-        __syncthreads();                                        // everyone has read s_next
-        if (threadIdx.x == 0) {
-            const long long nx = (long long)atomicAdd(queue, 1ull);
-            s_next = nx;
-            if (nx < items) { issue(nx, b ^ 1); ++issued[b ^ 1]; }
-        }
-        // wait for this item's piece (bounded)
-        {
-            const uint32_t bar = full0 + 8 * b, par = (li >> 1) & 1;
-            const uint64_t t0 = globaltimer_ns();
-            while (true) {
-                uint32_t ok;
-                asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                             "selp.u32 %0, 1, 0, p;\n\t}"
-                             : "=r"(ok) : "r"(bar), "r"(par) : "memory");
-                if (ok) break;
-                if (globaltimer_ns() - t0 > 4000000000ull) { raise_status(DEV_TIMEOUT); abort_all = true; break; }
+    for (int64_t s = wid; s < na + lag; s += nw) {
+        if (s < na) {
+            const int64_t e = s / ipe, k = s % ipe;
+            if (e != red_e) {
+                if (red_e >= 0) publish();
+                red_e = e; red_acc = 0; red_n = 0;
             }
-        }
-        if (__syncthreads_or(abort_all)) break;
-        const Q2fItem w = q2f_item(it, batch, rows, cols);
-        const uint8_t* piece = buf + b * Q2F_PIECE_BYTES;
-        if (w.is_amax) {
-            // the loaded boxes of [16][256]; columns >= cols read as zero
-            const int nvec = (int)((w.cn + Q2F_BOX_COLS - 1) / Q2F_BOX_COLS) * (16 * Q2F_BOX_COLS / 8);
-            uint32_t acc = 0;
-#pragma unroll 4
-            for (int i = threadIdx.x; i < nvec; i += Q2F_THREADS)
-                acc = absmax_bits(*reinterpret_cast<const uint4*>(piece + 16 * i), acc);
-            uint32_t mbits = __float_as_uint(bits_to_amax(acc));
-            mbits = __reduce_max_sync(0xFFFFFFFFu, mbits);
-            if (lane == 0) s_red[warp] = mbits;
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                uint32_t mm = 0;
+            const uint16_t* wb = w + e * rows * ld;
+            const int64_t rs = (k / ncc) * 16, cb = (k % ncc) * Q2F_ITEM_COLS;
+            uint4 v[Q2F_STRIPS][4];
 #pragma unroll
-                for (int i = 0; i < Q2F_THREADS / 32; ++i) mm = max(mm, s_red[i]);
-                if (mm != 0u) atomicMax(reinterpret_cast<unsigned int*>(amax + w.e), mm);
-                __threadfence();
-                atomicAdd(counters + w.e, 1u);
-            }
-        } else {
-            if (threadIdx.x == 0) {
-                const uint32_t np = (uint32_t)((rows / 16) * ((cols + Q2F_COLS - 1) / Q2F_COLS));
+            for (int j = 0; j < Q2F_STRIPS; ++j) quant2d_strip_load(wb, rows, cols, ld, rs, cb + 64 * j, v[j]);
+#pragma unroll
+            for (int j = 0; j < Q2F_STRIPS; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) red_acc = absmax_bits(v[j][i], red_acc);
+            ++red_n;
+        } else if (red_e >= 0) {
+            publish();
+            red_e = -1;
+        }
+        const int64_t q = s - lag;
+        if (q < 0) continue;
+        const int64_t e = q / ipe, k = q % ipe;
+        if (e != ready_e) {
+            uint32_t am = 0u, ok = 1u;
+            if (lane == 0) {
                 const uint64_t t0 = globaltimer_ns();
-                bool ok = true;
-                while (ld_acquire_u32(counters + w.e) < np) {
-                    __nanosleep(64);
-                    if (ld_acquire_u32(counters + batch) != 0u) { ok = false; break; }
-                    if (globaltimer_ns() - t0 > 4000000000ull) {
+                while (ld_acquire_u32(counters + e) < (uint32_t)ipe) {
+                    if (ld_acquire_u32(counters + batch) != 0u) { ok = 0u; break; }
+                    if (globaltimer_ns() - t0 > Q2F_WAIT_NS) {
                         raise_status(DEV_TIMEOUT);
                         atomicExch(counters + batch, 1u);
-                        ok = false;
+                        ok = 0u;
                         break;
                     }
+                    __nanosleep(128);
                 }
-                s_amax = ok ? *reinterpret_cast<volatile float*>(amax + w.e) : -1.0f;
+                if (ok) am = *reinterpret_cast<volatile const uint32_t*>(amax + e);
             }
-            __syncthreads();
-            const float am = s_amax;
-            if (am < 0.0f) abort_all = true;
-            if (!abort_all) {
-                const float s_enc = tensor_encode_scale(am);
-                // warp w takes the 64-column blocks w, w + 8, ... of the piece
-                for (int64_t c = 64 * warp; c < w.cn; c += 64 * (Q2F_THREADS / 32)) {
-                    const int box = (int)(c / Q2F_BOX_COLS), bc = (int)(c % Q2F_BOX_COLS) + 8 * (lane & 7);
-                    uint4 v[4];
+            if (__shfl_sync(0xFFFFFFFFu, ok, 0) == 0u) return;
+            s_enc = tensor_encode_scale(__uint_as_float(__shfl_sync(0xFFFFFFFFu, am, 0)));
+            ready_e = e;
+        }
+        const uint16_t* wb = w + e * rows * ld;
+        const int64_t rs = (k / ncc) * 16, cb = (k % ncc) * Q2F_ITEM_COLS;
+        uint4 v[Q2F_STRIPS][4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int rr = (lane >> 3) + 4 * i;
-                        v[i] = *reinterpret_cast<const uint4*>(piece + box * (16 * Q2F_BOX_COLS * 2) + rr * (Q2F_BOX_COLS * 2) + bc * 2);
-                    }
-                    uint32_t cw[4], word;
-                    quant2d_strip_encode(v, rows, cols, w.e, w.rs, w.cb + c, s_enc, codes, sf, tile_sf, cw, word);
-                }
-            }
-        }
-        __syncthreads();                                        // piece buffer free for the next issue
-        if (abort_all) break;
-        it = s_next;
-    }
-    // on abort, every load issued into a buffer must land before the CTA exits:
-    // the n-th load of a buffer completes its phase n-1 (parity (n-1) & 1)
-    if (threadIdx.x == 0 && abort_all) {
-        for (int bb = 0; bb < 2; ++bb) {
-            if (issued[bb] == 0u) continue;
-            const uint32_t par = (issued[bb] - 1u) & 1u;
-            const uint64_t t0 = globaltimer_ns();
-            while (globaltimer_ns() - t0 < 1000000000ull) {
-                uint32_t ok;
-                asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                             "selp.u32 %0, 1, 0, p;\n\t}"
-                             : "=r"(ok) : "r"(full0 + 8 * bb), "r"(par) : "memory");
-                if (ok) break;
-            }
+        for (int j = 0; j < Q2F_STRIPS; ++j) quant2d_strip_load(wb, rows, cols, ld, rs, cb + 64 * j, v[j]);
+#pragma unroll
+        for (int j = 0; j < Q2F_STRIPS; ++j) {
+            if (cb + 64 * j >= cols) break;
+            uint32_t cw[4], word;
+            quant2d_strip_encode(v[j], rows, cols, e, rs, cb + 64 * j, s_enc, codes, sf, tile_sf, cw, word);
         }
     }
+    if (red_e >= 0) publish();
 }
 
 // Padding of the 2D scale buffers (per batch entry: blockIdx.y).

@@ -77,18 +77,18 @@ def test_other_entry_points_validation(L):
     assert L.nvfp4_rht_quantize(FAKE, 40, 32, 32, 1, 0, 0, None, ctypes.byref(_t(32, 40)), None) == 2
     assert L.nvfp4_rht_amax(FAKE, 32, 8, 8, 1, None, None) == 1
     a, b = _t(64, 64), _t(48, 64)
-    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(_t(48, 80)), FAKE, 48, 0, None) == 2      # K mismatch
-    assert L.nvfp4_gemm(ctypes.byref(_t(64, 48)), ctypes.byref(_t(48, 48)), FAKE, 48, 0, None) == 2  # K % 32
-    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), FAKE, 40, 0, None) == 2              # ldc < N
-    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), FAKE + 1, 48, 0, None) == 3          # c misaligned
-    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), None, 48, 0, None) == 1
-    assert L.nvfp4_grouped_gemm(ctypes.byref(a), None, 4, ctypes.byref(b), 48, FAKE, 48, 0, None) == 1
-    assert L.nvfp4_grouped_gemm(ctypes.byref(a), FAKE, 2000, ctypes.byref(b), 48, FAKE, 48, 0, None) == 7
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(_t(48, 80)), FAKE, 48, 0, None, None) == 2      # K mismatch
+    assert L.nvfp4_gemm(ctypes.byref(_t(64, 48)), ctypes.byref(_t(48, 48)), FAKE, 48, 0, None, None) == 2  # K % 32
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), FAKE, 40, 0, None, None) == 2              # ldc < N
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), FAKE + 1, 48, 0, None, None) == 3          # c misaligned
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), None, 48, 0, None, None) == 1
+    assert L.nvfp4_grouped_gemm(ctypes.byref(a), None, 4, ctypes.byref(b), 48, FAKE, 48, 0, None, None) == 1
+    assert L.nvfp4_grouped_gemm(ctypes.byref(a), FAKE, 2000, ctypes.byref(b), 48, FAKE, 48, 0, None, None) == 7
     assert L.nvfp4_quantize_1d_grouped(FAKE, 64, 32, 32, FAKE, 0, 0, 0, None, ctypes.byref(_t(64, 32)), None) == 7
     assert L.nvfp4_quantize_2d_fused(FAKE, 2, 32, 32, 32, None, 64, ctypes.byref(_t(32, 32)), None, None) == 1
     assert L.nvfp4_quantize_2d_fused(FAKE, 2, 32, 32, 32, FAKE, 4, ctypes.byref(_t(32, 32)), None, None) == 2
     assert L.nvfp4_quantize_2d_fused_workspace(512) == 2064
-    assert L.nvfp4_quantize_2d_fused_workspace(5) == 48
+    assert L.nvfp4_quantize_2d_fused_workspace(5) == 32
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
@@ -97,13 +97,13 @@ def test_valid_calls_report_missing_device(L):
     assert L.nvfp4_quantize_1d(FAKE, 64, 32, 32, 0, 0, None, ctypes.byref(ok), None) == 4
     assert b"device" in L.nvfp4_last_error().lower()
     a, b = _t(64, 64), _t(48, 64)
-    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), FAKE, 48, 0, None) == 4
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), FAKE, 48, 0, None, None) == 4
 
 
 def test_empty_gemm_is_a_no_op(L):
     # M == 0: valid, nothing to launch (returns before any device work)
     a, b = _t(0, 64), _t(48, 64)
-    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), None, 48, 0, None) == 0
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), None, 48, 0, None, None) == 0
 
 
 def test_inject_hook_is_host_side(L, B):
@@ -114,7 +114,7 @@ def test_inject_hook_is_host_side(L, B):
     assert L.nvfp4_quantize_1d(None, 64, 32, 32, 0, 0, None, ctypes.byref(_t(64, 32)), None) == 1
     with pytest.raises(B.Nvfp4Error) as e:
         B.debug_inject(6)
-        B._check(L.nvfp4_gemm(None, None, None, 0, 0, None))
+        B._check(L.nvfp4_gemm(None, None, None, 0, 0, None, None))
     assert e.value.status == 6
 
 

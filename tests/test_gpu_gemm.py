@@ -67,11 +67,14 @@ def test_gemm_fprop_shapes(B, orc, M, N, K, fp32):
     two_d = N % 16 == 0
     qa = B.quantize_1d(a.cuda())
     qw = _quant_b(B, w.cuda(), two_d)
-    out = B.gemm(qa, qw, out_dtype=B.OUT_FP32 if fp32 else B.OUT_BF16)
+    c_amax = torch.full((1,), -1.0, device="cuda")
+    out = B.gemm(qa, qw, out_dtype=B.OUT_FP32 if fp32 else B.OUT_BF16, c_amax=c_amax)
     torch.cuda.synchronize()
     ref, absum = _oracle_ref(orc, a, w, two_d)
     o = out.float().cpu().numpy()
     _check(o, ref, absum, bf16=not fp32)
+    # the epilogue's amax is the largest magnitude of the stored outputs, exactly
+    assert float(c_amax[0]) == float(np.abs(o).max())
 
 
 def test_tiny_fprop_workload(B, orc):
@@ -159,9 +162,15 @@ def test_grouped_gemm(B, orc, fp32):
     qw, _, _ = B.quantize_2d(w.cuda(), want_t=False)
     out = torch.full((R, n), -3.0, device="cuda",
                      dtype=torch.float32 if fp32 else torch.bfloat16)
-    B.grouped_gemm(qa, off, qw, n, out_dtype=B.OUT_FP32 if fp32 else B.OUT_BF16, out=out)
+    c_amax = torch.full((E,), -1.0, device="cuda")
+    B.grouped_gemm(qa, off, qw, n, out_dtype=B.OUT_FP32 if fp32 else B.OUT_BF16, out=out, c_amax=c_amax)
     torch.cuda.synchronize()
     o = out.float().cpu().numpy()
+    # per group: the largest stored magnitude, exactly (0 for an empty group)
+    got = c_amax.cpu().numpy()
+    for e in range(E):
+        want = float(np.abs(o[offsets[e]:offsets[e + 1]]).max()) if offsets[e + 1] > offsets[e] else 0.0
+        assert got[e] == want, (e, got[e], want)
     ra = orc.quantize_1d_grouped(a, offsets)
     rw = orc.quantize_2d(w, want_t=False)
     nsf = orc.sf_bytes(n, K)
