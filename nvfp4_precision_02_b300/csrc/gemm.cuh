@@ -12,9 +12,9 @@
 // Design (one CTA per SM, persistent over output tiles of 128 x 256):
 //   K stage 256 FP4 elements (128 B per row, 128B-swizzled TMA boxes);
 //   4 stages of A 16 KB + B 32 KB + scales 6 KB in shared memory.
-//   warp 0        TMA producer: A and B boxes by cp.async.bulk.tensor, the
-//                 scale atoms (512 B each, already in the 128x4 layout) by
-//                 cp.async.bulk
+//   warp 0        TMA producer: the scale atoms (512 B each, already in the
+//                 128x4 layout) by cp.async.bulk on a barrier of their own,
+//                 then the A and B boxes by cp.async.bulk.tensor
 //   warp 1        allocates TMEM; one lane issues the 4 MMAs 128x256x64 of a
 //                 stage from one asm block (descriptors advanced in place)
 //   warps 2..5    scale-factor writers, one per TMEM lane quarter: when a
@@ -409,8 +409,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
-    // bars: full[S], empty[S], sf_full[S], acc_full, acc_empty, drain
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * G_STAGES + 3);
+    // bars: full[S] (A, B landed), empty[S], sf_full[S] (scales in TMEM),
+    // sf_land[S] (scales landed in shared memory), acc_full, acc_empty, drain
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * G_STAGES + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int32_t* tab = reinterpret_cast<int32_t*>(smem + L::TAB_OFF);
     const int groups = p.groups;
@@ -418,13 +419,15 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + G_STAGES), sff0 = smem_u32(bars + 2 * G_STAGES);
-    const uint32_t acc_full = smem_u32(bars + 3 * G_STAGES), acc_empty = acc_full + 8, drain = acc_full + 16;
+    const uint32_t sfl0 = smem_u32(bars + 3 * G_STAGES);
+    const uint32_t acc_full = smem_u32(bars + 4 * G_STAGES), acc_empty = acc_full + 8, drain = acc_full + 16;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < G_STAGES; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
             mbar_init(sff0 + 8 * s, 4);
+            mbar_init(sfl0 + 8 * s, 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, G_EPI_WARPS);
@@ -480,17 +483,22 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) { ok = false; break; }
                     const int na = min(4, katoms - 4 * ks);
                     const uint32_t sfbytes = (uint32_t)na * 512u;
-                    const uint32_t bar = full0 + 8 * s;
-                    mbar_expect_tx(bar, G_A_BYTES + G_B_BYTES + sfbytes * (rb2 ? 3u : 2u));
                     const uint32_t st = smem_u32(stages + s * G_STAGE_BYTES);
-                    tma_load_2d(st, &tm_a, ks * 128, tc.row0, bar);
-                    tma_load_2d(st + G_A_BYTES, &tm_b, ks * 128, brow0, bar);
+                    // the scales first, on their own barrier: they are small, land
+                    // ahead of A and B, and the scale warps move them into TMEM
+                    // while A and B are still arriving
+                    const uint32_t sbar = sfl0 + 8 * s;
+                    mbar_expect_tx(sbar, sfbytes * (rb2 ? 3u : 2u));
                     const uint32_t ssf = st + G_A_BYTES + G_B_BYTES;
-                    bulk_load(ssf, p.sfa + ((int64_t)tc.mtg * katoms + 4 * ks) * 512, sfbytes, bar);
-                    bulk_load(ssf + G_SFA_BYTES, sfb_g + ((int64_t)(tc.nt * 2) * katoms + 4 * ks) * 512, sfbytes, bar);
+                    bulk_load(ssf, p.sfa + ((int64_t)tc.mtg * katoms + 4 * ks) * 512, sfbytes, sbar);
+                    bulk_load(ssf + G_SFA_BYTES, sfb_g + ((int64_t)(tc.nt * 2) * katoms + 4 * ks) * 512, sfbytes, sbar);
                     if (rb2)
                         bulk_load(ssf + G_SFA_BYTES + 2048, sfb_g + ((int64_t)(tc.nt * 2 + 1) * katoms + 4 * ks) * 512,
-                                  sfbytes, bar);
+                                  sfbytes, sbar);
+                    const uint32_t bar = full0 + 8 * s;
+                    mbar_expect_tx(bar, G_A_BYTES + G_B_BYTES);
+                    tma_load_2d(st, &tm_a, ks * 128, tc.row0, bar);
+                    tma_load_2d(st + G_A_BYTES, &tm_b, ks * 128, brow0, bar);
                     issued |= 1u << s;
                     issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                     if (++s == G_STAGES) { s = 0; ph ^= 1u; }
@@ -500,7 +508,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 // let every copy already issued land before the CTA exits
                 volatile int never = 0;
                 for (int i = 0; i < G_STAGES; ++i)
-                    if ((issued >> i) & 1u) mbar_wait(full0 + 8 * i, (issued_ph >> i) & 1u, &never);
+                    if ((issued >> i) & 1u) {
+                        mbar_wait(sfl0 + 8 * i, (issued_ph >> i) & 1u, &never);
+                        mbar_wait(full0 + 8 * i, (issued_ph >> i) & 1u, &never);
+                    }
             }
         }
     } else if (warp == G_W_MMA) {
@@ -546,7 +557,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     } else if (warp < G_W_EPI0) {
         // ------------------------------------------------ scale factors -> TMEM
         // The producer lands the stage's scale atoms in shared memory next to
-        // A and B.  Lane i of every quarter copies the 16 bytes at offset 16*i
+        // A and B (on their own barrier, ahead of A and B).  Lane i of every quarter copies the 16 bytes at offset 16*i
         // of each 512-byte atom (the 4 scales of rows i, i+32, i+64, i+96) into
         // the atom's 4 TMEM columns.  The stage's TMEM columns are free once
         // its data has landed: the producer refilled it only after the MMAs of
@@ -560,7 +571,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             const bool rb2 = (tc.nt * 2 + 1) < nrb;
             for (int ks = 0; ks < kstages; ++ks) {
                 const int na = min(4, katoms - 4 * ks);
-                if (!mbar_wait(full0 + 8 * s, ph, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(sfl0 + 8 * s, ph, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint8_t* ssf = stages + s * G_STAGE_BYTES + G_A_BYTES + G_B_BYTES + lane * 16;
                 uint4 va[4], vb[8];
