@@ -38,6 +38,15 @@
 //   Moving the scales with tcgen05.st from dedicated warps keeps them off
 //   the MMA issue thread: measured on B300, a tcgen05.cp per 512-byte atom
 //   cost as much tensor time as half an MMA.
+// CTA pairs (the default; cta_group::2, clusters of two CTAs on two SMs):
+//   tiles of 256 x 256; each CTA holds its 128 A rows and 128 of the 256 B
+//   rows of a stage (38 KB instead of 54 KB per stage, five stages instead
+//   of four), plus its A scales and all 256 rows of B scales in its own TMEM.
+//   Rank 0 issues 256 x 256 x 64 MMAs for both; both CTAs' TMA loads complete
+//   on rank 0's full barrier, both CTAs' scale warps and epilogues arrive on
+//   rank 0's barriers, and rank 0's commits arrive on the barriers of both.
+//   The second m-tile of a pair may lie past its group's end: it is computed
+//   and not stored.
 // Every wait is bounded (DEV_TIMEOUT in the status word, then a clean exit).
 #pragma once
 
@@ -53,6 +62,11 @@ constexpr int G_B_BYTES = G_BN * G_BK / 2;                 // 32768
 constexpr int G_SFA_BYTES = (G_BK / 64) * 512;             // 2048: 4 atoms of A scales
 constexpr int G_SFB_BYTES = 2 * (G_BK / 64) * 512;         // 4096: 2 row blocks x 4 atoms of B scales
 constexpr int G_STAGE_BYTES = G_A_BYTES + G_B_BYTES + G_SFA_BYTES + G_SFB_BYTES;  // 55296
+// CTA-pair kernel (cta_group::2, 256 x 256 tiles over two SMs): each CTA holds
+// its own 128 A rows and half of the 256 B rows of a stage, and all 256 rows
+// of B scales.
+constexpr int G2_B_BYTES = G_B_BYTES / 2;                                          // 16384
+constexpr int G2_STAGE_BYTES = G_A_BYTES + G2_B_BYTES + G_SFA_BYTES + G_SFB_BYTES;  // 38912
 constexpr int G_W_TMA = 0, G_W_MMA = 1, G_W_SF0 = 2, G_W_EPI0 = 6;
 constexpr int G_EPI_WARPS = 16;
 constexpr int G_THREADS = (G_W_EPI0 + G_EPI_WARPS) * 32;   // 704
@@ -70,18 +84,24 @@ constexpr int G_STORE_WARP_BYTES = 2048;                     // bf16 staging of 
 // The TMA-store epilogue gives up one stage for the 32 KB staging: it pays
 // when K is short (the epilogue of a tile is then as long as its mainloop),
 // while long-K GEMMs keep four stages and store directly.
-template <bool TMA_STORE>
+template <bool TMA_STORE, bool PAIR = false>
 struct GemmLayout {
-    static constexpr int STAGES = TMA_STORE ? 3 : 4;
-    static constexpr int STORE_OFF = STAGES * G_STAGE_BYTES;
+    static constexpr int STAGE_BYTES = PAIR ? G2_STAGE_BYTES : G_STAGE_BYTES;
+    static constexpr int B_BYTES = PAIR ? G2_B_BYTES : G_B_BYTES;
+    static constexpr int STAGES = PAIR ? (TMA_STORE ? 4 : 5) : (TMA_STORE ? 3 : 4);
+    static constexpr int STORE_OFF = STAGES * STAGE_BYTES;
     static constexpr int STORE_BYTES = TMA_STORE ? G_EPI_WARPS * G_STORE_WARP_BYTES : 0;
     static constexpr int BAR_OFF = STORE_OFF + STORE_BYTES;
     static constexpr int TAB_OFF = BAR_OFF + G_BAR_BYTES;
 };
 
-// dynamic shared memory: 1 KB alignment slack, layout, group tables
-__host__ __device__ constexpr int gemm_smem_bytes(bool tma_store, int groups) {
-    return 1024 + (tma_store ? GemmLayout<true>::TAB_OFF : GemmLayout<false>::TAB_OFF) + 2 * 4 * (groups + 1);
+// dynamic shared memory: 1 KB alignment slack, layout, group tables (row
+// offsets, 128-row padded offsets and, for CTA pairs, 256-row padded offsets)
+__host__ __device__ constexpr int gemm_smem_bytes(bool tma_store, int groups, bool pair = false) {
+    return 1024 +
+           (pair ? (tma_store ? GemmLayout<true, true>::TAB_OFF : GemmLayout<false, true>::TAB_OFF)
+                 : (tma_store ? GemmLayout<true>::TAB_OFF : GemmLayout<false>::TAB_OFF)) +
+           (pair ? 3 : 2) * 4 * (groups + 1);
 }
 
 // K below which a bf16 GEMM takes the TMA-store epilogue.
@@ -135,7 +155,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity.  Gives up (false) when
 // the shared abort flag is raised or after G_WAIT_NS, raising the flag and
-// DEV_TIMEOUT.
+// DEV_TIMEOUT.  (Barriers that the other CTA of a pair signals are waited on
+// the same way: what they announce is TMA data or TMEM traffic, not memory
+// written by the signalling thread.)
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -206,14 +228,23 @@ __host__ __device__ constexpr uint32_t mxf4nvf4_idesc(int m, int n) {
 }
 
 
+template <bool PAIR>
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                        uint32_t sfb, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
-        : "memory");
+    if (PAIR)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+            : "memory");
 }
 
 #define NVFP4_R32(i) "=r"(v[i]), "=r"(v[i + 1]), "=r"(v[i + 2]), "=r"(v[i + 3])
@@ -240,27 +271,89 @@ __device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t* v) {
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 
+#define NVFP4_MMA4_ASM(CG)                                                                                   \
+    asm volatile(                                                                                            \
+        "{\n\t.reg .pred p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"                                   \
+        ".reg .b32 sa1, sa2, sa3, sb1, sb2, sb3;\n\t"                                                        \
+        "setp.ne.b32 p, %4, 0;\n\t"                                                                          \
+        "setp.eq.u32 t, 0, 0;\n\t"                                                                           \
+        "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"                                \
+        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"                                \
+        "add.u32 sa1, %5, 4;\n\tadd.u32 sa2, %5, 8;\n\tadd.u32 sa3, %5, 12;\n\t"                            \
+        "add.u32 sb1, %6, 8;\n\tadd.u32 sb2, %6, 16;\n\tadd.u32 sb3, %6, 24;\n\t"                           \
+        "tcgen05.mma.cta_group::" #CG ".kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t" \
+        "tcgen05.mma.cta_group::" #CG ".kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [sa1], [sb1], t;\n\t" \
+        "tcgen05.mma.cta_group::" #CG ".kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a2, b2, %3, [sa2], [sb2], t;\n\t" \
+        "tcgen05.mma.cta_group::" #CG ".kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a3, b3, %3, [sa3], [sb3], t;\n\t}" \
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)                          \
+        : "memory")
+
 // Four K=64 MMAs covering one 256-wide K stage.  The shared-memory
 // descriptors advance by 32 bytes (2 in descriptor units) per MMA inside the
 // 128-byte swizzle atom; scale columns advance by 4 (A) and 8 (B).  Only the
-// first MMA may start a fresh accumulator.
+// first MMA may start a fresh accumulator.  PAIR: cta_group::2, issued by the
+// first CTA of a pair for both (A rows and B rows split between the two
+// CTAs' shared memory at the same offsets, each CTA's TMEM holding its rows).
+template <bool PAIR>
 __device__ __forceinline__ void tc_mma4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                         uint32_t sfb, uint32_t accumulate) {
+    if (PAIR) NVFP4_MMA4_ASM(2);
+    else NVFP4_MMA4_ASM(1);
+}
+#undef NVFP4_MMA4_ASM
+
+// ------------------------------------------------------------------ CTA pairs
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address in the shared::cluster window of the variable at shared::cta
+// address `addr` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrivals on the other CTA's barriers are relaxed: what they announce is
+// either TMEM traffic already completed by tcgen05.wait::st / wait::ld (and
+// ordered by tcgen05.fence::before_thread_sync) or bytes that the TMA itself
+// reports, so no release of this thread's memory writes is needed.  Measured
+// on B300, cluster-scope release arrivals made the pair kernel twice as slow
+// as the single-CTA one (3.45 ms against 1.81 ms for the Ultra fprop GEMM).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t cluster_addr, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// TMA load into this CTA's shared memory that signals an mbarrier of either
+// CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 uint32_t cluster_bar) {
     asm volatile(
-        "{\n\t.reg .pred p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
-        ".reg .b32 sa1, sa2, sa3, sb1, sb2, sb3;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "setp.eq.u32 t, 0, 0;\n\t"
-        "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
-        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
-        "add.u32 sa1, %5, 4;\n\tadd.u32 sa2, %5, 8;\n\tadd.u32 sa3, %5, 12;\n\t"
-        "add.u32 sb1, %6, 8;\n\tadd.u32 sb2, %6, 16;\n\tadd.u32 sb3, %6, 24;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a1, b1, %3, [sa1], [sb1], t;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a2, b2, %3, [sa2], [sb2], t;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], a3, b3, %3, [sa3], [sb3], t;\n\t}"
-        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar)
         : "memory");
+}
+
+// Arrive once on the mbarrier at shared::cta offset `bar` in every CTA of
+// the pair when the pair MMAs issued so far have completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 ::"r"(bar), "h"(mask)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // tcgen05.st of 16 / 32 consecutive 32-bit columns into this warp's 32 TMEM lanes.
@@ -393,18 +486,52 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int mtiles, int ntil
     return c;
 }
 
+// Tiles of a CTA pair: 256 rows (two 128-row m-tiles of one group, the
+// second possibly past the group's end) x 256 columns, numbered in bands of
+// G_BAND / 2 row pairs like decode_tile.  Returns the m-tile of CTA `rank`.
+// A second m-tile past the group's end has rows = 0 and takes its partner's
+// scale row (mtg), so that its loads stay inside the scale buffer; its
+// results are never stored.
+__device__ __forceinline__ TileCoord decode_pair_tile(int64_t t, int ptiles, int ntiles, const int32_t* off,
+                                                      const int32_t* pad, const int32_t* pair, int groups,
+                                                      uint32_t rank) {
+    constexpr int PB = G_BAND / 2;
+    const int64_t band_tiles = (int64_t)PB * ntiles;
+    const int band = (int)(t / band_tiles);
+    const int64_t local = t - (int64_t)band * band_tiles;
+    const int bsize = min(PB, ptiles - band * PB);
+    const int pt = band * PB + (int)(local % bsize);
+    TileCoord c;
+    c.nt = (int)(local / bsize);
+    int lo = 0, hi = groups;
+    const int32_t key = pt * 256;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pair[mid] <= key) lo = mid; else hi = mid;
+    }
+    c.g = lo;
+    const int32_t lm = 2 * (pt - pair[lo] / 256) + (int32_t)rank;     // m-tile inside the group
+    c.row0 = off[lo] + lm * 128;
+    c.rows = max(0, min(128, off[lo + 1] - c.row0));
+    c.mtg = pad[lo] / 128 + (c.rows > 0 ? lm : lm - 1);
+    return c;
+}
+
 __device__ __forceinline__ uint4 ldg_u4(const uint8_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
 // ------------------------------------------------------------------ kernel
 // OUT_FP32: FP32 output (stored directly); otherwise bf16.  TMA_STORE (bf16
 // only): the output leaves through tm_c (rows 16-byte aligned).
-template <bool OUT_FP32, bool TMA_STORE>
+template <bool OUT_FP32, bool TMA_STORE, bool PAIR>
 __global__ void __launch_bounds__(G_THREADS, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                  const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
     static_assert(!(OUT_FP32 && TMA_STORE), "the TMA-store epilogue is bf16 only");
-    using L = GemmLayout<TMA_STORE>;
+    using L = GemmLayout<TMA_STORE, PAIR>;
     constexpr int G_STAGES = L::STAGES;
+    constexpr int STAGE_BYTES = L::STAGE_BYTES;
+    static_assert(G_SF_COL0 + G_STAGES * G_SF_COLS_PER_STAGE <= G_TMEM_COLS, "scale columns exceed TMEM");
+    static_assert((4 * G_STAGES + 3) * 8 + 8 <= G_BAR_BYTES, "barriers exceed their space");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
@@ -415,7 +542,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int32_t* tab = reinterpret_cast<int32_t*>(smem + L::TAB_OFF);
     const int groups = p.groups;
-    GroupTables gt{tab, tab + groups + 1};
+    GroupTables gt{tab, tab + groups + 1, PAIR ? tab + 2 * (groups + 1) : nullptr};
+    // CTA pairs: rank 0 issues the MMAs of both; barriers that collect both
+    // CTAs' arrivals (full, sf_full, acc_empty) are rank 0's.
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + G_STAGES), sff0 = smem_u32(bars + 2 * G_STAGES);
@@ -424,13 +554,13 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < G_STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1);
+            mbar_init(full0 + 8 * s, PAIR ? 2 : 1);
             mbar_init(empty0 + 8 * s, 1);
-            mbar_init(sff0 + 8 * s, 4);
+            mbar_init(sff0 + 8 * s, PAIR ? 8 : 4);
             mbar_init(sfl0 + 8 * s, 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, G_EPI_WARPS);
+        mbar_init(acc_empty, PAIR ? 2 * G_EPI_WARPS : G_EPI_WARPS);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -442,10 +572,17 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         if (TMA_STORE) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_c)) : "memory");
     }
     if (warp == G_W_MMA) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(G_TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (PAIR) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                         "r"(G_TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                         "r"(G_TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     if (p.offsets != nullptr) {
         build_group_tables(p.offsets, groups, p.M, gt);
@@ -454,15 +591,25 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         gt.off[1] = (int32_t)p.M;
         gt.pad[0] = 0;
         gt.pad[1] = (int32_t)(((p.M + 127) >> 7) << 7);
+        if (PAIR) { gt.pair[0] = 0; gt.pair[1] = (int32_t)(((p.M + 255) >> 8) << 8); }
     }
     tc_fence_before();
-    __syncthreads();
+    if (PAIR) cluster_sync();   // both CTAs' barriers initialised before any arrival from the other
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     const int mtiles = gt.pad[groups] >> 7;
+    const int ptiles = PAIR ? (gt.pair[groups] >> 8) : 0;
     const int ntiles = (int)((p.N + G_BN - 1) / G_BN);
-    const int64_t total = (int64_t)mtiles * ntiles;
+    const int64_t total = (int64_t)(PAIR ? ptiles : mtiles) * ntiles;
+    // a pair walks the tiles of its cluster (blockIdx.x / 2), both CTAs alike
+    const int64_t t_first = PAIR ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+    const int64_t t_step = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
+    auto tile_at = [&](int64_t t) {
+        return PAIR ? decode_pair_tile(t, ptiles, ntiles, gt.off, gt.pad, gt.pair, groups, rank)
+                    : decode_tile(t, mtiles, ntiles, gt.off, gt.pad, groups);
+    };
     const int kstages = (int)((p.K + G_BK - 1) / G_BK);
     const int katoms = (int)((p.K + 63) / 64);
     const int nrb = (int)((p.N + 127) / 128);            // 128-row scale blocks of one B operand
@@ -474,54 +621,70 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             int s = 0;
             uint32_t ph = 0, issued = 0, issued_ph = 0;   // per-stage bits: ever issued, parity of last issue
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const TileCoord tc = decode_tile(t, mtiles, ntiles, gt.off, gt.pad, groups);
-                const int32_t brow0 = (int32_t)(tc.g * b_rows_per_group + (int64_t)tc.nt * G_BN);
+            for (int64_t t = t_first; t < total && ok; t += t_step) {
+                const TileCoord tc = tile_at(t);
+                // PAIR: this CTA loads B rows 128 * rank .. + 127 of the 256-row tile
+                const int32_t brow0 =
+                    (int32_t)(tc.g * b_rows_per_group + (int64_t)tc.nt * G_BN + (PAIR ? 128 * (int64_t)rank : 0));
                 const uint8_t* sfb_g = p.sfb + (int64_t)tc.g * p.sfb_group_stride;
                 const bool rb2 = (tc.nt * 2 + 1) < nrb;
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) { ok = false; break; }
                     const int na = min(4, katoms - 4 * ks);
                     const uint32_t sfbytes = (uint32_t)na * 512u;
-                    const uint32_t st = smem_u32(stages + s * G_STAGE_BYTES);
+                    const uint32_t st = smem_u32(stages + s * STAGE_BYTES);
                     // the scales first, on their own barrier: they are small, land
                     // ahead of A and B, and the scale warps move them into TMEM
                     // while A and B are still arriving
                     const uint32_t sbar = sfl0 + 8 * s;
                     mbar_expect_tx(sbar, sfbytes * (rb2 ? 3u : 2u));
-                    const uint32_t ssf = st + G_A_BYTES + G_B_BYTES;
+                    const uint32_t ssf = st + G_A_BYTES + L::B_BYTES;
                     bulk_load(ssf, p.sfa + ((int64_t)tc.mtg * katoms + 4 * ks) * 512, sfbytes, sbar);
                     bulk_load(ssf + G_SFA_BYTES, sfb_g + ((int64_t)(tc.nt * 2) * katoms + 4 * ks) * 512, sfbytes, sbar);
                     if (rb2)
                         bulk_load(ssf + G_SFA_BYTES + 2048, sfb_g + ((int64_t)(tc.nt * 2 + 1) * katoms + 4 * ks) * 512,
                                   sfbytes, sbar);
-                    const uint32_t bar = full0 + 8 * s;
-                    mbar_expect_tx(bar, G_A_BYTES + G_B_BYTES);
-                    tma_load_2d(st, &tm_a, ks * 128, tc.row0, bar);
-                    tma_load_2d(st + G_A_BYTES, &tm_b, ks * 128, brow0, bar);
+                    if (PAIR) {
+                        // A and B of both CTAs complete on rank 0's full barrier
+                        const uint32_t bar = mapa_shared(full0 + 8 * s, 0);
+                        mbar_expect_tx_cluster(bar, G_A_BYTES + L::B_BYTES);
+                        tma_load_2d_pair(st, &tm_a, ks * 128, tc.row0, bar);
+                        tma_load_2d_pair(st + G_A_BYTES, &tm_b, ks * 128, brow0, bar);
+                    } else {
+                        const uint32_t bar = full0 + 8 * s;
+                        mbar_expect_tx(bar, G_A_BYTES + G_B_BYTES);
+                        tma_load_2d(st, &tm_a, ks * 128, tc.row0, bar);
+                        tma_load_2d(st + G_A_BYTES, &tm_b, ks * 128, brow0, bar);
+                    }
                     issued |= 1u << s;
                     issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                     if (++s == G_STAGES) { s = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
-                // let every copy already issued land before the CTA exits
+                // let every copy already issued land before the CTA exits (the
+                // other CTA of a pair cannot wait on rank 0's full barrier: it
+                // gives its copies a fixed millisecond instead)
                 volatile int never = 0;
                 for (int i = 0; i < G_STAGES; ++i)
                     if ((issued >> i) & 1u) {
                         mbar_wait(sfl0 + 8 * i, (issued_ph >> i) & 1u, &never);
-                        mbar_wait(full0 + 8 * i, (issued_ph >> i) & 1u, &never);
+                        if (rank == 0) mbar_wait(full0 + 8 * i, (issued_ph >> i) & 1u, &never);
                     }
+                if (PAIR && rank != 0) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
+                }
             }
         }
     } else if (warp == G_W_MMA) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = mxf4nvf4_idesc(G_BM, G_BN);
+        // ------------------------------------------------ MMA issuer (rank 0 of a pair)
+        if (lane == 0 && rank == 0) {
+            const uint32_t idesc = mxf4nvf4_idesc(PAIR ? 2 * G_BM : G_BM, G_BN);
             int s = 0;
             uint32_t ph = 0, it = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+            for (int64_t t = t_first; t < total && ok; t += t_step, ++it) {
                 if (!mbar_wait(acc_empty, (it & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 for (int ks = 0; ks < kstages; ++ks) {
@@ -531,49 +694,54 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     }
                     tc_fence_after();
                     const int na = min(4, katoms - 4 * ks);
-                    const uint32_t st = smem_u32(stages + s * G_STAGE_BYTES);
+                    const uint32_t st = smem_u32(stages + s * STAGE_BYTES);
                     const uint32_t sfa_t = tmem + G_SF_COL0 + s * G_SF_COLS_PER_STAGE;
                     const uint32_t sfb_t = sfa_t + 16;
                     const uint64_t ad = smem_desc(st, 16, 1024, 2);
                     const uint64_t bd = smem_desc(st + G_A_BYTES, 16, 1024, 2);
                     if (na == 4) {
-                        tc_mma4(tmem, ad, bd, idesc, sfa_t, sfb_t, ks != 0 ? 1u : 0u);
+                        tc_mma4<PAIR>(tmem, ad, bd, idesc, sfa_t, sfb_t, ks != 0 ? 1u : 0u);
                     } else {
                         for (int j = 0; j < na; ++j)
-                            tc_mma(tmem, ad + 2 * j, bd + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 8 * j,
-                                   (ks | j) != 0 ? 1u : 0u);
+                            tc_mma<PAIR>(tmem, ad + 2 * j, bd + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 8 * j,
+                                         (ks | j) != 0 ? 1u : 0u);
                     }
-                    tc_commit(empty0 + 8 * s);
+                    if (PAIR) tc_commit_pair(empty0 + 8 * s, 3);
+                    else tc_commit(empty0 + 8 * s);
                     if (++s == G_STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit(acc_full);
+                if (PAIR) tc_commit_pair(acc_full, 3);
+                else tc_commit(acc_full);
             }
             // every MMA issued by this thread completes before teardown
-            tc_commit(drain);
+            if (PAIR) tc_commit_pair(drain, 1);
+            else tc_commit(drain);
             volatile int never = 0;
             mbar_wait(drain, 0, &never);
         }
     } else if (warp < G_W_EPI0) {
         // ------------------------------------------------ scale factors -> TMEM
         // The producer lands the stage's scale atoms in shared memory next to
-        // A and B (on their own barrier, ahead of A and B).  Lane i of every quarter copies the 16 bytes at offset 16*i
-        // of each 512-byte atom (the 4 scales of rows i, i+32, i+64, i+96) into
-        // the atom's 4 TMEM columns.  The stage's TMEM columns are free once
-        // its data has landed: the producer refilled it only after the MMAs of
-        // its previous use completed.
+        // A and B (on their own barrier, ahead of A and B).  Lane i of every
+        // quarter copies the 16 bytes at offset 16*i of each 512-byte atom (the
+        // 4 scales of rows i, i+32, i+64, i+96) into the atom's 4 TMEM columns.
+        // The stage's TMEM columns are free once its data has landed: the
+        // producer refilled it only after the MMAs of its previous use
+        // completed.  In a CTA pair each CTA writes its own A scales and all
+        // 256 rows of B scales into its own TMEM.
         const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const TileCoord tc = decode_tile(t, mtiles, ntiles, gt.off, gt.pad, groups);
+        for (int64_t t = t_first; t < total && ok; t += t_step) {
+            const TileCoord tc = tile_at(t);
             const bool rb2 = (tc.nt * 2 + 1) < nrb;
             for (int ks = 0; ks < kstages; ++ks) {
                 const int na = min(4, katoms - 4 * ks);
                 if (!mbar_wait(sfl0 + 8 * s, ph, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint8_t* ssf = stages + s * G_STAGE_BYTES + G_A_BYTES + G_B_BYTES + lane * 16;
+                const uint8_t* ssf = stages + s * STAGE_BYTES + G_A_BYTES + L::B_BYTES + lane * 16;
                 uint4 va[4], vb[8];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -589,7 +757,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sff0 + 8 * s);
+                if (lane == 0) {
+                    if (PAIR) mbar_arrive_cluster(mapa_shared(sff0 + 8 * s, 0));
+                    else mbar_arrive(sff0 + 8 * s);
+                }
                 if (++s == G_STAGES) { s = 0; ph ^= 1u; }
             }
         }
@@ -599,8 +770,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         const int chunk = (warp - G_W_EPI0) >> 2;        // 64-column chunk of the tile
         const int r = q * 32 + lane;                     // row inside the tile
         uint32_t it = 0;
-        for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-            const TileCoord tc = decode_tile(t, mtiles, ntiles, gt.off, gt.pad, groups);
+        // PAIR: the accumulator of this CTA's 128 rows is released to rank 0
+        const uint32_t acc_release = PAIR ? mapa_shared(acc_empty, 0) : acc_empty;
+        for (int64_t t = t_first; t < total; t += t_step, ++it) {
+            const TileCoord tc = tile_at(t);
             const float alpha = __fmul_rn(tensor_decode_scale(p.amax_a[tc.g]), tensor_decode_scale(p.amax_b[tc.g]));
             if (!mbar_wait(acc_full, it & 1u, abort_flag)) break;
             tc_fence_after();
@@ -618,7 +791,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     if (h == 1) {
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty);
+                        if (lane == 0) { if (PAIR) mbar_arrive_cluster(acc_release); else mbar_arrive(acc_empty); }
                     }
                     const int64_t cstart = col0 + 32 * h;
                     if (cstart >= p.N) continue;
@@ -663,7 +836,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                         if (h == 1 && k == 1) {
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(acc_empty);
+                            if (lane == 0) { if (PAIR) mbar_arrive_cluster(acc_release); else mbar_arrive(acc_empty); }
                         }
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
@@ -722,7 +895,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     if (h == 3) {
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty);
+                        if (lane == 0) { if (PAIR) mbar_arrive_cluster(acc_release); else mbar_arrive(acc_empty); }
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -753,10 +926,14 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     }
 
     tc_fence_before();
-    __syncthreads();
+    if (PAIR) cluster_sync();   // neither CTA leaves while the other may still signal or read it
+    else __syncthreads();
     if (warp == G_W_MMA) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(G_TMEM_COLS) : "memory");
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(G_TMEM_COLS) : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(G_TMEM_COLS) : "memory");
     }
 }
 

@@ -4,6 +4,7 @@
 // kernels of quant.cuh and gemm.cuh on the caller's stream.  It allocates no
 // device memory.
 #include <cuda.h>
+#include <cstdlib>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -47,6 +48,7 @@ struct DeviceInfo {
     bool ok = false;
     int sms = 0;
     bool gemm_attr = false;
+    int pair_clusters = 0;
 };
 DeviceInfo g_dev[64];
 std::mutex g_dev_mu;
@@ -494,31 +496,112 @@ static nvfp4_status check_operand(const nvfp4_tensor* t, const char* name) {
     return NVFP4_OK;
 }
 
+}  // extern "C"
+
+// CTA pairs (cta_group::2) unless NVFP4_GEMM_PAIR=0 is set in the
+// environment (read at every call, so a process can compare both kernels).
+static bool use_pair() {
+    const char* e = std::getenv("NVFP4_GEMM_PAIR");
+    return !(e != nullptr && e[0] == '0');
+}
+
+template <bool F32, bool TS, bool PAIR>
+static nvfp4_status launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                               const GemmParams& p, int grid, int smem, nvfp4_stream_t stream) {
+    auto kern = k_gemm_nvfp4<F32, TS, PAIR>;
+    if (!PAIR) {
+        kern<<<grid, G_THREADS, smem, stream>>>(ma, mb, mc, p);
+        return launched("k_gemm_nvfp4");
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(G_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    NVFP4_TRY(cuda_call(cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, p), "k_gemm_nvfp4 pair launch"));
+    return launched("k_gemm_nvfp4 pair");
+}
+
+template <bool F32, bool TS, bool PAIR>
+static nvfp4_status set_gemm_attr() {
+    NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<F32, TS, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             gemm_smem_bytes(TS, NVFP4_MAX_GROUPS, PAIR)),
+                        "smem attr"));
+    if (PAIR)
+        NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<F32, TS, PAIR>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0),
+                            "cluster attr"));
+    return NVFP4_OK;
+}
+
+// Largest number of co-resident CTA pairs of the pair kernel (the grid is
+// sized to it: the kernel is persistent over tiles).
+template <bool F32, bool TS>
+static nvfp4_status pair_clusters(int smem, int* out) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(G_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    NVFP4_TRY(cuda_call(cudaOccupancyMaxActiveClusters(&n, k_gemm_nvfp4<F32, TS, true>, &cfg), "cluster occupancy"));
+    *out = n;
+    return NVFP4_OK;
+}
+
+// tiles_1cta: output tiles of 128 x 256 (grid bound of the single-CTA
+// kernel); pair_tiles: tiles of 256 x 256.
 static nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
-                                const GemmParams& p, int grid, nvfp4_out_dtype dt, bool tma_store,
-                                nvfp4_stream_t stream, int dev) {
+                                const GemmParams& p, int64_t tiles_1cta, int64_t pair_tiles, int sms,
+                                nvfp4_out_dtype dt, bool tma_store, bool pair, nvfp4_stream_t stream, int dev) {
     const bool f32 = dt == NVFP4_OUT_FP32;
-    const int smem = gemm_smem_bytes(tma_store, p.groups);
+    const int smem = gemm_smem_bytes(tma_store, p.groups, pair);
+    int clusters = 0;
     {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         if (!g_dev[dev].gemm_attr) {
-            NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     gemm_smem_bytes(false, NVFP4_MAX_GROUPS)), "smem attr"));
-            NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     gemm_smem_bytes(true, NVFP4_MAX_GROUPS)), "smem attr"));
-            NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     gemm_smem_bytes(false, NVFP4_MAX_GROUPS)), "smem attr"));
+            NVFP4_TRY((set_gemm_attr<false, false, false>()));
+            NVFP4_TRY((set_gemm_attr<false, true, false>()));
+            NVFP4_TRY((set_gemm_attr<true, false, false>()));
+            NVFP4_TRY((set_gemm_attr<false, false, true>()));
+            NVFP4_TRY((set_gemm_attr<false, true, true>()));
+            NVFP4_TRY((set_gemm_attr<true, false, true>()));
+            const int full = gemm_smem_bytes(true, NVFP4_MAX_GROUPS, true);   // the largest pair layout
+            int c0 = 0, c1 = 0, c2 = 0;
+            NVFP4_TRY((pair_clusters<false, false>(full, &c0)));
+            NVFP4_TRY((pair_clusters<false, true>(full, &c1)));
+            NVFP4_TRY((pair_clusters<true, false>(full, &c2)));
+            g_dev[dev].pair_clusters = std::min(c0, std::min(c1, c2));
             g_dev[dev].gemm_attr = true;
         }
+        clusters = g_dev[dev].pair_clusters;
     }
-    if (f32)
-        k_gemm_nvfp4<true, false><<<grid, G_THREADS, smem, stream>>>(ma, mb, mc, p);
-    else if (tma_store)
-        k_gemm_nvfp4<false, true><<<grid, G_THREADS, smem, stream>>>(ma, mb, mc, p);
-    else
-        k_gemm_nvfp4<false, false><<<grid, G_THREADS, smem, stream>>>(ma, mb, mc, p);
-    return launched("k_gemm_nvfp4");
+    if (!pair) {
+        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_1cta, sms));
+        if (f32) return launch_one<true, false, false>(ma, mb, mc, p, grid, smem, stream);
+        if (tma_store) return launch_one<false, true, false>(ma, mb, mc, p, grid, smem, stream);
+        return launch_one<false, false, false>(ma, mb, mc, p, grid, smem, stream);
+    }
+    if (clusters < 1) return fail(NVFP4_ERR_CUDA, "the CTA-pair GEMM cannot be resident");
+    const int grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(pair_tiles, clusters));
+    if (f32) return launch_one<true, false, true>(ma, mb, mc, p, grid, smem, stream);
+    if (tma_store) return launch_one<false, true, true>(ma, mb, mc, p, grid, smem, stream);
+    return launch_one<false, false, true>(ma, mb, mc, p, grid, smem, stream);
 }
+
+extern "C" {
 
 // Store tensor map of a bf16 output [rows, n] with row stride ldc: boxes of
 // 32 x 32 elements (64-byte rows) with 64-byte swizzle.  Only built when C
@@ -558,9 +641,10 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* c, i
     if (((uintptr_t)c % esz) != 0) return fail(NVFP4_ERR_ALIGN, "c is not aligned to its element size");
     int sms = 0, dev = 0;
     NVFP4_TRY(check_device(&sms, &dev));
+    const bool pair = use_pair();
     CUtensorMap ma, mb;
     NVFP4_TRY(make_code_map(&ma, a->codes, M, K / 2, G_BM));
-    NVFP4_TRY(make_code_map(&mb, b->codes, N, K / 2, G_BN));
+    NVFP4_TRY(make_code_map(&mb, b->codes, N, K / 2, pair ? G_BN / 2 : G_BN));
     GemmParams p{};
     p.M = M; p.N = N; p.K = K;
     p.offsets = nullptr; p.groups = 1;
@@ -578,8 +662,8 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* c, i
     std::memset(&mc, 0, sizeof(mc));
     if (c_dtype == NVFP4_OUT_BF16 && K < G_TMA_STORE_MAX_K) NVFP4_TRY(make_store_map(&mc, c, M, N, ldc, &tma_store));
     const int64_t tiles = cdiv(M, G_BM) * cdiv(N, G_BN);
-    const int grid = (int)std::min<int64_t>(tiles, sms);
-    return launch_gemm(ma, mb, mc, p, grid, c_dtype, tma_store, stream, dev);
+    const int64_t pair_tiles = cdiv(M, 2 * G_BM) * cdiv(N, G_BN);
+    return launch_gemm(ma, mb, mc, p, tiles, pair_tiles, sms, c_dtype, tma_store, pair, stream, dev);
 }
 
 nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, int32_t num_groups,
@@ -604,9 +688,10 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, i
     if (((uintptr_t)c % esz) != 0) return fail(NVFP4_ERR_ALIGN, "c is not aligned to its element size");
     int sms = 0, dev = 0;
     NVFP4_TRY(check_device(&sms, &dev));
+    const bool pair = use_pair();
     CUtensorMap ma, mb;
     NVFP4_TRY(make_code_map(&ma, a->codes, R, K / 2, G_BM));
-    NVFP4_TRY(make_code_map(&mb, b->codes, n * num_groups, K / 2, G_BN));
+    NVFP4_TRY(make_code_map(&mb, b->codes, n * num_groups, K / 2, pair ? G_BN / 2 : G_BN));
     GemmParams p{};
     p.M = R; p.N = n; p.K = K;
     p.offsets = offsets; p.groups = num_groups;
@@ -623,7 +708,8 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, i
     bool tma_store = false;
     std::memset(&mc, 0, sizeof(mc));
     if (c_dtype == NVFP4_OUT_BF16 && K < G_TMA_STORE_MAX_K) NVFP4_TRY(make_store_map(&mc, c, R, n, ldc, &tma_store));
-    return launch_gemm(ma, mb, mc, p, sms, c_dtype, tma_store, stream, dev);
+    // tiles depend on the group sizes (device data): the grid is the SM count
+    return launch_gemm(ma, mb, mc, p, sms, sms / 2, sms, c_dtype, tma_store, pair, stream, dev);
 }
 
 nvfp4_status nvfp4_device_status(int32_t* flags) {

@@ -86,8 +86,9 @@ __global__ void __launch_bounds__(256) k_amax(const uint16_t* __restrict__ x, in
 // scale-row offsets P[0..G] (P[g] = sum_{i<g} ceil(cnt_i/128)*128).  Offsets
 // that are out of range or decreasing are clamped (and flagged).
 struct GroupTables {
-    int32_t* off;    // [G+1]
-    int32_t* pad;    // [G+1]
+    int32_t* off;              // [G+1]
+    int32_t* pad;              // [G+1]
+    int32_t* pair = nullptr;   // [G+1], optional: sum_{i<g} ceil(cnt_i/256)*256 (tiles of CTA pairs)
 };
 
 __device__ void build_group_tables(const int64_t* __restrict__ offsets, int32_t groups,
@@ -140,28 +141,33 @@ __device__ void build_group_tables(const int64_t* __restrict__ offsets, int32_t 
         }
     }
     __syncthreads();
-    // 2) padded scale rows: exclusive sum of ceil(cnt/128)*128
-    int32_t local_sum = 0;
-    for (int i = 0; i < per; ++i) {
-        const int g = g0 + i;
-        if (g < groups) local_sum += ((t.off[g + 1] - t.off[g] + 127) >> 7) << 7;
-    }
-    int32_t inc = local_sum;
-    for (int d = 1; d < 32; d <<= 1) {
-        const int32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
-        if (lane >= d) inc += o;
-    }
-    __syncthreads();
-    if (lane == 31) s_wsum[warp] = inc;
-    __syncthreads();
-    int32_t base = 0;
-    for (int w = 0; w < warp; ++w) base += s_wsum[w];
-    int32_t acc = base + inc - local_sum;
-    for (int i = 0; i < per; ++i) {
-        const int g = g0 + i;
-        if (g <= groups) {
-            t.pad[g] = acc;
-            if (g < groups) acc += ((t.off[g + 1] - t.off[g] + 127) >> 7) << 7;
+    // 2) padded rows: exclusive sums of ceil(cnt/128)*128 (scale rows) and,
+    //    when asked, of ceil(cnt/256)*256 (row tiles of CTA pairs)
+    for (int which = 0; which < (t.pair != nullptr ? 2 : 1); ++which) {
+        const int sh = which == 0 ? 7 : 8;
+        int32_t* dst = which == 0 ? t.pad : t.pair;
+        int32_t local_sum = 0;
+        for (int i = 0; i < per; ++i) {
+            const int g = g0 + i;
+            if (g < groups) local_sum += ((t.off[g + 1] - t.off[g] + (1 << sh) - 1) >> sh) << sh;
+        }
+        int32_t inc = local_sum;
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+            if (lane >= d) inc += o;
+        }
+        __syncthreads();
+        if (lane == 31) s_wsum[warp] = inc;
+        __syncthreads();
+        int32_t base = 0;
+        for (int w = 0; w < warp; ++w) base += s_wsum[w];
+        int32_t acc = base + inc - local_sum;
+        for (int i = 0; i < per; ++i) {
+            const int g = g0 + i;
+            if (g <= groups) {
+                dst[g] = acc;
+                if (g < groups) acc += ((t.off[g + 1] - t.off[g] + (1 << sh) - 1) >> sh) << sh;
+            }
         }
     }
     if (bad && blockIdx.x == 0) raise_status(DEV_BAD_OFFSETS);

@@ -12,6 +12,17 @@ from parity import gemm_within_bound, np_u8
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["pair", "single"], autouse=True)
+def gemm_kernel(request, monkeypatch):
+    """Every GEMM test runs on both kernels: CTA pairs (cta_group::2, the
+    default) and single CTAs (NVFP4_GEMM_PAIR=0)."""
+    if request.param == "single":
+        monkeypatch.setenv("NVFP4_GEMM_PAIR", "0")
+    else:
+        monkeypatch.delenv("NVFP4_GEMM_PAIR", raising=False)
+    return request.param
+
+
 @pytest.fixture(scope="module")
 def B():
     from nvfp4_precision_02_b300 import binding, build
