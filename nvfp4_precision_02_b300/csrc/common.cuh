@@ -91,29 +91,26 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float (&f)[8]) {
 // neighbours lo <= |v| < hi and p = (|v| - lo) / (hi - lo), the magnitude
 // rounds up iff (u >> 8) < p * 2^24, i.e. iff u < 256 * ceil(p * 2^24).
 // Branch-free integer form on the FP32 bits mb of |v|:
-//   |v| in [1, 6):   the grid step is bit 22 of mb; adding (~u >> 10) to the
-//                    22 bits below it carries into bit 22 exactly when
-//                    (u >> 10) < those bits, and the carried value's bits
-//                    22..30 give the code: (mb + (~u >> 10)) >> 22, minus 252;
-//   |v| in [0.5, 1): the step is the exponent: (mb + (~u >> 9)) >> 23, minus 125;
-//   |v| in [0, 0.5): up iff u < 256 * ceil(|v| * 2^25), the ceiling taken by
-//                    a rounding-up shift of the significand.
+//   |v| >= 0.5: the grid step is bit k of mb (k = 22 on [1, 6), the mantissa
+//               bit; k = 23 on [0.5, 1), the exponent); adding (~u >> (32-k))
+//               to the k bits below it carries into bit k exactly when
+//               (u >> (32-k)) < those bits, and (mb + (~u >> (32-k))) >> k,
+//               minus 252 (k = 22) or 125 (k = 23), is the code; codes past
+//               7 (|v| >= 6, including rounding 6 <= |v| < 8 upwards) clamp
+//               to 7;
+//   |v| < 0.5:  up iff u < 256 * ceil(|v| * 2^25) (|v| * 2^25 < 2^24 is
+//               exact in FP32 and converted with rounding up).
 // It equals the FP32 statement above at both sides of every threshold for
 // every FP32 bit pattern (checked exhaustively on the host); the decision is
 // monotone in u, so that covers all words.
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u) {
     const uint32_t bits = __float_as_uint(v);
     const uint32_t mb = bits & 0x7FFFFFFFu;
-    const uint32_t nu = ~u;
-    const uint32_t c_hi = ((mb + (nu >> 10)) >> 22) - 252u;
-    const uint32_t c_mid = ((mb + (nu >> 9)) >> 23) - 125u;
-    const uint32_t ef = mb >> 23;
-    const uint32_t sh = (uint32_t)min(max(125 - (int)ef, 0), 31);
-    const uint32_t sig = (mb & 0x7FFFFFu) | (ef != 0u ? 0x800000u : 0u);
-    const uint32_t x = (sig + (1u << sh) - 1u) >> sh;              // ceil(|v| * 2^25) < 2^24
-    const uint32_t c_lo = u < (x << 8) ? 1u : 0u;
-    uint32_t c = mb >= 0x3F800000u ? c_hi : (mb >= 0x3F000000u ? c_mid : c_lo);
-    c = mb >= 0x40C00000u ? 7u : c;                                 // |v| >= 6 saturates
+    const bool ge1 = mb >= 0x3F800000u;
+    const uint32_t k = ge1 ? 22u : 23u;
+    const uint32_t c_up = min(((mb + (~u >> (32u - k))) >> k) - (ge1 ? 252u : 125u), 7u);
+    const uint32_t x = __float2uint_ru(fabsf(v) * 33554432.0f);    // ceil(|v| * 2^25)
+    const uint32_t c = mb >= 0x3F000000u ? c_up : (u < (x << 8) ? 1u : 0u);
     return ((bits >> 28) & 8u) | c;
 }
 

@@ -772,8 +772,17 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         uint32_t it = 0;
         // PAIR: the accumulator of this CTA's 128 rows is released to rank 0
         const uint32_t acc_release = PAIR ? mapa_shared(acc_empty, 0) : acc_empty;
+        // output amax: each lane keeps a running max over the tiles of one
+        // group; the warp merges it into c_amax[group] when the group changes
+        int amax_g = -1;
+        uint32_t amax_run = 0;
         for (int64_t t = t_first; t < total; t += t_step, ++it) {
             const TileCoord tc = tile_at(t);
+            if (p.c_amax != nullptr && tc.g != amax_g) {
+                if (amax_g >= 0) warp_amax_to(p.c_amax + amax_g, amax_run);
+                amax_g = tc.g;
+                amax_run = 0;
+            }
             const float alpha = __fmul_rn(tensor_decode_scale(p.amax_a[tc.g]), tensor_decode_scale(p.amax_b[tc.g]));
             if (!mbar_wait(acc_full, it & 1u, abort_flag)) break;
             tc_fence_after();
@@ -802,7 +811,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             m = fmaxf(m, i < valid ? fabsf(__uint_as_float(v[i])) : 0.0f);
-                        warp_amax_to(p.c_amax + tc.g, __float_as_uint(__fmul_rn(alpha, m)));
+                        amax_run = max(amax_run, __float_as_uint(__fmul_rn(alpha, m)));
                     }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[i])));
@@ -849,7 +858,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     if (cstart >= p.N) continue;
                     if (p.c_amax != nullptr) {
                         const int valid = r < tc.rows ? (int)(p.N - cstart >= 32 ? 32 : p.N - cstart) : 0;
-                        warp_amax_to(p.c_amax + tc.g, bf16_absmax(w, valid) << 16);
+                        amax_run = max(amax_run, bf16_absmax(w, valid) << 16);
                     }
                     if (rows_full) {
                         // the staging buffer is free once the previous box has been read
@@ -907,7 +916,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 if (col0 >= p.N) continue;
                 if (p.c_amax != nullptr) {
                     const int valid = r < tc.rows ? (int)(p.N - col0 >= 64 ? 64 : p.N - col0) : 0;
-                    warp_amax_to(p.c_amax + tc.g, bf16_absmax(w, valid) << 16);
+                    amax_run = max(amax_run, bf16_absmax(w, valid) << 16);
                 }
                 if (p.vec_store) {
                     rows_to_segments(w);
@@ -921,6 +930,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 }
             }
         }
+        if (amax_g >= 0) warp_amax_to(p.c_amax + amax_g, amax_run);
         // every TMA store of this warp has finished before the CTA exits
         if (TMA_STORE && lane == 0) bulk_wait0();
     }
