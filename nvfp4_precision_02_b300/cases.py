@@ -4,7 +4,9 @@ Usage:
   python -m nvfp4_precision_02_b300.cases <op> [--workload super|ultra] [--iters N]
 
 <op> is one of: amax, quant1d_rne, quant1d_sr, quant2d, quant2d_moe, quant2d_moe_fused, rht_sr,
-gemm_fprop, gemm_dgrad, gemm_wgrad, grouped_up, grouped_down.  The inputs of the op are generated on the device and
+quant1d_grouped_a (per-expert amax + RNE of the routed activations), quant1d_grouped_h (RNE of
+the expert hidden activations with their amax supplied), gemm_fprop, gemm_dgrad, gemm_wgrad,
+grouped_up, grouped_down.  The inputs of the op are generated on the device and
 its operands quantised once; the op itself is then launched `iters` times back to back, so
 a profiler can skip the set-up launches and capture the op alone (for example with
 `ncu -k regex:<kernel> -s 1 -c 1`).  It prints the mean CUDA-event time per launch.
@@ -20,7 +22,8 @@ from . import binding as B
 from . import workloads as wl
 
 OPS = ["amax", "quant1d_rne", "quant1d_sr", "quant2d", "quant2d_moe", "quant2d_moe_fused", "rht_sr",
-       "gemm_fprop", "gemm_dgrad", "gemm_wgrad", "grouped_up", "grouped_down"]
+       "quant1d_grouped_a", "quant1d_grouped_h", "gemm_fprop", "gemm_dgrad", "gemm_wgrad", "grouped_up",
+       "grouped_down"]
 
 
 def prepare(op: str, which: str, dev):
@@ -51,6 +54,18 @@ def prepare(op: str, which: str, dev):
             return lambda: B.quantize_2d(w, want_t=False, out=qw)
         ws = torch.empty(B.quantize_2d_fused_workspace(m.experts), dtype=torch.uint8, device=dev)
         return lambda: B.quantize_2d_fused(w, workspace=ws, out=qw)
+    if op.startswith("quant1d_grouped"):
+        mi = wl.moe_inputs(m, which, device=dev, want=("a",))
+        off = mi["routing"].offsets.to(dev)
+        R = int(mi["routing"].offsets[-1])
+        if op == "quant1d_grouped_a":
+            qa = B.empty_qtensor(R, m.latent, dev, n_amax=m.experts, sf_size=B.sf_bytes_grouped(R, m.latent, m.experts))
+            return lambda: B.quantize_1d_grouped(mi["a"], off, B.RNE, 0, out=qa)
+        h = wl.normal_bf16((R, m.expert_hidden), 1.0, 99, dev)
+        qh = B.empty_qtensor(R, m.expert_hidden, dev, n_amax=m.experts,
+                             sf_size=B.sf_bytes_grouped(R, m.expert_hidden, m.experts))
+        B.quantize_1d_grouped(h, off, B.RNE, 0, out=qh)          # per-expert amax, reused below
+        return lambda: B.quantize_1d_grouped(h, off, B.RNE, 0, amax_in=qh.amax, out=qh)
     if op.startswith("gemm_"):
         ins = wl.dense_inputs(d, which, device=dev)
         x, w, dy = ins["x"], ins["w"], ins["dy"]

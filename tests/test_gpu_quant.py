@@ -164,13 +164,13 @@ def test_quantize_1d_ties_signed_zeros_saturation(B, orc):
 
 @pytest.mark.parametrize("batch,rows,cols", [(1, 48, 80), (2, 144, 1040), (5, 320, 256), (3, 64, 64),
                                              (7, 2688 // 8, 1024 // 8), (4, 16, 3072),
-                                             (40, 512, 2048), (2, 2048, 8192)])
+                                             (40, 512, 2048), (2, 2048, 8192), (1, 5120, 2048), (3, 5120, 2048)])
 def test_quantize_2d_fused(B, orc, batch, rows, cols):
     """One-pass (amax in the same cooperative launch) 2D quantisation gives
     the oracle's bytes, for one entry and several, one 16-row strip per entry
     and many, a column count that leaves a partial 256-column item, entries
     of fewer items than the grid has warps (40 x 256 items) and of more
-    (2 x 4096 items)."""
+    (2 x 4096 items), and Ultra expert weights (5120 x 2048)."""
     g = torch.Generator().manual_seed(batch * 1000 + rows + cols)
     w = (torch.randn(batch, rows, cols, generator=g) * 0.02 *
          torch.exp(torch.rand(batch, 1, 1, generator=g) * 6 - 3)).to(torch.bfloat16)
