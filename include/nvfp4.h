@@ -251,7 +251,11 @@ nvfp4_status nvfp4_rht_quantize(const void *x, int64_t tokens, int64_t cols, int
  * max |c| over the written outputs (of the stored bf16 values for a bf16 c),
  * the tensor amax a following quantisation of c can take as amax_in instead
  * of reading c again; it is zeroed by the call (left untouched when M or N
- * is 0). */
+ * is 0).
+ * Kernel: pairs of CTAs on two SMs (tcgen05 cta_group::2, 256 x 256 tiles)
+ * unless the environment variable NVFP4_GEMM_PAIR is "0" at the call, which
+ * selects single CTAs (128 x 256 tiles); both give the same bits.  The same
+ * holds for nvfp4_grouped_gemm. */
 nvfp4_status nvfp4_gemm(const nvfp4_tensor *a, const nvfp4_tensor *b, void *c, int64_t ldc,
                         nvfp4_out_dtype c_dtype, float *c_amax, nvfp4_stream_t stream);
 
