@@ -70,6 +70,9 @@ def lib():
             "oracle_rht_amax": (f32, [P, i64, i64, i64, ctypes.c_uint16]),
             "oracle_rht_quantize": (None, [P, i64, i64, i64, ctypes.c_uint16, ctypes.c_int, u64,
                                            P, P, P, P]),
+            "oracle_group_k_offset": (i64, [P, i32]),
+            "oracle_rht_quantize_grouped": (None, [P, i64, i64, i64, P, i32, i64, ctypes.c_uint16, ctypes.c_int,
+                                                   u64, P, P, P, P]),
             "oracle_dequantize_rows": (None, [P, P, i64, i64, f32, P, i64, P]),
             "oracle_gemm": (None, [P, P, i64, i64, i64, P, P]),
             "oracle_num_threads": (ctypes.c_int, []),
@@ -244,6 +247,28 @@ def rht_quantize(x, sign_mask: int, mode: int = RNE, seed: int = 0, amax_in: Opt
     lib().oracle_rht_quantize(_p(xb), tokens, cols, cols, sign_mask, mode, seed, _p(ain),
                               _p(codes), _p(sf), _p(am))
     return {"codes": codes, "sf": sf, "amax": float(am[0])}
+
+
+def group_k_offset(offsets, g: int) -> int:
+    """Column where expert g's 64-padded token segment starts (R14)."""
+    o = np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
+    return lib().oracle_group_k_offset(_p(o), g)
+
+
+def rht_quantize_grouped(x, offsets, kt: int, sign_mask: int, mode: int = RNE, seed: int = 0, amax_in=None):
+    """x: bf16 [rows, cols], expert-sorted -> transposed operand [cols, kt]
+    with every expert's segment padded to 64 tokens (R14)."""
+    xb = _bf16_bits(x)
+    rows, cols = xb.shape
+    off = np.ascontiguousarray(np.asarray(offsets, dtype=np.int64))
+    groups = off.size - 1
+    codes = np.zeros((cols, kt // 2), dtype=np.uint8)
+    sf = np.zeros(sf_bytes(cols, kt), dtype=np.uint8)
+    am = np.zeros(groups, dtype=np.float32)
+    ain = None if amax_in is None else np.ascontiguousarray(np.asarray(amax_in, dtype=np.float32))
+    lib().oracle_rht_quantize_grouped(_p(xb), rows, cols, cols, _p(off), groups, kt, sign_mask, mode, seed,
+                                      _p(ain), _p(codes), _p(sf), _p(am))
+    return {"codes": codes, "sf": sf, "amax": am}
 
 
 def dequantize_rows(codes: np.ndarray, sf: np.ndarray, cols: int, amax: float,

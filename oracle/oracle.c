@@ -497,6 +497,75 @@ void oracle_rht_quantize(const uint16_t *x, int64_t tokens, int64_t cols, int64_
     *amax_out = amax;
 }
 
+/* Expert-segmented RHT quantisation for the wgrad of the LatentMoE
+ * expert GEMMs ([SL-2.2] routed-expert GEMMs in NVFP4 in every pass; [U-2.2]
+ * RHT on the wgrad inputs).  Reading R14: the pages do not say how an
+ * expert's token segment meets the 16-token transform; here each expert's
+ * segment of cnt_g tokens (rows offsets[g] .. offsets[g+1] of the
+ * expert-sorted x [rows, cols]) is padded with zero tokens to
+ * kp_g = ceil(cnt_g / 64) * 64 and placed at columns ko_g = sum_{i<g} kp_i
+ * of the transposed operand [cols, kt] (kt >= ko_G; columns from ko_G on
+ * are left as they are).  Padding to 64 rather than 16 puts every expert on
+ * a boundary of the 128x4 scale atoms (64 tokens per atom column), so the
+ * grouped wgrad GEMM can take one expert's K range as a plain K slice.
+ * Each padded segment is transformed in 16-token chunks (R5) and quantised
+ * in 1x16 blocks along tokens with its own tensor amax (the largest
+ * magnitude of the segment's transformed values) or amax_in[g]; SR index
+ * e = c * kt + ko_g + t. */
+int64_t oracle_group_k_offset(const int64_t *offsets, int32_t g)
+{
+    int64_t k = 0;
+    int32_t i;
+    for (i = 0; i < g; ++i) k += (offsets[i + 1] - offsets[i] + 63) / 64 * 64;
+    return k;
+}
+
+void oracle_rht_quantize_grouped(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld,
+                                 const int64_t *offsets, int32_t groups, int64_t kt,
+                                 uint16_t sign_mask, int mode, uint64_t seed,
+                                 const float *amax_in, uint8_t *codes_t, uint8_t *sf_t,
+                                 float *amax_out)
+{
+    int32_t g;
+    (void)rows;
+    for (g = 0; g < groups; ++g) {
+        const int64_t o0 = offsets[g], cnt = offsets[g + 1] - offsets[g];
+        const int64_t kp = (cnt + 63) / 64 * 64, ko = oracle_group_k_offset(offsets, g);
+        float amax = 0.0f, s_enc;
+        int64_t c, t;
+        /* the segment's transformed values, chunk by chunk; zero tokens past cnt */
+        if (amax_in) {
+            amax = amax_in[g];
+        } else {
+            for (c = 0; c < cols; ++c)
+                for (t = 0; t < kp; t += 16) {
+                    float in[16], y[16];
+                    int i;
+                    for (i = 0; i < 16; ++i)
+                        in[i] = (t + i < cnt) ? bf16_to_float(x[(o0 + t + i) * ld + c]) : 0.0f;
+                    oracle_rht16(in, sign_mask, y);
+                    for (i = 0; i < 16; ++i) if (fabsf(y[i]) > amax) amax = fabsf(y[i]);
+                }
+        }
+        amax_out[g] = amax;
+        s_enc = oracle_tensor_scale(amax);
+        for (c = 0; c < cols; ++c)
+            for (t = 0; t < kp; t += 16) {
+                float in[16], y[16], bamax = 0.0f;
+                uint8_t sc, cd[16];
+                int i;
+                for (i = 0; i < 16; ++i)
+                    in[i] = (t + i < cnt) ? bf16_to_float(x[(o0 + t + i) * ld + c]) : 0.0f;
+                oracle_rht16(in, sign_mask, y);
+                for (i = 0; i < 16; ++i) if (fabsf(y[i]) > bamax) bamax = fabsf(y[i]);
+                sc = oracle_block_scale(bamax, s_enc);
+                sf_t[oracle_sf_offset(c, (ko + t) / 16, kt)] = sc;
+                encode_block(y, 16, s_enc, sc, mode, seed, (uint64_t)(c * kt + ko + t), 1, cd);
+                for (i = 0; i < 16; ++i) put_code(codes_t, c, ko + t + i, kt, cd[i]);
+            }
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* Dequantisation and the GEMM definition [S-infra].                    */
 /* ------------------------------------------------------------------ */

@@ -335,6 +335,58 @@ def test_rht_quantize_equals_quantize_of_exact_transform(orc, mode):
     assert (q["codes"] == ref["codes"]).all() and (q["sf"] == ref["sf"]).all()
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rht_quantize_grouped_is_per_expert_padded_rht(orc, mode):
+    """Expert-segmented RHT quantisation (reading R14): expert g's tokens,
+    padded with zero tokens to a multiple of 64, sit at columns ko_g (the sum
+    of the earlier padded counts) of the transposed operand.  Checked against
+    the plain RHT quantiser run on each zero-padded segment on its own (RNE:
+    same bytes; SR: the same words once the index space is shifted by the
+    segment's column, via single blocks), and one expert of a multiple of 64
+    tokens spanning the operand is exactly the plain RHT quantiser."""
+    rng = np.random.default_rng(30 + mode)
+    cols, mask, seed = 24, 0x5A3C, 91
+    offsets = np.array([0, 30, 30, 100, 164, 165], dtype=np.int64)      # 30, 0, 70, 64, 1 tokens
+    counts = np.diff(offsets)
+    kp = (counts + 63) // 64 * 64
+    ko = np.concatenate([[0], np.cumsum(kp)])
+    kt = int(ko[-1]) + 64                                                 # capacity past the last expert
+    x = _bf16(rng.standard_normal((int(offsets[-1]), cols)) * np.repeat([1, 1, 5, 0.02, 3], counts)[:, None])
+    q = orc.rht_quantize_grouped(x, offsets, kt, mask, mode=mode, seed=seed)
+    for g in range(len(counts)):
+        assert orc.group_k_offset(offsets, g) == ko[g]
+        if counts[g] == 0:
+            assert q["amax"][g] == 0
+            continue
+        xp = torch.zeros(int(kp[g]), cols, dtype=torch.bfloat16)
+        xp[:counts[g]] = x[offsets[g]:offsets[g + 1]]
+        ref = orc.rht_quantize(xp, mask, mode=orc.RNE)
+        assert q["amax"][g] == ref["amax"]
+        if mode == 0:
+            assert (q["codes"][:, ko[g] // 2:(ko[g] + kp[g]) // 2] == ref["codes"]).all()
+            for c in range(cols):
+                for b in range(int(kp[g]) // 16):
+                    assert q["sf"][orc.sf_offset(c, ko[g] // 16 + b, kt)] == ref["sf"][orc.sf_offset(c, b, kp[g])]
+        else:
+            # every SR block: the padded segment's transform, encoded with words c*kt + ko_g + t
+            s_enc = orc.tensor_scale(q["amax"][g])
+            xf = xp.float().numpy()
+            codes = _unpack(q["codes"], kt)
+            for c in range(0, cols, 7):
+                for t in range(0, int(kp[g]), 16):
+                    y = orc.rht16(xf[t:t + 16, c], mask)
+                    sf_b, cd = orc.encode_block(y, s_enc, orc.SR, seed, c * kt + int(ko[g]) + t)
+                    assert q["sf"][orc.sf_offset(c, (int(ko[g]) + t) // 16, kt)] == sf_b
+                    assert (codes[c, int(ko[g]) + t:int(ko[g]) + t + 16] == cd).all()
+    # nothing is written past the last expert
+    assert (q["codes"][:, ko[-1] // 2:] == 0).all()
+    # one expert of 128 tokens spanning the operand: the plain RHT quantiser
+    one = orc.rht_quantize_grouped(x[:128], np.array([0, 128]), 128, mask, mode=mode, seed=seed)
+    ref = orc.rht_quantize(x[:128], mask, mode=mode, seed=seed)
+    assert one["amax"][0] == ref["amax"]
+    assert (one["codes"] == ref["codes"]).all() and (one["sf"] == ref["sf"]).all()
+
+
 def test_grouped_quantize_equals_per_group(orc):
     rng = np.random.default_rng(12)
     cols = 32
