@@ -401,6 +401,8 @@ def main():
                   "unit": "GB/s", "frac": round(wk.ops[3][2] / (q_dy * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                   "traffic": None}
 
+    supplied = measure_supplied_amax(wk, pk["hbm_gbs"])
+
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
         e2e = measure_e2e(wk, args.e2e_steps, dev)
@@ -421,6 +423,7 @@ def main():
         "quantize_gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1),
         "quantize_frac_hbm": round(quant_bytes / (quant_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
         "ops": ops, "roofline": roofline, "roofline_quantize": roofline_q,
+        "quantize_supplied_amax": supplied,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk,
         "device_status": status, "routing": {"max_vio": round(wk.routing.max_vio, 3),
                                              "empty_experts": int((wk.routing.counts == 0).sum())},
@@ -442,6 +445,49 @@ def host_mem_available() -> int:
     except OSError:
         pass
     return 0
+
+
+def measure_supplied_amax(wk: Workload, hbm_gbs: float, iters: int = 5):
+    """Each quantiser of the step with its amax supplied (the step's own
+    amaxes, already in the output tensors), timed alone after the timed
+    region: one HBM read of the input, so the algorithmic bytes are 2.5625 per
+    element (3.125 with the transposed 2D copy).  Not part of the step."""
+    import torch
+    B = wk.B
+    d, m = wk.dense, wk.moe
+    T, K, N = d.tokens, d.hidden, d.out
+    E, L, Hh, R = m.experts, m.latent, m.expert_hidden, wk.R
+    cases = [
+        ("quantize_1d X (RNE)", 2.5625 * T * K, lambda: B.quantize_1d(wk.x, B.RNE, 0, amax_in=wk.qx.amax, out=wk.qx)),
+        ("quantize_1d dY (SR)", 2.5625 * T * N,
+         lambda: B.quantize_1d(wk.dy, B.SR, wk.seed, amax_in=wk.qdy.amax, out=wk.qdy)),
+        ("quantize_2d W (W, W^T)", 3.125 * N * K,
+         lambda: B.quantize_2d(wk.w, want_t=True, amax_in=wk.qw.amax, out=wk.qw, out_t=wk.qwt)),
+        ("quantize_2d W_up (batched, W)", 2.5625 * E * Hh * L,
+         lambda: B.quantize_2d(wk.w_up, want_t=False, amax_in=wk.qwu.amax, out=wk.qwu)),
+        ("rht_quantize dY (SR)", 2.5625 * T * N,
+         lambda: B.rht_quantize(wk.dy, wk.mask, B.SR, wk.wseed, amax_in=wk.sdy.amax, out=wk.sdy)),
+        ("rht_quantize X (RNE)", 2.5625 * T * K,
+         lambda: B.rht_quantize(wk.x, wk.mask, B.RNE, 0, amax_in=wk.sx.amax, out=wk.sx)),
+        ("quantize_1d_grouped A (RNE)", 2.5625 * R * L,
+         lambda: B.quantize_1d_grouped(wk.a, wk.offsets, B.RNE, 0, amax_in=wk.qa.amax, out=wk.qa)),
+        ("quantize_1d_grouped H (RNE)", 2.5625 * R * Hh,
+         lambda: B.quantize_1d_grouped(wk.h, wk.offsets, B.RNE, 0, amax_in=wk.qh.amax, out=wk.qh)),
+    ]
+    out = {}
+    for name, nbytes, fn in cases:
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4)}
+    return out
 
 
 def measure_e2e(wk: Workload, steps: int, dev):

@@ -239,6 +239,30 @@ nvfp4_status nvfp4_rht_quantize(const void *x, int64_t tokens, int64_t cols, int
                                 const float *amax_in, nvfp4_tensor *out_t,
                                 nvfp4_stream_t stream);
 
+/* Columns needed by nvfp4_rht_quantize_grouped for `rows` expert-sorted
+ * tokens in `groups` experts, whatever the split: ceil((rows + 63 * groups)
+ * / 64) * 64 (every expert's segment is padded to a multiple of 64). */
+int64_t nvfp4_group_k_capacity(int64_t rows, int32_t groups);
+
+/* Expert-segmented RHT + 1D quantisation: the wgrad inputs of the LatentMoE
+ * expert GEMMs (Super summary section 2.2: routed-expert GEMMs in NVFP4;
+ * Ultra report 2.2: RHT on the inputs of wgrad).  x: bf16 [rows, cols],
+ * rows sorted by expert, expert g owning rows offsets[g] .. offsets[g+1]
+ * (device, num_groups + 1 values).  Expert g's segment is padded with zero
+ * tokens to kp_g = ceil(cnt_g / 64) * 64 and written at columns ko_g =
+ * sum_{i<g} kp_i of the transposed operand out_t ([cols, kt]: codes
+ * [cols, kt/2], sf nvfp4_sf_bytes(cols, kt), amax num_groups floats); the
+ * pages do not say how a segment meets the 16-token transform, 64 puts every
+ * expert on a scale-atom boundary.  Each segment is transformed in 16-token
+ * chunks and quantised with its own amax (computed, or amax_in[g]); SR index
+ * e = c * kt + ko_g + t.  kt: a multiple of 64, at least
+ * nvfp4_group_k_capacity(rows, num_groups); columns past the last segment
+ * are not written.  Use the same sign_mask for both operands of a wgrad. */
+nvfp4_status nvfp4_rht_quantize_grouped(const void *x, int64_t rows, int64_t cols, int64_t ld,
+                                        const int64_t *offsets, int32_t num_groups, int64_t kt,
+                                        uint16_t sign_mask, nvfp4_round mode, uint64_t seed,
+                                        const float *amax_in, nvfp4_tensor *out_t, nvfp4_stream_t stream);
+
 /* ------------------------------------------------------------- GEMMs */
 
 /* C[m, n] = alpha * sum_k a_k * sa * b_k * sb with FP32 accumulation, where
@@ -275,6 +299,21 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor *a, const int64_t *offsets, i
                                 nvfp4_out_dtype c_dtype, float *c_amax, nvfp4_stream_t stream);
 
 /* ------------------------------------------------------------- status */
+
+/* GEMM whose groups split K: the wgrad of the LatentMoE expert GEMMs,
+ * dW_g = dH_g^T . A_g over expert g's tokens (Super summary section 2.2:
+ * routed-expert GEMMs in NVFP4; Ultra report 2.2: wgrad on RHT operands).
+ * a: [M, KT] and b: [N, KT], both from nvfp4_rht_quantize_grouped with the
+ * same offsets and sign mask (amax: num_groups floats each); KT % 64 == 0.
+ * offsets: device, num_groups + 1 token offsets; group g's K slice is
+ * columns ko_g .. ko_g + ceil(cnt_g / 64) * 64 (nvfp4_rht_quantize_grouped).
+ * c: [num_groups * M, N], row stride ldc; rows g*M .. g*M + M - 1 receive
+ * C_g = alpha_g * A[:, slice_g] . B[:, slice_g]^T, alpha_g =
+ * dec(a->amax[g]) * dec(b->amax[g]); an expert without tokens gets zeros.
+ * c_amax: nullable, num_groups floats, as for nvfp4_grouped_gemm. */
+nvfp4_status nvfp4_grouped_gemm_k(const nvfp4_tensor *a, const nvfp4_tensor *b, const int64_t *offsets,
+                                  int32_t num_groups, void *c, int64_t ldc, nvfp4_out_dtype c_dtype,
+                                  float *c_amax, nvfp4_stream_t stream);
 
 const char *nvfp4_status_string(nvfp4_status status);
 

@@ -32,7 +32,8 @@ EXPORTS = ["nvfp4_sf_bytes", "nvfp4_sf_bytes_grouped", "nvfp4_sf_offset", "nvfp4
            "nvfp4_quantize_1d", "nvfp4_quantize_1d_grouped", "nvfp4_quantize_2d",
            "nvfp4_quantize_2d_fused_workspace", "nvfp4_quantize_2d_fused", "nvfp4_quantize_2d_fused_static",
            "nvfp4_rht_amax",
-           "nvfp4_rht_quantize", "nvfp4_gemm", "nvfp4_grouped_gemm", "nvfp4_status_string",
+           "nvfp4_rht_quantize", "nvfp4_group_k_capacity", "nvfp4_rht_quantize_grouped", "nvfp4_gemm",
+           "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_k", "nvfp4_status_string",
            "nvfp4_last_error", "nvfp4_device_status", "nvfp4_launch_count", "nvfp4_debug_inject",
            "nvfp4_debug_wait_timeout"]
 
@@ -78,6 +79,10 @@ def lib():
             "nvfp4_rht_quantize": (st, [P, i64, i64, i64, ctypes.c_uint16, ctypes.c_int, u64, P, TP, P]),
             "nvfp4_gemm": (st, [TP, TP, P, i64, ctypes.c_int, P, P]),
             "nvfp4_grouped_gemm": (st, [TP, P, i32, TP, i64, P, i64, ctypes.c_int, P, P]),
+            "nvfp4_group_k_capacity": (i64, [i64, i32]),
+            "nvfp4_rht_quantize_grouped": (st, [P, i64, i64, i64, P, i32, i64, ctypes.c_uint16, ctypes.c_int,
+                                                ctypes.c_uint64, P, TP, P]),
+            "nvfp4_grouped_gemm_k": (st, [TP, TP, P, i32, P, i64, ctypes.c_int, P, P]),
             "nvfp4_status_string": (ctypes.c_char_p, [st]),
             "nvfp4_last_error": (ctypes.c_char_p, []),
             "nvfp4_device_status": (st, [ctypes.POINTER(ctypes.c_int32)]),
@@ -266,6 +271,43 @@ def rht_quantize(x: torch.Tensor, sign_mask: int, mode: int = RNE, seed: int = 0
     co = out.c()
     _check(lib().nvfp4_rht_quantize(_ptr(x), tokens, cols, ld, sign_mask, mode, seed, _ptr(amax_in),
                                     ctypes.byref(co), _stream(stream)))
+    return out
+
+
+def group_k_capacity(rows: int, groups: int) -> int:
+    """Columns of an expert-segmented RHT operand for any split of `rows` tokens."""
+    return lib().nvfp4_group_k_capacity(rows, groups)
+
+
+def rht_quantize_grouped(x: torch.Tensor, offsets: torch.Tensor, sign_mask: int, mode: int = RNE, seed: int = 0,
+                         kt: Optional[int] = None, amax_in: Optional[torch.Tensor] = None,
+                         out: Optional[QTensor] = None, stream=None) -> QTensor:
+    """x: bf16 [rows, cols], expert-sorted -> transposed operand [cols, kt] with every
+    expert's tokens zero-padded to a multiple of 64 (amax per expert)."""
+    rows, cols, ld = _rows2d(x)
+    assert offsets.dtype == torch.int64 and offsets.is_cuda
+    groups = offsets.numel() - 1
+    if kt is None:
+        kt = group_k_capacity(rows, groups) if out is None else out.cols
+    out = empty_qtensor(cols, kt, x.device, n_amax=groups) if out is None else out
+    co = out.c()
+    _check(lib().nvfp4_rht_quantize_grouped(_ptr(x), rows, cols, ld, _ptr(offsets), groups, kt, sign_mask, mode,
+                                            seed, _ptr(amax_in), ctypes.byref(co), _stream(stream)))
+    return out
+
+
+def grouped_gemm_k(a: QTensor, b: QTensor, offsets: torch.Tensor, out_dtype: int = OUT_FP32,
+                   out: Optional[torch.Tensor] = None, stream=None,
+                   c_amax: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Groups along K (expert wgrad): C[g*M:(g+1)*M] = alpha_g * A[:, slice_g] . B[:, slice_g]^T
+    for a [M, KT], b [N, KT] from rht_quantize_grouped with the same offsets."""
+    groups = offsets.numel() - 1
+    if out is None:
+        out = torch.empty(groups * a.rows, b.rows, dtype=torch.float32 if out_dtype == OUT_FP32 else torch.bfloat16,
+                          device=a.codes.device)
+    ca, cb = a.c(), b.c()
+    _check(lib().nvfp4_grouped_gemm_k(ctypes.byref(ca), ctypes.byref(cb), _ptr(offsets), groups, _ptr(out),
+                                      out.stride(0), out_dtype, _ptr(c_amax), _stream(stream)))
     return out
 
 

@@ -6,7 +6,8 @@ Usage:
 <op> is one of: amax, quant1d_rne, quant1d_sr, quant2d, quant2d_moe, quant2d_moe_fused, rht_sr,
 quant1d_grouped_a (per-expert amax + RNE of the routed activations), quant1d_grouped_h (RNE of
 the expert hidden activations with their amax supplied), gemm_fprop, gemm_dgrad, gemm_wgrad,
-grouped_up, grouped_down.  The inputs of the op are generated on the device and
+grouped_up, grouped_down, grouped_dgrad (dA = dH . W_up per expert, W_up^T from the 2D quantiser),
+grouped_wgrad (dW_up = RHT(dH)^T . RHT(A) per expert, groups along K, FP32 out).  The inputs of the op are generated on the device and
 its operands quantised once; the op itself is then launched `iters` times back to back, so
 a profiler can skip the set-up launches and capture the op alone (for example with
 `ncu -k regex:<kernel> -s 1 -c 1`).  It prints the mean CUDA-event time per launch.
@@ -23,7 +24,7 @@ from . import workloads as wl
 
 OPS = ["amax", "quant1d_rne", "quant1d_sr", "quant2d", "quant2d_moe", "quant2d_moe_fused", "rht_sr",
        "quant1d_grouped_a", "quant1d_grouped_h", "gemm_fprop", "gemm_dgrad", "gemm_wgrad", "grouped_up",
-       "grouped_down"]
+       "grouped_down", "grouped_dgrad", "grouped_wgrad"]
 
 
 def prepare(op: str, which: str, dev):
@@ -81,6 +82,21 @@ def prepare(op: str, which: str, dev):
         qb = B.rht_quantize(x, mask, B.RNE)
         out = torch.empty(N, K, dtype=torch.float32, device=dev)
         return lambda: B.gemm(qa, qb, B.OUT_FP32, out=out)
+    if op in ("grouped_dgrad", "grouped_wgrad"):
+        mi = wl.moe_inputs(m, which, device=dev, want=("a", "w_up") if op == "grouped_dgrad" else ("a",))
+        off = mi["routing"].offsets.to(dev)
+        R = int(mi["routing"].offsets[-1])
+        dh = wl.normal_bf16((R, m.expert_hidden), 1e-3, 98, dev)
+        if op == "grouped_dgrad":
+            qdh = B.quantize_1d_grouped(dh, off, B.SR, seed)
+            qwt = B.quantize_2d(mi["w_up"], want_t=True)[1]          # [E, latent, hidden]
+            out = torch.empty(R, m.latent, dtype=torch.bfloat16, device=dev)
+            return lambda: B.grouped_gemm(qdh, off, qwt, m.latent, B.OUT_BF16, out=out)
+        kt = B.group_k_capacity(R, m.experts)
+        sdh = B.rht_quantize_grouped(dh, off, mask, B.SR, wl.wgrad_seed(seed), kt=kt)
+        sa = B.rht_quantize_grouped(mi["a"], off, mask, B.RNE, kt=kt)
+        out = torch.empty(m.experts * m.expert_hidden, m.latent, dtype=torch.float32, device=dev)
+        return lambda: B.grouped_gemm_k(sdh, sa, off, B.OUT_FP32, out=out)
     if op.startswith("grouped_"):
         up = op == "grouped_up"
         mi = wl.moe_inputs(m, which, device=dev, want=("a", "w_up") if up else ("a", "w_down"))

@@ -122,6 +122,8 @@ struct GemmParams {
     int64_t ldc;
     float* c_amax;              // nullable: max |C| over the written outputs, per group (zeroed by the host)
     bool vec_store;             // rows of C start 16-byte aligned: vector stores
+    bool kgroup;                // groups split K (expert wgrad): group g owns the 64-padded token
+                                // segment of offsets[g] .. offsets[g+1] and C rows g*M .. g*M+M-1
 };
 
 // ------------------------------------------------------------------ PTX
@@ -459,6 +461,9 @@ struct TileCoord {
     int nt;           // n-tile
     int32_t row0;     // first A row of the tile
     int32_t rows;     // valid rows (<= 128)
+    int32_t k0 = 0;   // first K element of the tile (groups along K)
+    int32_t ka = -1;  // 64-wide K atoms of the tile; -1: all of K
+    int64_t crow0 = -1;  // first C row; -1: row0
 };
 
 // Tiles are numbered in bands of G_BAND m-tiles: inside a band, the m-tile
@@ -517,6 +522,30 @@ __device__ __forceinline__ TileCoord decode_pair_tile(int64_t t, int ptiles, int
     return c;
 }
 
+// Tiles of a GEMM whose groups split K: for every group, the m-tiles (or
+// row pairs) of the shared M rows x the n-tiles, the m-tile fastest.  Group
+// g's K slice starts at kpad[g] and spans (kpad[g+1] - kpad[g]) / 64 atoms
+// (possibly none: C_g is then zero); its C rows start at g * M.
+__device__ __forceinline__ TileCoord decode_kgroup_tile(int64_t t, int mt, int ntiles, const int32_t* kpad,
+                                                        int64_t M, int64_t K, bool pair, uint32_t rank) {
+    const int64_t per_g = (int64_t)mt * ntiles;
+    TileCoord c;
+    c.g = (int)(t / per_g);
+    const int64_t local = t - (int64_t)c.g * per_g;
+    const int m = (int)(local % mt);
+    c.nt = (int)(local / mt);
+    const int lm = pair ? 2 * m + (int)rank : m;
+    c.row0 = lm * 128;
+    c.rows = (int32_t)max((int64_t)0, min((int64_t)128, M - (int64_t)c.row0));
+    c.mtg = c.rows > 0 ? lm : lm - 1;                  // a pair's ghost m-tile borrows its partner's scales
+    // K slices never reach past K (offsets are device data)
+    const int32_t k1 = (int32_t)min((int64_t)kpad[c.g + 1], K);
+    c.k0 = (int32_t)min((int64_t)kpad[c.g], K);
+    c.ka = max(0, k1 - c.k0) / 64;
+    c.crow0 = (int64_t)c.g * M + c.row0;
+    return c;
+}
+
 __device__ __forceinline__ uint4 ldg_u4(const uint8_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
 // ------------------------------------------------------------------ kernel
@@ -542,7 +571,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int32_t* tab = reinterpret_cast<int32_t*>(smem + L::TAB_OFF);
     const int groups = p.groups;
-    GroupTables gt{tab, tab + groups + 1, PAIR ? tab + 2 * (groups + 1) : nullptr};
+    // groups along K: pad[] holds the 64-padded token segments (no pair table)
+    GroupTables gt{tab, tab + groups + 1, (PAIR && !p.kgroup) ? tab + 2 * (groups + 1) : nullptr};
     // CTA pairs: rank 0 issues the MMAs of both; barriers that collect both
     // CTAs' arrivals (full, sf_full, acc_empty) are rank 0's.
     const uint32_t rank = PAIR ? cluster_rank() : 0u;
@@ -584,7 +614,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         }
     }
-    if (p.offsets != nullptr) {
+    if (p.kgroup) {
+        build_group_tables(p.offsets, groups, p.K, gt, 6);
+    } else if (p.offsets != nullptr) {
         build_group_tables(p.offsets, groups, p.M, gt);
     } else if (threadIdx.x == 0) {
         gt.off[0] = 0;
@@ -599,21 +631,26 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int mtiles = gt.pad[groups] >> 7;
-    const int ptiles = PAIR ? (gt.pair[groups] >> 8) : 0;
     const int ntiles = (int)((p.N + G_BN - 1) / G_BN);
-    const int64_t total = (int64_t)(PAIR ? ptiles : mtiles) * ntiles;
+    // groups along M: tiles from the padded row tables; groups along K: every
+    // group has all m-tiles (or row pairs) of the shared M rows
+    const int kg_mt = (int)(PAIR ? (p.M + 255) / 256 : (p.M + 127) / 128);
+    const int mtiles = p.kgroup ? 0 : gt.pad[groups] >> 7;
+    const int ptiles = (PAIR && !p.kgroup) ? (gt.pair[groups] >> 8) : 0;
+    const int64_t total = p.kgroup ? (int64_t)groups * kg_mt * ntiles : (int64_t)(PAIR ? ptiles : mtiles) * ntiles;
     // a pair walks the tiles of its cluster (blockIdx.x / 2), both CTAs alike
     const int64_t t_first = PAIR ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
     const int64_t t_step = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
     auto tile_at = [&](int64_t t) {
+        if (p.kgroup) return decode_kgroup_tile(t, kg_mt, ntiles, gt.pad, p.M, p.K, PAIR, rank);
         return PAIR ? decode_pair_tile(t, ptiles, ntiles, gt.off, gt.pad, gt.pair, groups, rank)
                     : decode_tile(t, mtiles, ntiles, gt.off, gt.pad, groups);
     };
-    const int kstages = (int)((p.K + G_BK - 1) / G_BK);
-    const int katoms = (int)((p.K + 63) / 64);
+    const int katoms = (int)((p.K + 63) / 64);           // atoms of a whole operand row (scale row stride)
+    // K atoms and stages of a tile
+    auto tile_atoms = [&](const TileCoord& tc) { return tc.ka >= 0 ? tc.ka : katoms; };
     const int nrb = (int)((p.N + 127) / 128);            // 128-row scale blocks of one B operand
-    const int64_t b_rows_per_group = (p.offsets != nullptr) ? p.N : 0;
+    const int64_t b_rows_per_group = (p.offsets != nullptr && !p.kgroup) ? p.N : 0;
 
     if (warp == G_W_TMA) {
         // ------------------------------------------------ TMA producer (A, B)
@@ -628,9 +665,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     (int32_t)(tc.g * b_rows_per_group + (int64_t)tc.nt * G_BN + (PAIR ? 128 * (int64_t)rank : 0));
                 const uint8_t* sfb_g = p.sfb + (int64_t)tc.g * p.sfb_group_stride;
                 const bool rb2 = (tc.nt * 2 + 1) < nrb;
-                for (int ks = 0; ks < kstages; ++ks) {
+                const int ka = tile_atoms(tc), kst = (ka + 3) / 4, kc0 = tc.k0 / 64;
+                for (int ks = 0; ks < kst; ++ks) {
                     if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) { ok = false; break; }
-                    const int na = min(4, katoms - 4 * ks);
+                    const int na = min(4, ka - 4 * ks);
                     const uint32_t sfbytes = (uint32_t)na * 512u;
                     const uint32_t st = smem_u32(stages + s * STAGE_BYTES);
                     // the scales first, on their own barrier: they are small, land
@@ -639,22 +677,24 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     const uint32_t sbar = sfl0 + 8 * s;
                     mbar_expect_tx(sbar, sfbytes * (rb2 ? 3u : 2u));
                     const uint32_t ssf = st + G_A_BYTES + L::B_BYTES;
-                    bulk_load(ssf, p.sfa + ((int64_t)tc.mtg * katoms + 4 * ks) * 512, sfbytes, sbar);
-                    bulk_load(ssf + G_SFA_BYTES, sfb_g + ((int64_t)(tc.nt * 2) * katoms + 4 * ks) * 512, sfbytes, sbar);
+                    bulk_load(ssf, p.sfa + ((int64_t)tc.mtg * katoms + kc0 + 4 * ks) * 512, sfbytes, sbar);
+                    bulk_load(ssf + G_SFA_BYTES, sfb_g + ((int64_t)(tc.nt * 2) * katoms + kc0 + 4 * ks) * 512, sfbytes,
+                              sbar);
                     if (rb2)
-                        bulk_load(ssf + G_SFA_BYTES + 2048, sfb_g + ((int64_t)(tc.nt * 2 + 1) * katoms + 4 * ks) * 512,
-                                  sfbytes, sbar);
+                        bulk_load(ssf + G_SFA_BYTES + 2048,
+                                  sfb_g + ((int64_t)(tc.nt * 2 + 1) * katoms + kc0 + 4 * ks) * 512, sfbytes, sbar);
+                    const int32_t kx = tc.k0 / 2 + ks * 128;     // byte column of the K stage
                     if (PAIR) {
                         // A and B of both CTAs complete on rank 0's full barrier
                         const uint32_t bar = mapa_shared(full0 + 8 * s, 0);
                         mbar_expect_tx_cluster(bar, G_A_BYTES + L::B_BYTES);
-                        tma_load_2d_pair(st, &tm_a, ks * 128, tc.row0, bar);
-                        tma_load_2d_pair(st + G_A_BYTES, &tm_b, ks * 128, brow0, bar);
+                        tma_load_2d_pair(st, &tm_a, kx, tc.row0, bar);
+                        tma_load_2d_pair(st + G_A_BYTES, &tm_b, kx, brow0, bar);
                     } else {
                         const uint32_t bar = full0 + 8 * s;
                         mbar_expect_tx(bar, G_A_BYTES + G_B_BYTES);
-                        tma_load_2d(st, &tm_a, ks * 128, tc.row0, bar);
-                        tma_load_2d(st + G_A_BYTES, &tm_b, ks * 128, brow0, bar);
+                        tma_load_2d(st, &tm_a, kx, tc.row0, bar);
+                        tma_load_2d(st + G_A_BYTES, &tm_b, kx, brow0, bar);
                     }
                     issued |= 1u << s;
                     issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
@@ -687,13 +727,16 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             for (int64_t t = t_first; t < total && ok; t += t_step, ++it) {
                 if (!mbar_wait(acc_empty, (it & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                for (int ks = 0; ks < kstages; ++ks) {
+                // a tile with no K (an expert without tokens) issues nothing: its
+                // epilogue writes zeros
+                const int ka = tile_atoms(tile_at(t)), kst = (ka + 3) / 4;
+                for (int ks = 0; ks < kst; ++ks) {
                     if (!mbar_wait(full0 + 8 * s, ph, abort_flag) || !mbar_wait(sff0 + 8 * s, ph, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const int na = min(4, katoms - 4 * ks);
+                    const int na = min(4, ka - 4 * ks);
                     const uint32_t st = smem_u32(stages + s * STAGE_BYTES);
                     const uint32_t sfa_t = tmem + G_SF_COL0 + s * G_SF_COLS_PER_STAGE;
                     const uint32_t sfb_t = sfa_t + 16;
@@ -737,8 +780,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         for (int64_t t = t_first; t < total && ok; t += t_step) {
             const TileCoord tc = tile_at(t);
             const bool rb2 = (tc.nt * 2 + 1) < nrb;
-            for (int ks = 0; ks < kstages; ++ks) {
-                const int na = min(4, katoms - 4 * ks);
+            const int ka = tile_atoms(tc), kst = (ka + 3) / 4;
+            for (int ks = 0; ks < kst; ++ks) {
+                const int na = min(4, ka - 4 * ks);
                 if (!mbar_wait(sfl0 + 8 * s, ph, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint8_t* ssf = stages + s * STAGE_BYTES + G_A_BYTES + L::B_BYTES + lane * 16;
@@ -787,7 +831,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             if (!mbar_wait(acc_full, it & 1u, abort_flag)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(chunk * 64);
-            const int64_t row = tc.row0 + r;
+            // groups along K: C rows of group g start at g * M; a group without
+            // K (an expert without tokens) stores zeros (vmask clears the
+            // accumulator words, which no MMA wrote)
+            const int64_t crow0 = tc.crow0 >= 0 ? tc.crow0 : (int64_t)tc.row0;
+            const uint32_t vmask = tile_atoms(tc) == 0 ? 0u : 0xFFFFFFFFu;
+            const int64_t row = crow0 + r;
             const int64_t col0 = (int64_t)tc.nt * G_BN + chunk * 64;
             if (OUT_FP32) {
                 // two 32-column halves: load, scale, store; release after the second load
@@ -810,15 +859,15 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                         float m = 0.0f;
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            m = fmaxf(m, i < valid ? fabsf(__uint_as_float(v[i])) : 0.0f);
+                            m = fmaxf(m, i < valid ? fabsf(__uint_as_float(v[i] & vmask)) : 0.0f);
                         amax_run = max(amax_run, __float_as_uint(__fmul_rn(alpha, m)));
                     }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[i])));
+                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(v[i] & vmask)));
                     if (p.vec_store) {
-                        // rows of this warp: tc.row0 + 32q .. ; 32 columns = 128 bytes per row
+                        // rows of this warp: crow0 + 32q .. ; 32 columns = 128 bytes per row
                         rows_to_segments(v);
-                        store_segments(v, reinterpret_cast<uint8_t*>(reinterpret_cast<float*>(p.c) + (tc.row0 + q * 32) * p.ldc + cstart),
+                        store_segments(v, reinterpret_cast<uint8_t*>(reinterpret_cast<float*>(p.c) + (crow0 + q * 32) * p.ldc + cstart),
                                        p.ldc * 4, tc.rows - q * 32, (int)(p.N - cstart >= 32 ? 128 : (p.N - cstart) * 4));
                     } else if (live) {
                         float* out = reinterpret_cast<float*>(p.c) + row * p.ldc + cstart;
@@ -849,8 +898,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                         }
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(v[2 * j])),
-                                                                            __fmul_rn(alpha, __uint_as_float(v[2 * j + 1])));
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(v[2 * j] & vmask)),
+                                                                            __fmul_rn(alpha, __uint_as_float(v[2 * j + 1] & vmask)));
                             w[8 * k + j] = *reinterpret_cast<const uint32_t*>(&b2);
                         }
                     }
@@ -875,7 +924,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            tma_store_2d(&tm_c, stage_buf, (int32_t)cstart, (int32_t)(tc.row0 + q * 32));
+                            tma_store_2d(&tm_c, stage_buf, (int32_t)cstart, (int32_t)(crow0 + q * 32));
                             bulk_commit();
                         }
                     } else if (r < tc.rows) {
@@ -908,8 +957,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(v[2 * j])),
-                                                                        __fmul_rn(alpha, __uint_as_float(v[2 * j + 1])));
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(v[2 * j] & vmask)),
+                                                                        __fmul_rn(alpha, __uint_as_float(v[2 * j + 1] & vmask)));
                         w[8 * h + j] = *reinterpret_cast<const uint32_t*>(&b2);
                     }
                 }
@@ -920,7 +969,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 }
                 if (p.vec_store) {
                     rows_to_segments(w);
-                    store_segments(w, reinterpret_cast<uint8_t*>(reinterpret_cast<uint16_t*>(p.c) + (tc.row0 + q * 32) * p.ldc + col0),
+                    store_segments(w, reinterpret_cast<uint8_t*>(reinterpret_cast<uint16_t*>(p.c) + (crow0 + q * 32) * p.ldc + col0),
                                    p.ldc * 2, tc.rows - q * 32, (int)(p.N - col0 >= 64 ? 128 : (p.N - col0) * 2));
                 } else if (r < tc.rows) {
                     uint16_t* out = reinterpret_cast<uint16_t*>(p.c) + row * p.ldc + col0;

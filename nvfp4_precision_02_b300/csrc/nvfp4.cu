@@ -487,6 +487,62 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t tokens, int64_t cols, int
     return NVFP4_OK;
 }
 
+int64_t nvfp4_group_k_capacity(int64_t rows, int32_t groups) {
+    if (rows < 0 || groups < 1) return 0;
+    return cdiv(rows + 63 * (int64_t)groups, 64) * 64;
+}
+
+nvfp4_status nvfp4_rht_quantize_grouped(const void* x, int64_t rows, int64_t cols, int64_t ld, const int64_t* offsets,
+                                        int32_t num_groups, int64_t kt, uint16_t sign_mask, nvfp4_round mode,
+                                        uint64_t seed, const float* amax_in, nvfp4_tensor* out_t,
+                                        nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    NVFP4_TRY(check_input(x, rows, cols, ld, 1, "x", false));
+    if (offsets == nullptr) return fail(NVFP4_ERR_NULL, "offsets is NULL");
+    if (num_groups < 1 || num_groups > NVFP4_MAX_GROUPS)
+        return fail(NVFP4_ERR_LIMIT, "num_groups must be in [1, %d]", NVFP4_MAX_GROUPS);
+    if (kt % 64 != 0 || kt < nvfp4_group_k_capacity(rows, num_groups))
+        return fail(NVFP4_ERR_SHAPE, "kt=%lld must be a multiple of 64 and at least nvfp4_group_k_capacity = %lld",
+                    (long long)kt, (long long)nvfp4_group_k_capacity(rows, num_groups));
+    if (kt / 64 > 65535 || rows >= (int64_t(1) << 31)) return fail(NVFP4_ERR_LIMIT, "too many tokens");
+    NVFP4_TRY(check_out(out_t, cols, kt, true, "out_t"));
+    if (mode != NVFP4_ROUND_RNE && mode != NVFP4_ROUND_SR) return fail(NVFP4_ERR_SHAPE, "bad rounding mode");
+    NVFP4_TRY(check_device());
+    const int tab = 2 * 4 * (num_groups + 1);
+    const float* am = amax_in;
+    float* copy = nullptr;
+    const dim3 grid((unsigned)cdiv(cols, 256), (unsigned)(kt / 64));
+    if (am == nullptr) {
+        NVFP4_TRY(cuda_call(cudaMemsetAsync(out_t->amax, 0, sizeof(float) * num_groups, stream), "memset amax"));
+        if (rows > 0 && cols > 0) {
+            k_rht<0, true><<<grid, 256, tab, stream>>>((const uint16_t*)x, rows, cols, ld, sign_mask, out_t->amax, 0,
+                                                      nullptr, nullptr, nullptr, offsets, num_groups, kt);
+            NVFP4_TRY(launched("k_rht amax grouped"));
+        }
+        am = out_t->amax;
+    } else if (amax_in != out_t->amax) {
+        copy = out_t->amax;
+    }
+    if (rows == 0 || cols == 0) {
+        if (copy)
+            NVFP4_TRY(cuda_call(cudaMemcpyAsync(copy, amax_in, 4 * num_groups, cudaMemcpyDeviceToDevice, stream),
+                                "amax copy"));
+        return NVFP4_OK;
+    }
+    if (mode == NVFP4_ROUND_SR)
+        k_rht<2, true><<<grid, 256, tab, stream>>>((const uint16_t*)x, rows, cols, ld, sign_mask, const_cast<float*>(am),
+                                                  seed, (uint8_t*)out_t->codes, out_t->sf, copy, offsets, num_groups, kt);
+    else
+        k_rht<1, true><<<grid, 256, tab, stream>>>((const uint16_t*)x, rows, cols, ld, sign_mask, const_cast<float*>(am),
+                                                  seed, (uint8_t*)out_t->codes, out_t->sf, copy, offsets, num_groups, kt);
+    NVFP4_TRY(launched("k_rht quantize grouped"));
+    if (cols % 128 != 0) {
+        k_zero_pad_rows<<<64, 256, 0, stream>>>(out_t->sf, cols, kt, nullptr, 0);
+        NVFP4_TRY(launched("k_zero_pad_rows"));
+    }
+    return NVFP4_OK;
+}
+
 static nvfp4_status check_operand(const nvfp4_tensor* t, const char* name) {
     if (t == nullptr) return fail(NVFP4_ERR_NULL, "%s is NULL", name);
     if (t->rows < 0 || t->cols < 0) return fail(NVFP4_ERR_SHAPE, "%s: negative size", name);
@@ -710,6 +766,54 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, i
     if (c_dtype == NVFP4_OUT_BF16 && K < G_TMA_STORE_MAX_K) NVFP4_TRY(make_store_map(&mc, c, R, n, ldc, &tma_store));
     // tiles depend on the group sizes (device data): the grid is the SM count
     return launch_gemm(ma, mb, mc, p, sms, sms / 2, sms, c_dtype, tma_store, pair, stream, dev);
+}
+
+nvfp4_status nvfp4_grouped_gemm_k(const nvfp4_tensor* a, const nvfp4_tensor* b, const int64_t* offsets,
+                                  int32_t num_groups, void* c, int64_t ldc, nvfp4_out_dtype c_dtype, float* c_amax,
+                                  nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    NVFP4_TRY(check_operand(a, "a"));
+    NVFP4_TRY(check_operand(b, "b"));
+    if (offsets == nullptr) return fail(NVFP4_ERR_NULL, "offsets is NULL");
+    if (num_groups < 1 || num_groups > NVFP4_MAX_GROUPS)
+        return fail(NVFP4_ERR_LIMIT, "num_groups must be in [1, %d]", NVFP4_MAX_GROUPS);
+    const int64_t M = a->rows, N = b->rows, KT = a->cols;
+    if (b->cols != KT) return fail(NVFP4_ERR_SHAPE, "a->cols=%lld != b->cols=%lld", (long long)KT, (long long)b->cols);
+    if (KT % 64 != 0 || KT == 0) return fail(NVFP4_ERR_SHAPE, "K=%lld must be a positive multiple of 64", (long long)KT);
+    if (c_dtype != NVFP4_OUT_BF16 && c_dtype != NVFP4_OUT_FP32) return fail(NVFP4_ERR_SHAPE, "bad output dtype");
+    if (ldc < N) return fail(NVFP4_ERR_SHAPE, "ldc < N");
+    if (M * (int64_t)num_groups >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || KT >= (int64_t(1) << 31))
+        return fail(NVFP4_ERR_LIMIT, "groups * M, N or K >= 2^31");
+    if (M == 0 || N == 0) return NVFP4_OK;
+    if (c == nullptr) return fail(NVFP4_ERR_NULL, "c is NULL");
+    const int esz = c_dtype == NVFP4_OUT_FP32 ? 4 : 2;
+    if (((uintptr_t)c % esz) != 0) return fail(NVFP4_ERR_ALIGN, "c is not aligned to its element size");
+    int sms = 0, dev = 0;
+    NVFP4_TRY(check_device(&sms, &dev));
+    const bool pair = use_pair();
+    CUtensorMap ma, mb;
+    NVFP4_TRY(make_code_map(&ma, a->codes, M, KT / 2, G_BM));
+    NVFP4_TRY(make_code_map(&mb, b->codes, N, KT / 2, pair ? G_BN / 2 : G_BN));
+    GemmParams p{};
+    p.M = M; p.N = N; p.K = KT;
+    p.offsets = offsets; p.groups = num_groups; p.kgroup = true;
+    p.sfa = a->sf; p.sfb = b->sf; p.sfb_group_stride = 0;
+    p.amax_a = a->amax; p.amax_b = b->amax;
+    p.c = c; p.ldc = ldc;
+    p.c_amax = c_amax;
+    p.vec_store = aligned16(c) && (ldc * esz) % 16 == 0;
+    if (c_amax != nullptr) {
+        if (((uintptr_t)c_amax & 3u) != 0) return fail(NVFP4_ERR_ALIGN, "c_amax not 4-byte aligned");
+        NVFP4_TRY(cuda_call(cudaMemsetAsync(c_amax, 0, sizeof(float) * num_groups, stream), "memset c_amax"));
+    }
+    CUtensorMap mc;
+    bool tma_store = false;
+    std::memset(&mc, 0, sizeof(mc));
+    // the tokens of one expert are few: the short-K epilogue
+    if (c_dtype == NVFP4_OUT_BF16) NVFP4_TRY(make_store_map(&mc, c, M * num_groups, N, ldc, &tma_store));
+    const int64_t tiles = (int64_t)num_groups * cdiv(M, G_BM) * cdiv(N, G_BN);
+    const int64_t pair_tiles = (int64_t)num_groups * cdiv(M, 2 * G_BM) * cdiv(N, G_BN);
+    return launch_gemm(ma, mb, mc, p, tiles, pair_tiles, sms, c_dtype, tma_store, pair, stream, dev);
 }
 
 nvfp4_status nvfp4_device_status(int32_t* flags) {

@@ -91,8 +91,10 @@ struct GroupTables {
     int32_t* pair = nullptr;   // [G+1], optional: sum_{i<g} ceil(cnt_i/256)*256 (tiles of CTA pairs)
 };
 
+// pad_shift: pad[] pads each count to a multiple of 2^pad_shift (7: the
+// 128-row scale blocks; 6: the 64-token expert segments of the grouped wgrad).
 __device__ void build_group_tables(const int64_t* __restrict__ offsets, int32_t groups,
-                                   int64_t rows, GroupTables t) {
+                                   int64_t rows, GroupTables t, int pad_shift = 7) {
     __shared__ int32_t s_wsum[32];
     // 1) clamped offsets: o[g] = min(max(offsets[g], 0), rows); monotone fix-up
     //    is a running max, computed below together with the scan.
@@ -141,10 +143,10 @@ __device__ void build_group_tables(const int64_t* __restrict__ offsets, int32_t 
         }
     }
     __syncthreads();
-    // 2) padded rows: exclusive sums of ceil(cnt/128)*128 (scale rows) and,
+    // 2) padded rows: exclusive sums of ceil(cnt/2^pad_shift)*2^pad_shift and,
     //    when asked, of ceil(cnt/256)*256 (row tiles of CTA pairs)
     for (int which = 0; which < (t.pair != nullptr ? 2 : 1); ++which) {
-        const int sh = which == 0 ? 7 : 8;
+        const int sh = which == 0 ? pad_shift : 8;
         int32_t* dst = which == 0 ? t.pad : t.pair;
         int32_t local_sum = 0;
         for (int i = 0; i < per; ++i) {
@@ -666,20 +668,54 @@ __device__ __forceinline__ void rht16(float (&x)[16], uint32_t sign_mask) {
 // MODE 0: amax of the transform (amax must be zero on entry).
 // MODE 1/2: transform + quantise (RNE / SR) into the transposed operand
 // [cols, tokens]: codes_t [cols, tokens/2], sf_t for [cols, tokens].
-template <int MODE>
+// GROUPED: x holds expert-sorted tokens (rows of expert g: offsets[g] ..
+// offsets[g+1]); expert g's segment, padded with zero tokens to a multiple of
+// 64, occupies output columns kpad[g] .. kpad[g+1] of the [cols, kt] operand
+// (kpad = sums of the padded counts), is transformed in 16-token chunks and
+// quantised with its own amax (amax[g]).  A block covers 64 padded tokens of
+// one expert; blocks past kpad[G] do nothing.  Dynamic shared memory: two
+// tables of G+1 ints.
+template <int MODE, bool GROUPED = false>
 __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int64_t tokens,
                                              int64_t cols, int64_t ld, uint32_t sign_mask,
                                              float* __restrict__ amax, uint64_t seed,
                                              uint8_t* __restrict__ codes_t, uint8_t* __restrict__ sf_t,
-                                             float* __restrict__ amax_copy) {
+                                             float* __restrict__ amax_copy,
+                                             const int64_t* __restrict__ offsets = nullptr, int32_t groups = 1,
+                                             int64_t kt = 0) {
     __shared__ __align__(16) uint16_t tile[64][256 + 8];
     const int64_t c0 = (int64_t)blockIdx.x * 256, t0 = (int64_t)blockIdx.y * 64;
     const int tid = threadIdx.x;
-    if (MODE != 0 && amax_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
-        amax_copy[0] = amax[0];
-    const int64_t left16 = (tokens - t0) >> 4;
-    const int nchunks = left16 < 4 ? (int)left16 : 4;
-    const int ntok = 16 * nchunks;
+    int g = 0;                       // expert of this block (GROUPED)
+    int64_t src0 = t0;               // first source token of the block
+    int nvalid;                      // source tokens of the block (the rest read as zero)
+    int nchunks;                     // 16-token chunks written
+    const int64_t ocols = GROUPED ? kt : tokens;   // columns of the output operand
+    if (GROUPED) {
+        extern __shared__ int32_t s_rtab[];
+        GroupTables gt{s_rtab, s_rtab + groups + 1};          // pad = kpad: 64-token segments
+        build_group_tables(offsets, groups, tokens, gt, 6);
+        if (MODE != 0 && amax_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0)
+            for (int i = tid; i < groups; i += blockDim.x) amax_copy[i] = amax[i];
+        if (t0 >= gt.pad[groups]) return;     // block-uniform
+        int lo = 0, hi = groups;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (gt.pad[mid] <= t0) lo = mid; else hi = mid;
+        }
+        g = lo;
+        src0 = gt.off[g] + (t0 - gt.pad[g]);
+        const int64_t left = gt.off[g + 1] - src0;
+        nvalid = left < 0 ? 0 : (left > 64 ? 64 : (int)left);
+        nchunks = 4;
+    } else {
+        if (MODE != 0 && amax_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
+            amax_copy[0] = amax[0];
+        const int64_t left16 = (tokens - t0) >> 4;
+        nchunks = left16 < 4 ? (int)left16 : 4;
+        nvalid = 16 * nchunks;
+    }
+    const int ntok = nvalid;
     const bool vec = ((ld & 7) == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
     // ---- stage 64 x 256 bf16 (zeros outside the tensor)
 #pragma unroll
@@ -689,7 +725,7 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
         uint4 v = make_uint4(0, 0, 0, 0);
         const int64_t gc = c0 + cc;
         if (rr < ntok && gc < cols) {
-            const uint16_t* src = x + (t0 + rr) * ld + gc;
+            const uint16_t* src = x + (src0 + rr) * ld + gc;
             if (vec && gc + 8 <= cols) {
                 v = __ldg(reinterpret_cast<const uint4*>(src));
             } else {
@@ -717,11 +753,11 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
                 for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
             }
         }
-        block_max_atomic(__float_as_uint(m), amax);
+        block_max_atomic(__float_as_uint(m), amax + g);
         return;
     }
     if (!active) return;
-    const float s_enc = tensor_encode_scale(amax[0]);
+    const float s_enc = tensor_encode_scale(amax[g]);
     const PhiloxKeys key = philox_keys(seed);
     uint32_t packed[4][2];
     uint32_t sfw = 0;
@@ -744,7 +780,7 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
 #pragma unroll
         for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(v[i], ratio);
         if (MODE == 2) {
-            const uint64_t e0 = (uint64_t)c * (uint64_t)tokens + (uint64_t)(t0 + 16 * j);
+            const uint64_t e0 = (uint64_t)c * (uint64_t)ocols + (uint64_t)(t0 + 16 * j);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint4 wd = sr_words(key, (e0 >> 2) + q);
@@ -759,22 +795,22 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
             packed[j][1] = e2m1x8_rne(hi);
         }
     }
-    uint8_t* crow = codes_t + c * (tokens >> 1) + (t0 >> 1);
+    uint8_t* crow = codes_t + c * (ocols >> 1) + (t0 >> 1);
     const int64_t sfc = t0 >> 4;
-    // a code row is tokens/2 bytes (a multiple of 8), so 8-byte stores are aligned
+    // a code row is ocols/2 bytes (a multiple of 8), so 8-byte stores are aligned
     if (nchunks == 4) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
-        *reinterpret_cast<uint32_t*>(sf_t + sf_offset(c, sfc, tokens)) = sfw;
+        *reinterpret_cast<uint32_t*>(sf_t + sf_offset(c, sfc, ocols)) = sfw;
     } else {
         for (int j = 0; j < nchunks; ++j) {
             reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
-            sf_t[sf_offset(c, sfc + j, tokens)] = (uint8_t)(sfw >> (8 * j));
+            sf_t[sf_offset(c, sfc + j, ocols)] = (uint8_t)(sfw >> (8 * j));
         }
         for (int j = nchunks; j < 4; ++j) {
             // scale-column padding of the last atom column (tokens/16 % 4 != 0)
             const int64_t cc = sfc + j;
-            if (cc < ((((tokens >> 4) + 3) >> 2) << 2)) sf_t[sf_offset(c, cc, tokens)] = 0;
+            if (cc < ((((ocols >> 4) + 3) >> 2) << 2)) sf_t[sf_offset(c, cc, ocols)] = 0;
         }
     }
 }

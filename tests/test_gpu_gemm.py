@@ -223,3 +223,83 @@ def test_wait_timeout_is_reported_not_hung(B):
     q = B.quantize_1d(x)
     torch.cuda.synchronize()
     assert np_u8(q.amax)[0] == 1.0
+
+
+@pytest.mark.parametrize("fp32", [False, True])
+def test_grouped_dgrad_with_transposed_expert_weights(B, orc, fp32):
+    """Backward of the LatentMoE up-projection H = A . W_e^T: the input
+    gradient dA_e = dH_e . W_e runs on the grouped GEMM with the SR-quantised
+    expert-sorted dH as A and, as B, the per-expert W_e^T that the batched 2D
+    quantiser emits (16x16 tiles quantise identically in both orientations)."""
+    latent, hidden = 192, 320                 # dA is [R, latent]; the dgrad K is hidden
+    offsets = np.array([0, 3, 3, 150, 300, 301, 520], dtype=np.int64)   # an empty and 1-row experts
+    E = len(offsets) - 1
+    R = int(offsets[-1])
+    g = torch.Generator().manual_seed(21)
+    dh = (torch.randn(R, hidden, generator=g) * 1e-3).to(torch.bfloat16)
+    w = (torch.randn(E, hidden, latent, generator=g) * 0.02 * torch.linspace(0.5, 3, E)[:, None, None]).to(torch.bfloat16)
+    off = torch.from_numpy(offsets).cuda()
+    qdh = B.quantize_1d_grouped(dh.cuda(), off, mode=B.SR, seed=17)
+    _, qwt, _ = B.quantize_2d(w.cuda(), want_t=True)             # W_e^T: [E, latent, hidden]
+    out = torch.full((R, latent), -3.0, device="cuda", dtype=torch.float32 if fp32 else torch.bfloat16)
+    B.grouped_gemm(qdh, off, qwt, latent, out_dtype=B.OUT_FP32 if fp32 else B.OUT_BF16, out=out)
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy()
+    rdh = orc.quantize_1d_grouped(dh, offsets, mode=orc.SR, seed=17)
+    rw = orc.quantize_2d(w)
+    nsf = orc.sf_bytes(latent, hidden)
+    for e in range(E):
+        o0, o1 = offsets[e], offsets[e + 1]
+        if o1 == o0:
+            continue
+        A = orc.dequantize_rows(rdh["codes"], rdh["sf"], hidden, float(rdh["amax"][e]), np.arange(o0, o1),
+                                sf_row0=orc.group_sf_row(offsets, e) - int(o0))
+        Wt = orc.dequantize_rows(rw["codes_t"][e], rw["sf_t"][e * nsf:(e + 1) * nsf], hidden, float(rw["amax"][e]),
+                                 np.arange(latent))
+        ref, absum = orc.gemm(A, Wt)
+        _check(o[o0:o1], ref, absum, bf16=not fp32)
+    assert B.device_status() == 0
+
+
+@pytest.mark.parametrize("fp32", [False, True])
+def test_grouped_wgrad_groups_along_k(B, orc, fp32):
+    """wgrad of the LatentMoE up-projection: dW_g = RHT(dH_g)^T . RHT(A_g) over
+    expert g's tokens, both operands from the expert-segmented RHT quantiser
+    (SR for dH, RNE for A) and the GEMM splitting K by expert.  An expert
+    without tokens gets dW_g = 0."""
+    hidden, latent = 320, 192                 # dW_g is [hidden, latent]
+    offsets = np.array([0, 0, 1, 90, 90, 300, 301, 430], dtype=np.int64)
+    E = len(offsets) - 1
+    R = int(offsets[-1])
+    g = torch.Generator().manual_seed(33)
+    dh = (torch.randn(R, hidden, generator=g) * 1e-3).to(torch.bfloat16)
+    a = torch.randn(R, latent, generator=g).to(torch.bfloat16)
+    off = torch.from_numpy(offsets).cuda()
+    mask, seed = 0x6B1D, 29
+    kt = B.group_k_capacity(R, E)
+    sdh = B.rht_quantize_grouped(dh.cuda(), off, mask, mode=B.SR, seed=seed, kt=kt)
+    sa = B.rht_quantize_grouped(a.cuda(), off, mask, mode=B.RNE, kt=kt)
+    out = torch.full((E * hidden, latent), -3.0, device="cuda", dtype=torch.float32 if fp32 else torch.bfloat16)
+    c_amax = torch.full((E,), -1.0, device="cuda")
+    B.grouped_gemm_k(sdh, sa, off, out_dtype=B.OUT_FP32 if fp32 else B.OUT_BF16, out=out, c_amax=c_amax)
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy().reshape(E, hidden, latent)
+    rdh = orc.rht_quantize_grouped(dh, offsets, kt, mask, mode=orc.SR, seed=seed)
+    ra = orc.rht_quantize_grouped(a, offsets, kt, mask, mode=orc.RNE)
+    got_amax = c_amax.cpu().numpy()
+    for e in range(E):
+        ko0, ko1 = orc.group_k_offset(offsets, e), orc.group_k_offset(offsets, e + 1)
+        if ko1 == ko0:
+            assert (o[e] == 0).all() and got_amax[e] == 0.0
+            continue
+        Ad = orc.dequantize_rows(rdh["codes"], rdh["sf"], kt, float(rdh["amax"][e]), np.arange(hidden))[:, ko0:ko1]
+        Bd = orc.dequantize_rows(ra["codes"], ra["sf"], kt, float(ra["amax"][e]), np.arange(latent))[:, ko0:ko1]
+        ref, absum = orc.gemm(np.ascontiguousarray(Ad), np.ascontiguousarray(Bd))
+        _check(o[e], ref, absum, bf16=not fp32)
+        assert got_amax[e] == float(np.abs(o[e]).max())
+        # the transform is orthogonal: the result estimates dH_g^T A_g
+        exact = dh[offsets[e]:offsets[e + 1]].double().T @ a[offsets[e]:offsets[e + 1]].double()
+        if offsets[e + 1] - offsets[e] > 64:
+            rel = np.linalg.norm(o[e] - exact.numpy()) / np.linalg.norm(exact.numpy())
+            assert rel < 0.3
+    assert B.device_status() == 0

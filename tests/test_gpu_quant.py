@@ -184,3 +184,37 @@ def test_quantize_2d_fused(B, orc, batch, rows, cols):
         assert (np_u8(qw.sf) == ref["sf"]).all()
         assert (np_u8(tile) == ref["tile_sf"]).all()
     assert B.device_status() == 0
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("cols", [48, 300])
+def test_rht_quantize_grouped(B, orc, mode, cols):
+    """Expert-segmented RHT + quantisation (wgrad inputs of the expert GEMMs):
+    every expert's tokens zero-padded to a multiple of 64 at the running sum of
+    padded counts, its own amax; bytes equal the oracle's on the used columns,
+    with empty and one-token experts and a capacity larger than needed."""
+    offsets = np.array([0, 0, 1, 70, 70, 200, 265], dtype=np.int64)
+    counts = np.diff(offsets)
+    rows = int(offsets[-1])
+    g = torch.Generator().manual_seed(cols + mode)
+    scale = torch.from_numpy(np.repeat([1, 1, 4, 1, 0.01, 2.0], counts)).float()[:, None]
+    x = (torch.randn(rows, cols, generator=g) * scale).to(torch.bfloat16)
+    off = torch.from_numpy(offsets).cuda()
+    kt = B.group_k_capacity(rows, len(counts))
+    assert kt % 64 == 0 and kt >= ((counts + 63) // 64 * 64).sum()
+    q = B.rht_quantize_grouped(x.cuda(), off, 0x2D71, mode=mode, seed=4321)
+    torch.cuda.synchronize()
+    ref = orc.rht_quantize_grouped(x, offsets, kt, 0x2D71, mode=mode, seed=4321)
+    used = orc.group_k_offset(offsets, len(counts))
+    assert (np_u8(q.amax) == ref["amax"]).all()
+    assert (np_u8(q.codes)[:, :used // 2] == ref["codes"][:, :used // 2]).all()
+    sf = np_u8(q.sf)
+    for c in range(cols):
+        for b in range(used // 16):
+            off_b = orc.sf_offset(c, b, kt)
+            assert sf[off_b] == ref["sf"][off_b], (c, b)
+    # the supplied-amax path gives the same bytes
+    q2 = B.rht_quantize_grouped(x.cuda(), off, 0x2D71, mode=mode, seed=4321, amax_in=q.amax.clone())
+    torch.cuda.synchronize()
+    assert (np_u8(q2.codes)[:, :used // 2] == ref["codes"][:, :used // 2]).all()
+    assert B.device_status() == 0
