@@ -402,6 +402,7 @@ def main():
                   "traffic": None}
 
     supplied = measure_supplied_amax(wk, pk["hbm_gbs"])
+    next_rows = measure_next_rows(wk, pk["hbm_gbs"], fp4_peak_sust)
 
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
@@ -424,6 +425,7 @@ def main():
         "quantize_frac_hbm": round(quant_bytes / (quant_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
         "ops": ops, "roofline": roofline, "roofline_quantize": roofline_q,
         "quantize_supplied_amax": supplied,
+        "next_rows": next_rows,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk,
         "device_status": status, "routing": {"max_vio": round(wk.routing.max_vio, 3),
                                              "empty_experts": int((wk.routing.counts == 0).sum())},
@@ -487,6 +489,63 @@ def measure_supplied_amax(wk: Workload, hbm_gbs: float, iters: int = 5):
         ms = e0.elapsed_time(e1) / iters
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4)}
+    return out
+
+
+def measure_next_rows(wk: Workload, hbm_gbs: float, fp4_peak: float, iters: int = 3):
+    """The grouped backward of the LatentMoE up-projection, timed alone after
+    the timed region (not part of the step): dgrad dA = dH . W_up per expert
+    (W_up^T from the batched 2D quantiser, dH in 1x16 SR) and wgrad
+    dW_up = RHT(dH)^T . RHT(A) per expert (expert-segmented RHT quantisers,
+    groups along K, FP32 dW).  The step's H stands in for dH."""
+    import torch
+    B = wk.B
+    m = wk.moe
+    E, L, Hh, R = m.experts, m.latent, m.expert_hidden, wk.R
+    dev = wk.h.device
+    dh = wk.h
+    qdh = B.quantize_1d_grouped(dh, wk.offsets, B.SR, wk.seed)
+    qwt = B.quantize_2d(wk.w_up, want_t=True)[1]
+    da = torch.empty(R, L, dtype=torch.bfloat16, device=dev)
+    kt = B.group_k_capacity(R, E)
+    sdh = B.empty_qtensor(Hh, kt, dev, n_amax=E)
+    sa = B.empty_qtensor(L, kt, dev, n_amax=E)
+    dw = torch.empty(E * Hh, L, dtype=torch.float32, device=dev)
+    gem = 2.0 * R * Hh * L
+    cases = [
+        ("grouped_gemm dgrad (dA = dH . W_up)", "tensor", gem,
+         lambda: B.grouped_gemm(qdh, wk.offsets, qwt, L, B.OUT_BF16, out=da)),
+        ("rht_quantize_grouped dH (amax + SR)", "hbm", 4.5625 * R * Hh,
+         lambda: B.rht_quantize_grouped(dh, wk.offsets, wk.mask, B.SR, wk.wseed, kt=kt, out=sdh)),
+        ("rht_quantize_grouped A (amax + RNE)", "hbm", 4.5625 * R * L,
+         lambda: B.rht_quantize_grouped(wk.a, wk.offsets, wk.mask, B.RNE, 0, kt=kt, out=sa)),
+        ("grouped_gemm_k wgrad (dW_up, FP32)", "tensor", gem,
+         lambda: B.grouped_gemm_k(sdh, sa, wk.offsets, B.OUT_FP32, out=dw)),
+    ]
+    out = {}
+    for name, kind, work, fn in cases:
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / iters
+        if kind == "tensor":
+            tf = work / (ms * 1e-3) / 1e12
+            out[name] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_fp4_sustained": round(tf / fp4_peak, 4)}
+        else:
+            gbs = work / (ms * 1e-3) / 1e9
+            out[name] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4)}
+    # the wgrad writes E * Hh * L FP32 outputs: its HBM roof
+    w = out["grouped_gemm_k wgrad (dW_up, FP32)"]
+    wbytes = 4.0 * E * Hh * L + 0.5625 * (Hh + L) * kt
+    w["hbm_gbs"] = round(wbytes / (w["ms"] * 1e-3) / 1e9, 1)
+    w["frac_hbm"] = round(w["hbm_gbs"] / hbm_gbs, 4)
+    del qdh, qwt, da, sdh, sa, dw
+    torch.cuda.empty_cache()
     return out
 
 
