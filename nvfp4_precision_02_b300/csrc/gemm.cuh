@@ -122,8 +122,6 @@ struct GemmParams {
     int64_t ldc;
     float* c_amax;              // nullable: max |C| over the written outputs, per group (zeroed by the host)
     bool vec_store;             // rows of C start 16-byte aligned: vector stores
-    bool kgroup;                // groups split K (expert wgrad): group g owns the 64-padded token
-                                // segment of offsets[g] .. offsets[g+1] and C rows g*M .. g*M+M-1
 };
 
 // ------------------------------------------------------------------ PTX
@@ -461,9 +459,8 @@ struct TileCoord {
     int nt;           // n-tile
     int32_t row0;     // first A row of the tile
     int32_t rows;     // valid rows (<= 128)
-    int32_t k0 = 0;   // first K element of the tile (groups along K)
+    int32_t k0 = 0;   // first K element of the tile (groups along K; C rows then start at g * M + row0)
     int32_t ka = -1;  // 64-wide K atoms of the tile; -1: all of K
-    int64_t crow0 = -1;  // first C row; -1: row0
 };
 
 // Tiles are numbered in bands of G_BAND m-tiles: inside a band, the m-tile
@@ -525,7 +522,7 @@ __device__ __forceinline__ TileCoord decode_pair_tile(int64_t t, int ptiles, int
 // Tiles of a GEMM whose groups split K: for every group, the m-tiles (or
 // row pairs) of the shared M rows x the n-tiles, the m-tile fastest.  Group
 // g's K slice starts at kpad[g] and spans (kpad[g+1] - kpad[g]) / 64 atoms
-// (possibly none: C_g is then zero); its C rows start at g * M.
+// (possibly none: C_g is then zero); its C rows start at g * M + row0.
 __device__ __forceinline__ TileCoord decode_kgroup_tile(int64_t t, int mt, int ntiles, const int32_t* kpad,
                                                         int64_t M, int64_t K, bool pair, uint32_t rank) {
     const int64_t per_g = (int64_t)mt * ntiles;
@@ -542,7 +539,6 @@ __device__ __forceinline__ TileCoord decode_kgroup_tile(int64_t t, int mt, int n
     const int32_t k1 = (int32_t)min((int64_t)kpad[c.g + 1], K);
     c.k0 = (int32_t)min((int64_t)kpad[c.g], K);
     c.ka = max(0, k1 - c.k0) / 64;
-    c.crow0 = (int64_t)c.g * M + c.row0;
     return c;
 }
 
@@ -551,7 +547,7 @@ __device__ __forceinline__ uint4 ldg_u4(const uint8_t* p) { return __ldg(reinter
 // ------------------------------------------------------------------ kernel
 // OUT_FP32: FP32 output (stored directly); otherwise bf16.  TMA_STORE (bf16
 // only): the output leaves through tm_c (rows 16-byte aligned).
-template <bool OUT_FP32, bool TMA_STORE, bool PAIR>
+template <bool OUT_FP32, bool TMA_STORE, bool PAIR, bool KGROUP = false>
 __global__ void __launch_bounds__(G_THREADS, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                  const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
@@ -572,7 +568,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     int32_t* tab = reinterpret_cast<int32_t*>(smem + L::TAB_OFF);
     const int groups = p.groups;
     // groups along K: pad[] holds the 64-padded token segments (no pair table)
-    GroupTables gt{tab, tab + groups + 1, (PAIR && !p.kgroup) ? tab + 2 * (groups + 1) : nullptr};
+    GroupTables gt{tab, tab + groups + 1, (PAIR && !KGROUP) ? tab + 2 * (groups + 1) : nullptr};
     // CTA pairs: rank 0 issues the MMAs of both; barriers that collect both
     // CTAs' arrivals (full, sf_full, acc_empty) are rank 0's.
     const uint32_t rank = PAIR ? cluster_rank() : 0u;
@@ -614,7 +610,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         }
     }
-    if (p.kgroup) {
+    if (KGROUP) {
         build_group_tables(p.offsets, groups, p.K, gt, 6);
     } else if (p.offsets != nullptr) {
         build_group_tables(p.offsets, groups, p.M, gt);
@@ -635,22 +631,22 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     // groups along M: tiles from the padded row tables; groups along K: every
     // group has all m-tiles (or row pairs) of the shared M rows
     const int kg_mt = (int)(PAIR ? (p.M + 255) / 256 : (p.M + 127) / 128);
-    const int mtiles = p.kgroup ? 0 : gt.pad[groups] >> 7;
-    const int ptiles = (PAIR && !p.kgroup) ? (gt.pair[groups] >> 8) : 0;
-    const int64_t total = p.kgroup ? (int64_t)groups * kg_mt * ntiles : (int64_t)(PAIR ? ptiles : mtiles) * ntiles;
+    const int mtiles = KGROUP ? 0 : gt.pad[groups] >> 7;
+    const int ptiles = (PAIR && !KGROUP) ? (gt.pair[groups] >> 8) : 0;
+    const int64_t total = KGROUP ? (int64_t)groups * kg_mt * ntiles : (int64_t)(PAIR ? ptiles : mtiles) * ntiles;
     // a pair walks the tiles of its cluster (blockIdx.x / 2), both CTAs alike
     const int64_t t_first = PAIR ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
     const int64_t t_step = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
     auto tile_at = [&](int64_t t) {
-        if (p.kgroup) return decode_kgroup_tile(t, kg_mt, ntiles, gt.pad, p.M, p.K, PAIR, rank);
+        if (KGROUP) return decode_kgroup_tile(t, kg_mt, ntiles, gt.pad, p.M, p.K, PAIR, rank);
         return PAIR ? decode_pair_tile(t, ptiles, ntiles, gt.off, gt.pad, gt.pair, groups, rank)
                     : decode_tile(t, mtiles, ntiles, gt.off, gt.pad, groups);
     };
     const int katoms = (int)((p.K + 63) / 64);           // atoms of a whole operand row (scale row stride)
     // K atoms and stages of a tile
-    auto tile_atoms = [&](const TileCoord& tc) { return tc.ka >= 0 ? tc.ka : katoms; };
+    auto tile_atoms = [&](const TileCoord& tc) { return KGROUP ? tc.ka : katoms; };
     const int nrb = (int)((p.N + 127) / 128);            // 128-row scale blocks of one B operand
-    const int64_t b_rows_per_group = (p.offsets != nullptr && !p.kgroup) ? p.N : 0;
+    const int64_t b_rows_per_group = (p.offsets != nullptr && !KGROUP) ? p.N : 0;
 
     if (warp == G_W_TMA) {
         // ------------------------------------------------ TMA producer (A, B)
@@ -729,7 +725,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 tc_fence_after();
                 // a tile with no K (an expert without tokens) issues nothing: its
                 // epilogue writes zeros
-                const int ka = tile_atoms(tile_at(t)), kst = (ka + 3) / 4;
+                const int ka = KGROUP ? tile_at(t).ka : katoms, kst = (ka + 3) / 4;
                 for (int ks = 0; ks < kst; ++ks) {
                     if (!mbar_wait(full0 + 8 * s, ph, abort_flag) || !mbar_wait(sff0 + 8 * s, ph, abort_flag)) {
                         ok = false;
@@ -834,8 +830,8 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             // groups along K: C rows of group g start at g * M; a group without
             // K (an expert without tokens) stores zeros (vmask clears the
             // accumulator words, which no MMA wrote)
-            const int64_t crow0 = tc.crow0 >= 0 ? tc.crow0 : (int64_t)tc.row0;
-            const uint32_t vmask = tile_atoms(tc) == 0 ? 0u : 0xFFFFFFFFu;
+            const int32_t crow0 = KGROUP ? tc.g * (int32_t)p.M + tc.row0 : tc.row0;   // < 2^31 (host check)
+            const uint32_t vmask = (KGROUP && tc.ka == 0) ? 0u : 0xFFFFFFFFu;
             const int64_t row = crow0 + r;
             const int64_t col0 = (int64_t)tc.nt * G_BN + chunk * 64;
             if (OUT_FP32) {

@@ -561,10 +561,10 @@ static bool use_pair() {
     return !(e != nullptr && e[0] == '0');
 }
 
-template <bool F32, bool TS, bool PAIR>
+template <bool F32, bool TS, bool PAIR, bool KG = false>
 static nvfp4_status launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                                const GemmParams& p, int grid, int smem, nvfp4_stream_t stream) {
-    auto kern = k_gemm_nvfp4<F32, TS, PAIR>;
+    auto kern = k_gemm_nvfp4<F32, TS, PAIR, KG>;
     if (!PAIR) {
         kern<<<grid, G_THREADS, smem, stream>>>(ma, mb, mc, p);
         return launched("k_gemm_nvfp4");
@@ -585,13 +585,14 @@ static nvfp4_status launch_one(const CUtensorMap& ma, const CUtensorMap& mb, con
     return launched("k_gemm_nvfp4 pair");
 }
 
-template <bool F32, bool TS, bool PAIR>
+template <bool F32, bool TS, bool PAIR, bool KG = false>
 static nvfp4_status set_gemm_attr() {
-    NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<F32, TS, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<F32, TS, PAIR, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              gemm_smem_bytes(TS, NVFP4_MAX_GROUPS, PAIR)),
                         "smem attr"));
     if (PAIR)
-        NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<F32, TS, PAIR>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0),
+        NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<F32, TS, PAIR, KG>,
+                                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 0),
                             "cluster attr"));
     return NVFP4_OK;
 }
@@ -618,10 +619,12 @@ static nvfp4_status pair_clusters(int smem, int* out) {
 }
 
 // tiles_1cta: output tiles of 128 x 256 (grid bound of the single-CTA
-// kernel); pair_tiles: tiles of 256 x 256.
+// kernel); pair_tiles: tiles of 256 x 256.  kgroup: groups split K (the
+// expert wgrad; FP32 or TMA-stored bf16 outputs).
 static nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                                 const GemmParams& p, int64_t tiles_1cta, int64_t pair_tiles, int sms,
-                                nvfp4_out_dtype dt, bool tma_store, bool pair, nvfp4_stream_t stream, int dev) {
+                                nvfp4_out_dtype dt, bool tma_store, bool pair, nvfp4_stream_t stream, int dev,
+                                bool kgroup = false) {
     const bool f32 = dt == NVFP4_OUT_FP32;
     const int smem = gemm_smem_bytes(tma_store, p.groups, pair);
     int clusters = 0;
@@ -634,6 +637,10 @@ static nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, co
             NVFP4_TRY((set_gemm_attr<false, false, true>()));
             NVFP4_TRY((set_gemm_attr<false, true, true>()));
             NVFP4_TRY((set_gemm_attr<true, false, true>()));
+            NVFP4_TRY((set_gemm_attr<true, false, false, true>()));
+            NVFP4_TRY((set_gemm_attr<false, true, false, true>()));
+            NVFP4_TRY((set_gemm_attr<true, false, true, true>()));
+            NVFP4_TRY((set_gemm_attr<false, true, true, true>()));
             const int full = gemm_smem_bytes(true, NVFP4_MAX_GROUPS, true);   // the largest pair layout
             int c0 = 0, c1 = 0, c2 = 0;
             NVFP4_TRY((pair_clusters<false, false>(full, &c0)));
@@ -644,14 +651,23 @@ static nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, co
         }
         clusters = g_dev[dev].pair_clusters;
     }
+    if (kgroup && !f32 && !tma_store) return fail(NVFP4_ERR_ALIGN, "bf16 output of a K-grouped GEMM needs 16-byte rows");
     if (!pair) {
         const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_1cta, sms));
+        if (kgroup) {
+            if (f32) return launch_one<true, false, false, true>(ma, mb, mc, p, grid, smem, stream);
+            return launch_one<false, true, false, true>(ma, mb, mc, p, grid, smem, stream);
+        }
         if (f32) return launch_one<true, false, false>(ma, mb, mc, p, grid, smem, stream);
         if (tma_store) return launch_one<false, true, false>(ma, mb, mc, p, grid, smem, stream);
         return launch_one<false, false, false>(ma, mb, mc, p, grid, smem, stream);
     }
     if (clusters < 1) return fail(NVFP4_ERR_CUDA, "the CTA-pair GEMM cannot be resident");
     const int grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(pair_tiles, clusters));
+    if (kgroup) {
+        if (f32) return launch_one<true, false, true, true>(ma, mb, mc, p, grid, smem, stream);
+        return launch_one<false, true, true, true>(ma, mb, mc, p, grid, smem, stream);
+    }
     if (f32) return launch_one<true, false, true>(ma, mb, mc, p, grid, smem, stream);
     if (tma_store) return launch_one<false, true, true>(ma, mb, mc, p, grid, smem, stream);
     return launch_one<false, false, true>(ma, mb, mc, p, grid, smem, stream);
@@ -796,7 +812,7 @@ nvfp4_status nvfp4_grouped_gemm_k(const nvfp4_tensor* a, const nvfp4_tensor* b, 
     NVFP4_TRY(make_code_map(&mb, b->codes, N, KT / 2, pair ? G_BN / 2 : G_BN));
     GemmParams p{};
     p.M = M; p.N = N; p.K = KT;
-    p.offsets = offsets; p.groups = num_groups; p.kgroup = true;
+    p.offsets = offsets; p.groups = num_groups;
     p.sfa = a->sf; p.sfb = b->sf; p.sfb_group_stride = 0;
     p.amax_a = a->amax; p.amax_b = b->amax;
     p.c = c; p.ldc = ldc;
@@ -813,7 +829,7 @@ nvfp4_status nvfp4_grouped_gemm_k(const nvfp4_tensor* a, const nvfp4_tensor* b, 
     if (c_dtype == NVFP4_OUT_BF16) NVFP4_TRY(make_store_map(&mc, c, M * num_groups, N, ldc, &tma_store));
     const int64_t tiles = (int64_t)num_groups * cdiv(M, G_BM) * cdiv(N, G_BN);
     const int64_t pair_tiles = (int64_t)num_groups * cdiv(M, 2 * G_BM) * cdiv(N, G_BN);
-    return launch_gemm(ma, mb, mc, p, tiles, pair_tiles, sms, c_dtype, tma_store, pair, stream, dev);
+    return launch_gemm(ma, mb, mc, p, tiles, pair_tiles, sms, c_dtype, tma_store, pair, stream, dev, true);
 }
 
 nvfp4_status nvfp4_device_status(int32_t* flags) {
