@@ -71,6 +71,8 @@ def lib():
             "oracle_rht_quantize": (None, [P, i64, i64, i64, ctypes.c_uint16, ctypes.c_int, u64,
                                            P, P, P, P]),
             "oracle_group_k_offset": (i64, [P, i32]),
+            "oracle_fp16_sr": (ctypes.c_uint16, [f32, u32]),
+            "oracle_sr_fp16": (None, [P, i64, u64, P]),
             "oracle_rht_quantize_grouped": (None, [P, i64, i64, i64, P, i32, i64, ctypes.c_uint16, ctypes.c_int,
                                                    u64, P, P, P, P]),
             "oracle_dequantize_rows": (None, [P, P, i64, i64, f32, P, i64, P]),
@@ -247,6 +249,19 @@ def rht_quantize(x, sign_mask: int, mode: int = RNE, seed: int = 0, amax_in: Opt
     lib().oracle_rht_quantize(_p(xb), tokens, cols, cols, sign_mask, mode, seed, _p(ain),
                               _p(codes), _p(sf), _p(am))
     return {"codes": codes, "sf": sf, "amax": float(am[0])}
+
+
+def fp16_sr(x: float, u: int) -> int:
+    """FP16 bits of x stochastically rounded with the 32-bit word u (R15)."""
+    return lib().oracle_fp16_sr(x, u)
+
+
+def sr_fp16(x, seed: int) -> np.ndarray:
+    """FP32 array -> FP16 bits (uint16) with SR, word of element e from (seed, e) (R4, R15)."""
+    xs = np.ascontiguousarray(np.asarray(x, dtype=np.float32)).reshape(-1)
+    out = np.zeros(xs.size, dtype=np.uint16)
+    lib().oracle_sr_fp16(_p(xs), xs.size, seed, _p(out))
+    return out
 
 
 def group_k_offset(offsets, g: int) -> int:

@@ -38,6 +38,8 @@
  *      y = 0.25 * H * (s .* x), FP32 butterfly with stages 1, 2, 4, 8.
  *   R6 layouts       codes packed two per byte (even index in the low
  *      nibble); block scales in 128x4 atoms (see oracle_sf_offset).
+ *   R14 expert segments of the grouped wgrad (oracle_rht_quantize_grouped).
+ *   R15 FP16 SR of the SSM cache (oracle_fp16_sr).
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fopenmp -shared -fPIC
  * The FP32 steps must not be contracted into FMAs or reassociated.
@@ -611,6 +613,60 @@ void oracle_gemm(const double *A, const double *B, int64_t M, int64_t N, int64_t
             absum[m * N + n] = a;
         }
     }
+}
+
+/* ------------------------------------------------------------------ */
+/* FP16 stochastic rounding for the SSM cache ([SL-4.3]).                */
+/* ------------------------------------------------------------------ */
+
+/* Reading R15: [SL-4.3] keeps the Mamba SSM cache in FP16 with stochastic
+ * rounding driven by Philox with 5 rounds and gives no further rule.  Here,
+ * for a finite x with m = |x| < 65504: lo = the largest FP16 magnitude <= m,
+ * hi = the next FP16 magnitude, p = (m - lo) / (hi - lo) (exact in FP64);
+ * the magnitude becomes hi iff u < 256 * ceil(p * 2^24) (the resolution of
+ * R4), u = the R4 word of element e; the sign is kept (so -0 stays -0).
+ * m >= 65504 (and infinities) saturate to 65504; NaN becomes the FP16
+ * quiet NaN 0x7E00 with the sign of x. */
+static double fp16_spacing(double m)
+{
+    int e;
+    if (m < ldexp(1.0, -14)) return ldexp(1.0, -24);
+    frexp(m, &e);                                    /* m = f * 2^e, f in [0.5, 1) */
+    return ldexp(1.0, e - 1 - 10);
+}
+
+static uint16_t fp16_bits_of(double v)               /* v: an FP16 magnitude <= 65504 */
+{
+    int e;
+    if (v < ldexp(1.0, -14)) return (uint16_t)(v * ldexp(1.0, 24));
+    frexp(v, &e);
+    return (uint16_t)(((e - 1 + 15) << 10) | (uint16_t)((v / ldexp(1.0, e - 1) - 1.0) * 1024.0));
+}
+
+uint16_t oracle_fp16_sr(float x, uint32_t u)
+{
+    uint32_t bits;
+    uint16_t sign;
+    double m, sp, lo, p, c;
+    memcpy(&bits, &x, 4);
+    sign = (uint16_t)((bits >> 16) & 0x8000u);
+    if (isnan(x)) return (uint16_t)(sign | 0x7E00u);
+    m = fabs((double)x);
+    if (m >= 65504.0) return (uint16_t)(sign | 0x7BFFu);
+    sp = fp16_spacing(m);
+    lo = floor(m / sp) * sp;
+    p = (m - lo) / sp;
+    c = ceil(p * 16777216.0);
+    if ((double)u < 256.0 * c) lo += sp;
+    return (uint16_t)(sign | fp16_bits_of(lo));
+}
+
+/* out[e] = SR of x[e] to FP16 with the R4 word of index e under seed. */
+void oracle_sr_fp16(const float *x, int64_t n, uint64_t seed, uint16_t *out)
+{
+    int64_t e;
+#pragma omp parallel for schedule(static)
+    for (e = 0; e < n; ++e) out[e] = oracle_fp16_sr(x[e], oracle_sr_word(seed, (uint64_t)e));
 }
 
 /* Number of threads the parallel loops above use. */

@@ -471,3 +471,57 @@ def test_maxvio_bound():
     counts[:22] = 100          # every one of 100 tokens picks the same 22 experts
     fake = wl.Routing(torch.zeros(0), torch.zeros(0), torch.zeros(513), counts, 22)
     assert abs(fake.max_vio - 512 / 22) < 1e-12
+
+
+# ------------------------------------------------------------ FP16 SR (SSM cache, reading R15)
+def test_fp16_sr_keeps_exact_fp16_values(orc):
+    """Every finite FP16 value is its own rounding for any word (p = 0)."""
+    h = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = h.view(np.float16)
+    keep = np.isfinite(vals)
+    xs = vals[keep].astype(np.float32)
+    bits = h[keep]
+    rng = np.random.default_rng(50)
+    for x, b, u in zip(xs[::7], bits[::7], rng.integers(0, 1 << 32, size=len(xs[::7]), dtype=np.uint64)):
+        assert orc.fp16_sr(float(x), int(u)) == b
+
+
+def test_fp16_sr_brackets_and_is_unbiased(orc):
+    """The result is one of the two FP16 neighbours of x, and over an even
+    grid of 65536 words its mean is x to within 2^-16 of the local spacing."""
+    rng = np.random.default_rng(51)
+    xs = (rng.standard_normal(300) * np.exp(rng.uniform(-20, 10, 300))).astype(np.float32)
+    us = (np.arange(65536, dtype=np.uint64) << 16) | 0x1234
+    for x in xs[:40]:
+        r = np.float16(x)                                   # RNE: one neighbour
+        if float(r) == float(x):
+            continue
+        other = np.nextafter(r, np.float16(np.inf) if float(x) > float(r) else np.float16(-np.inf))
+        lo, hi = sorted([abs(float(r)), abs(float(other))])
+        assert lo < abs(float(x)) < hi
+        got = np.array([orc.fp16_sr(float(x), int(u)) for u in us[::64]], dtype=np.uint16).view(np.float16)
+        assert set(np.abs(got.astype(np.float64))) <= {lo, hi}
+    for x in xs[:6]:
+        got = np.array([orc.fp16_sr(float(x), int(u)) for u in us], dtype=np.uint16).view(np.float16)
+        m = abs(float(x))
+        r = np.float16(m)
+        sp = abs(float(np.nextafter(r, np.float16(np.inf))) - float(r)) if float(r) <= m else \
+            abs(float(r) - float(np.nextafter(r, np.float16(0))))
+        assert abs(np.abs(got.astype(np.float64)).mean() - m) <= sp * 2.0 ** -16 + 1e-30
+
+
+def test_fp16_sr_threshold_and_special_values(orc):
+    """p = 3/4 rounds up for exactly the words below 3 * 2^30; saturation at
+    65504, NaN kept (sign too), signed zero kept, the FP16 subnormal range."""
+    x = 1.0 + 3 * 2.0 ** -12                                # 3/4 of the way from 1 to 1 + 2^-10
+    assert orc.fp16_sr(x, 3 * (1 << 30) - 1) == 0x3C01
+    assert orc.fp16_sr(x, 3 * (1 << 30)) == 0x3C00
+    assert orc.fp16_sr(70000.0, 0) == 0x7BFF and orc.fp16_sr(-float("inf"), 0) == 0xFBFF
+    assert orc.fp16_sr(float("nan"), 0) & 0x7FFF == 0x7E00
+    assert orc.fp16_sr(-0.0, 0) == 0x8000 and orc.fp16_sr(0.0, 0) == 0
+    t = 2.0 ** -24 * 0.25                                    # a quarter of the smallest subnormal
+    assert orc.fp16_sr(t, (1 << 30) - 1) == 1 and orc.fp16_sr(t, 1 << 30) == 0
+    # the word of element e is the R4 word of index e
+    xs = np.linspace(-3, 3, 37).astype(np.float32) * 1.001
+    got = orc.sr_fp16(xs, 99)
+    assert all(got[e] == orc.fp16_sr(float(xs[e]), orc.sr_word(99, e)) for e in range(len(xs)))
