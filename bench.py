@@ -497,7 +497,8 @@ def measure_next_rows(wk: Workload, hbm_gbs: float, fp4_peak: float, iters: int 
     the timed region (not part of the step): dgrad dA = dH . W_up per expert
     (W_up^T from the batched 2D quantiser, dH in 1x16 SR) and wgrad
     dW_up = RHT(dH)^T . RHT(A) per expert (expert-segmented RHT quantisers,
-    groups along K, FP32 dW).  The step's H stands in for dH."""
+    groups along K, FP32 dW).  The step's H stands in for dH.  Also the FP16
+    stochastic rounding of an SSM cache (FP32 in, FP16 out)."""
     import torch
     B = wk.B
     m = wk.moe
@@ -539,6 +540,22 @@ def measure_next_rows(wk: Workload, hbm_gbs: float, fp4_peak: float, iters: int 
         else:
             gbs = work / (ms * 1e-3) / 1e9
             out[name] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4)}
+    # FP16 SR of an SSM cache (next row f4): 256 sequences x 256 heads x 64 x state 128, FP32 in
+    ssm = torch.randn(256 * 256 * 64 * 128, device=dev)
+    ssm16 = torch.empty(ssm.numel(), dtype=torch.float16, device=dev)
+    B.sr_fp16(ssm, 5, out=ssm16)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        B.sr_fp16(ssm, 5, out=ssm16)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    gbs = 6.0 * ssm.numel() / (ms * 1e-3) / 1e9
+    out["sr_fp16 SSM cache (FP32 -> FP16, 6 B / element)"] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
+                                                              "frac_hbm": round(gbs / hbm_gbs, 4)}
+    del ssm, ssm16
     # the wgrad writes E * Hh * L FP32 outputs: its HBM roof
     w = out["grouped_gemm_k wgrad (dW_up, FP32)"]
     wbytes = 4.0 * E * Hh * L + 0.5625 * (Hh + L) * kt

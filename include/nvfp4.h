@@ -239,6 +239,17 @@ nvfp4_status nvfp4_rht_quantize(const void *x, int64_t tokens, int64_t cols, int
                                 const float *amax_in, nvfp4_tensor *out_t,
                                 nvfp4_stream_t stream);
 
+/* FP32 -> FP16 with stochastic rounding: the Mamba SSM-cache recipe of the
+ * Super summary (section 4.3: FP16 cache, stochastic rounding driven by
+ * Philox with 5 rounds).  x: device FP32 [n] (4-byte aligned); out: device
+ * FP16 bits [n] (2-byte aligned).  For m = |x[e]| < 65504 with FP16
+ * neighbours lo <= m < hi, the magnitude becomes hi iff u < 256 * ceil(p *
+ * 2^24), p = (m - lo) / (hi - lo), u = word e & 3 of Philox4x32-5 with key
+ * seed and counter (e >> 2, 0, 0) (the same words as the SR quantisers);
+ * m >= 65504 and infinities saturate to 65504, NaN becomes 0x7E00, the sign
+ * is kept.  Not part of the NVFP4 recipe itself: a second user of its SR. */
+nvfp4_status nvfp4_sr_fp16(const float *x, int64_t n, uint64_t seed, uint16_t *out, nvfp4_stream_t stream);
+
 /* Columns needed by nvfp4_rht_quantize_grouped for `rows` expert-sorted
  * tokens in `groups` experts, whatever the split: ceil((rows + 63 * groups)
  * / 64) * 64 (every expert's segment is padded to a multiple of 64). */

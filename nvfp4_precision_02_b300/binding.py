@@ -32,7 +32,7 @@ EXPORTS = ["nvfp4_sf_bytes", "nvfp4_sf_bytes_grouped", "nvfp4_sf_offset", "nvfp4
            "nvfp4_quantize_1d", "nvfp4_quantize_1d_grouped", "nvfp4_quantize_2d",
            "nvfp4_quantize_2d_fused_workspace", "nvfp4_quantize_2d_fused", "nvfp4_quantize_2d_fused_static",
            "nvfp4_rht_amax",
-           "nvfp4_rht_quantize", "nvfp4_group_k_capacity", "nvfp4_rht_quantize_grouped", "nvfp4_gemm",
+           "nvfp4_rht_quantize", "nvfp4_sr_fp16", "nvfp4_group_k_capacity", "nvfp4_rht_quantize_grouped", "nvfp4_gemm",
            "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_k", "nvfp4_status_string",
            "nvfp4_last_error", "nvfp4_device_status", "nvfp4_launch_count", "nvfp4_debug_inject",
            "nvfp4_debug_wait_timeout"]
@@ -80,6 +80,7 @@ def lib():
             "nvfp4_gemm": (st, [TP, TP, P, i64, ctypes.c_int, P, P]),
             "nvfp4_grouped_gemm": (st, [TP, P, i32, TP, i64, P, i64, ctypes.c_int, P, P]),
             "nvfp4_group_k_capacity": (i64, [i64, i32]),
+            "nvfp4_sr_fp16": (st, [P, i64, ctypes.c_uint64, P, P]),
             "nvfp4_rht_quantize_grouped": (st, [P, i64, i64, i64, P, i32, i64, ctypes.c_uint16, ctypes.c_int,
                                                 ctypes.c_uint64, P, TP, P]),
             "nvfp4_grouped_gemm_k": (st, [TP, TP, P, i32, P, i64, ctypes.c_int, P, P]),
@@ -271,6 +272,15 @@ def rht_quantize(x: torch.Tensor, sign_mask: int, mode: int = RNE, seed: int = 0
     co = out.c()
     _check(lib().nvfp4_rht_quantize(_ptr(x), tokens, cols, ld, sign_mask, mode, seed, _ptr(amax_in),
                                     ctypes.byref(co), _stream(stream)))
+    return out
+
+
+def sr_fp16(x: torch.Tensor, seed: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """FP32 tensor -> FP16 tensor with stochastic rounding (Philox-5 word of each element)."""
+    assert x.dtype == torch.float32 and x.is_cuda and x.is_contiguous()
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float16, device=x.device)
+    _check(lib().nvfp4_sr_fp16(_ptr(x), x.numel(), seed, _ptr(out), _stream(stream)))
     return out
 
 

@@ -487,6 +487,20 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t tokens, int64_t cols, int
     return NVFP4_OK;
 }
 
+nvfp4_status nvfp4_sr_fp16(const float* x, int64_t n, uint64_t seed, uint16_t* out, nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    if (n < 0) return fail(NVFP4_ERR_SHAPE, "n < 0");
+    if (n == 0) return NVFP4_OK;
+    if (x == nullptr || out == nullptr) return fail(NVFP4_ERR_NULL, "x or out is NULL");
+    if (((uintptr_t)x & 3u) || ((uintptr_t)out & 1u)) return fail(NVFP4_ERR_ALIGN, "x or out misaligned");
+    int sms = 0;
+    NVFP4_TRY(check_device(&sms));
+    const int64_t nq = cdiv(n, 4);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(nq, 256), (int64_t)sms * 8));
+    k_sr_fp16<<<grid, 256, 0, stream>>>(x, n, seed, out);
+    return launched("k_sr_fp16");
+}
+
 int64_t nvfp4_group_k_capacity(int64_t rows, int32_t groups) {
     if (rows < 0 || groups < 1) return 0;
     return cdiv(rows + 63 * (int64_t)groups, 64) * 64;

@@ -631,6 +631,56 @@ __global__ void __launch_bounds__(Q2F_THREADS, 2) k_quant2d_fused(const uint16_t
     if (red_e >= 0) publish();
 }
 
+// ------------------------------------------------------------------ FP16 SR
+// FP32 -> FP16 with stochastic rounding by the Philox-5 word of each element
+// (the SSM-cache recipe of the "Nemotron 3 Super" summary, papers.lianghsun.dev,
+// section 4.3).  For m = |x| < 65504 with FP16 neighbours lo <= m < hi and
+// p = (m - lo) / (hi - lo), the magnitude becomes hi iff
+// u < 256 * ceil(p * 2^24); m >= 65504 saturates to 65504, NaN becomes the
+// quiet NaN 0x7E00, the sign is kept.  Integer form:
+//   FP16 normal range (m >= 2^-14): the 13 FP32 mantissa bits below the FP16
+//     ones are the fraction p * 2^13; adding ~u >> 19 carries into the FP16
+//     bits exactly when u >> 19 < that fraction, then the exponent is rebiased;
+//   FP16 subnormal range: |x| * 2^24 (exact) splits into the FP16 code floor
+//     and the fraction p, compared with u at 2^-24 resolution.
+// Identical to the definition for every FP32 pattern (checked exhaustively on
+// the host).
+__device__ __forceinline__ uint32_t fp16_sr(float x, uint32_t u) {
+    const uint32_t bits = __float_as_uint(x);
+    const uint32_t mb = bits & 0x7FFFFFFFu;
+    const uint32_t sign = (bits >> 16) & 0x8000u;
+    if (mb > 0x7F800000u) return sign | 0x7E00u;
+    if (mb >= 0x477FE000u) return sign | 0x7BFFu;
+    if (mb >= 0x38800000u) return sign | (((mb + (~u >> 19)) >> 13) - (112u << 10));
+    const float v = fabsf(x) * 16777216.0f;
+    const float fl = floorf(v);
+    const uint32_t c = __float2uint_ru((v - fl) * 16777216.0f);
+    const uint32_t up = (uint64_t)u < ((uint64_t)c << 8) ? 1u : 0u;
+    return sign | ((uint32_t)fl + up);
+}
+
+// out[e] = fp16_sr(x[e], word e of (seed, e)): four elements per thread and
+// Philox call (counter e / 4), 16-byte loads and 8-byte stores when aligned.
+__global__ void __launch_bounds__(256) k_sr_fp16(const float* __restrict__ x, int64_t n, uint64_t seed,
+                                                 uint16_t* __restrict__ out) {
+    const PhiloxKeys key = philox_keys(seed);
+    const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0) && ((reinterpret_cast<uintptr_t>(out) & 7) == 0);
+    const int64_t nq = (n + 3) >> 2;
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nq; q += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 w = sr_words(key, (uint64_t)q);
+        const int64_t e0 = q << 2;
+        if (vec && e0 + 4 <= n) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(x + e0));
+            const uint32_t lo = fp16_sr(v.x, w.x) | (fp16_sr(v.y, w.y) << 16);
+            const uint32_t hi = fp16_sr(v.z, w.z) | (fp16_sr(v.w, w.w) << 16);
+            *reinterpret_cast<uint2*>(out + e0) = make_uint2(lo, hi);
+        } else {
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            for (int i = 0; i < 4 && e0 + i < n; ++i) out[e0 + i] = (uint16_t)fp16_sr(__ldg(x + e0 + i), ws[i]);
+        }
+    }
+}
+
 // Padding of the 2D scale buffers (per batch entry: blockIdx.y).
 __global__ void __launch_bounds__(256) k_quant2d_pad(uint8_t* __restrict__ sf, uint8_t* __restrict__ sf_t,
                                                      int64_t rows, int64_t cols) {

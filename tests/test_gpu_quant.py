@@ -218,3 +218,26 @@ def test_rht_quantize_grouped(B, orc, mode, cols):
     torch.cuda.synchronize()
     assert (np_u8(q2.codes)[:, :used // 2] == ref["codes"][:, :used // 2]).all()
     assert B.device_status() == 0
+
+
+@pytest.mark.parametrize("n", [1, 7, 1000003])
+def test_sr_fp16(B, orc, n):
+    """FP32 -> FP16 stochastic rounding (SSM cache) equals the oracle bit for
+    bit: wide exponent spread, the FP16 subnormal range, signed zeros,
+    saturation, infinities and NaN; aligned (vector) and offset (element)
+    paths."""
+    rng = np.random.default_rng(n)
+    x = (rng.standard_normal(n) * np.exp(rng.uniform(-25, 12, n))).astype(np.float32)
+    special = np.array([0.0, -0.0, 65504.0, 70000.0, -np.inf, np.nan, 2.0 ** -25, -3e-7, 6e-8, 1.0 + 2.0 ** -11],
+                       dtype=np.float32)
+    x[:min(n, len(special))] = special[:min(n, len(special))]
+    xt = torch.from_numpy(x).cuda()
+    got = B.sr_fp16(xt, 0xC0FFEE)
+    torch.cuda.synchronize()
+    ref = orc.sr_fp16(x, 0xC0FFEE)
+    assert (got.cpu().numpy().view(np.uint16) == ref).all()
+    if n > 1:
+        got1 = B.sr_fp16(xt[1:], 0xC0FFEE)                 # 4-byte offset: element path
+        torch.cuda.synchronize()
+        assert (got1.cpu().numpy().view(np.uint16) == orc.sr_fp16(x[1:], 0xC0FFEE)).all()
+    assert B.device_status() == 0
