@@ -72,6 +72,7 @@ def lib():
                                            P, P, P, P]),
             "oracle_group_k_offset": (i64, [P, i32]),
             "oracle_fp16_sr": (ctypes.c_uint16, [f32, u32]),
+            "oracle_quantize_1d_mse": (None, [P, i64, i64, i64, P, P, P, P]),
             "oracle_sr_fp16": (None, [P, i64, u64, P]),
             "oracle_rht_quantize_grouped": (None, [P, i64, i64, i64, P, i32, i64, ctypes.c_uint16, ctypes.c_int,
                                                    u64, P, P, P, P]),
@@ -248,6 +249,19 @@ def rht_quantize(x, sign_mask: int, mode: int = RNE, seed: int = 0, amax_in: Opt
     ain = None if amax_in is None else np.array([amax_in], dtype=np.float32)
     lib().oracle_rht_quantize(_p(xb), tokens, cols, cols, sign_mask, mode, seed, _p(ain),
                               _p(codes), _p(sf), _p(am))
+    return {"codes": codes, "sf": sf, "amax": float(am[0])}
+
+
+def quantize_1d_mse(x, amax_in=None):
+    """1x16 RNE quantisation with each block's E4M3 scale chosen by minimum
+    squared error over all finite positive codes (R16)."""
+    xb = _bf16_bits(x)
+    rows, cols = xb.shape
+    codes = np.zeros((rows, cols // 2), dtype=np.uint8)
+    sf = np.zeros(sf_bytes(rows, cols), dtype=np.uint8)
+    am = np.zeros(1, dtype=np.float32)
+    ain = None if amax_in is None else np.array([amax_in], dtype=np.float32)
+    lib().oracle_quantize_1d_mse(_p(xb), rows, cols, cols, _p(ain), _p(codes), _p(sf), _p(am))
     return {"codes": codes, "sf": sf, "amax": float(am[0])}
 
 

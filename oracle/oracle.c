@@ -40,6 +40,7 @@
  *      nibble); block scales in 128x4 atoms (see oracle_sf_offset).
  *   R14 expert segments of the grouped wgrad (oracle_rht_quantize_grouped).
  *   R15 FP16 SR of the SSM cache (oracle_fp16_sr).
+ *   R16 PTQ block scales by minimum squared error (oracle_quantize_1d_mse).
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fopenmp -shared -fPIC
  * The FP32 steps must not be contracted into FMAs or reassociated.
@@ -613,6 +614,69 @@ void oracle_gemm(const double *A, const double *B, int64_t M, int64_t N, int64_t
             absum[m * N + n] = a;
         }
     }
+}
+
+/* ------------------------------------------------------------------ */
+/* PTQ weight scales by minimum squared error ([SL-4.2]).                */
+/* ------------------------------------------------------------------ */
+
+/* Reading R16: [SL-4.2] calibrates the per-block weight scales of the NVFP4
+ * PTQ checkpoint by minimising the weight MSE instead of taking them from
+ * the block maximum.  Here: 1x16 blocks along the row, the tensor scale of
+ * R1 from the tensor amax.  A block whose largest magnitude is 0 gets scale
+ * 0 (R2).  Otherwise every finite positive E4M3 code c = 1 .. 126 is tried:
+ * codes q_j = E2M1_RNE(x_j * (S_enc / e4m3(c))) (R3) and the FP32 error
+ *     err_c = sum over j = 0 .. 15, in order, of d_j * d_j,
+ *     d_j = x_j - value(q_j) * step_c,  step_c = e4m3(c) * dec  (dec of R1),
+ * every product and sum one FP32 rounding; the block takes the c with the
+ * smallest err_c, the largest such c on ties, and its codes. */
+static uint8_t mse_block(const float *x, float s_enc, float dec, uint8_t *codes)
+{
+    float bamax = 0.0f, best = 0.0f;
+    int j, c, bestc = 0;
+    for (j = 0; j < 16; ++j) if (fabsf(x[j]) > bamax) bamax = fabsf(x[j]);
+    if (bamax == 0.0f) { for (j = 0; j < 16; ++j) codes[j] = 0; return 0; }
+    for (c = 1; c <= 126; ++c) {
+        const float sc = (float)oracle_e4m3_value(c);
+        const float r = s_enc / sc;
+        const float step = sc * dec;
+        float err = 0.0f;
+        for (j = 0; j < 16; ++j) {
+            const int q = oracle_e2m1_rne(x[j] * r);
+            const float rec = (float)oracle_e2m1_value(q) * step;
+            const float d = x[j] - rec;
+            const float d2 = d * d;
+            err = err + d2;
+        }
+        if (bestc == 0 || err <= best) { best = err; bestc = c; }
+    }
+    {
+        const float r = s_enc / (float)oracle_e4m3_value(bestc);
+        for (j = 0; j < 16; ++j) codes[j] = (uint8_t)oracle_e2m1_rne(x[j] * r);
+    }
+    return (uint8_t)bestc;
+}
+
+void oracle_quantize_1d_mse(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld,
+                            const float *amax_in, uint8_t *codes, uint8_t *sf, float *amax_out)
+{
+    const float amax = amax_in ? *amax_in : oracle_amax_bf16(x, rows, cols, ld);
+    const float s_enc = oracle_tensor_scale(amax), dec = oracle_tensor_decode_scale(amax);
+    int64_t r;
+    memset(sf, 0, oracle_sf_bytes(rows, cols));
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < rows; ++r) {
+        int64_t b;
+        for (b = 0; b < cols / 16; ++b) {
+            float blk[16];
+            uint8_t cd[16];
+            int j;
+            for (j = 0; j < 16; ++j) blk[j] = bf16_to_float(x[r * ld + b * 16 + j]);
+            sf[oracle_sf_offset(r, b, cols)] = mse_block(blk, s_enc, dec, cd);
+            for (j = 0; j < 16; ++j) put_code(codes, r, b * 16 + j, cols, cd[j]);
+        }
+    }
+    *amax_out = amax;
 }
 
 /* ------------------------------------------------------------------ */

@@ -525,3 +525,61 @@ def test_fp16_sr_threshold_and_special_values(orc):
     xs = np.linspace(-3, 3, 37).astype(np.float32) * 1.001
     got = orc.sr_fp16(xs, 99)
     assert all(got[e] == orc.fp16_sr(float(xs[e]), orc.sr_word(99, e)) for e in range(len(xs)))
+
+
+# ------------------------------------------------------------ PTQ block scales (reading R16)
+_E2M1 = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], dtype=np.float64)
+
+
+def _e2m1_rne_np(v):
+    """Nearest E2M1 magnitude code, ties to the even code, saturating at 6 (numpy, FP64)."""
+    m = np.minimum(np.abs(v), 6.0)
+    d = np.abs(m[..., None] - _E2M1[None, :])
+    best = d.min(axis=-1, keepdims=True)
+    cand = np.where(np.isclose(d, best, rtol=0, atol=0), np.arange(8)[None, :], 99)
+    even = np.where(cand % 2 == 0, cand, 99).min(axis=-1)
+    anyc = cand.min(axis=-1)
+    return np.where((cand < 99).sum(axis=-1) > 1, even, anyc)
+
+
+def test_mse_block_scales_minimise_the_error(orc):
+    """Each block's scale has the least FP64 squared error over all 126
+    finite positive E4M3 scales (to FP32 rounding of the oracle's sums), never
+    more than the max-based scale's, its codes are the RNE codes at that scale,
+    and all-zero blocks keep scale 0."""
+    rng = np.random.default_rng(60)
+    rows, cols = 6, 64
+    xf = rng.standard_normal((rows, cols)) * np.exp(rng.uniform(-3, 3, (rows, 1)))
+    xf[0, :16] = 0.0                                                  # an all-zero block
+    xf[1, 16] = 40.0                                                  # an outlier block
+    x = _bf16(xf)
+    q = orc.quantize_1d_mse(x)
+    ref = orc.quantize_1d(x)
+    xv = x.double().numpy()
+    amax = float(np.abs(xv).max())
+    s_enc = orc.tensor_scale(amax)
+    dec = orc.decode_scale(amax)
+    e4m3 = torch.arange(127, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    codes = _unpack(q["codes"], cols)
+    differs = 0
+    for r in range(rows):
+        for b in range(cols // 16):
+            blk = xv[r, 16 * b:16 * b + 16]
+            c = int(q["sf"][orc.sf_offset(r, b, cols)])
+            if not blk.any():
+                assert c == 0 and not codes[r, 16 * b:16 * b + 16].any()
+                continue
+            errs = {}
+            for cc in range(1, 127):
+                rq = np.float32(s_enc) / np.float32(e4m3[cc])
+                k = _e2m1_rne_np(blk * float(rq))
+                rec = np.sign(blk) * _E2M1[k] * (e4m3[cc] * dec)
+                errs[cc] = float(((blk - rec) ** 2).sum())
+            best = min(errs.values())
+            assert errs[c] <= best * (1 + 1e-5) + 1e-30, (r, b, c, errs[c], best)
+            c_max = int(ref["sf"][orc.sf_offset(r, b, cols)])
+            assert errs[c] <= errs[c_max] * (1 + 1e-5) + 1e-30
+            differs += c != c_max
+            kk = _e2m1_rne_np(blk * float(np.float32(s_enc) / np.float32(e4m3[c])))
+            assert ((codes[r, 16 * b:16 * b + 16] & 7) == kk).all()
+    assert differs > 0                                               # the search does change scales
