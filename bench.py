@@ -540,6 +540,21 @@ def measure_next_rows(wk: Workload, hbm_gbs: float, fp4_peak: float, iters: int 
         else:
             gbs = work / (ms * 1e-3) / 1e9
             out[name] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4)}
+    # PTQ block scales by minimum squared error (next row f3) on the in_proj weight
+    qptq = B.empty_qtensor(wk.dense.out, wk.dense.hidden, dev)
+    B.quantize_1d_mse(wk.w, amax_in=wk.qw.amax, out=qptq)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    B.quantize_1d_mse(wk.w, amax_in=wk.qw.amax, out=qptq)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    nel = wk.dense.out * wk.dense.hidden
+    out["quantize_1d_mse W (PTQ scales, 126 trial scales per block)"] = {
+        "ms": round(ms, 4), "gbs": round(2.5625 * nel / (ms * 1e-3) / 1e9, 1),
+        "g_elements_per_s": round(nel / (ms * 1e-3) / 1e9, 2)}
+    del qptq
     # FP16 SR of an SSM cache (next row f4): 256 sequences x 256 heads x 64 x state 128, FP32 in
     ssm = torch.randn(256 * 256 * 64 * 128, device=dev)
     ssm16 = torch.empty(ssm.numel(), dtype=torch.float16, device=dev)

@@ -239,6 +239,21 @@ nvfp4_status nvfp4_rht_quantize(const void *x, int64_t tokens, int64_t cols, int
                                 const float *amax_in, nvfp4_tensor *out_t,
                                 nvfp4_stream_t stream);
 
+/* 1x16 quantisation with block scales calibrated by minimum squared error:
+ * the weight scales of the NVFP4 PTQ checkpoint (Super summary section 4.2:
+ * per-block weight scales chosen to minimise the weight MSE rather than from
+ * the block maximum).  x: bf16 [rows, cols] (cols % 16 == 0, row stride
+ * ld % 8 == 0, 16-byte aligned); out as for nvfp4_quantize_1d (RNE codes,
+ * GEMM-ready scales, amax).
+ * The tensor scale is the usual 2688 / amax (amax computed, or amax_in).  A
+ * block whose largest magnitude is 0 gets scale 0; otherwise every finite
+ * positive E4M3 scale is tried and the block keeps the one with the smallest
+ * FP32 squared error sum_j (x_j - value(q_j) * e4m3(c) * dec)^2 (summed in
+ * element order; the larger scale on ties).  Offline work: 126 trial
+ * encodings per block. */
+nvfp4_status nvfp4_quantize_1d_mse(const void *x, int64_t rows, int64_t cols, int64_t ld,
+                                   const float *amax_in, nvfp4_tensor *out, nvfp4_stream_t stream);
+
 /* FP32 -> FP16 with stochastic rounding: the Mamba SSM-cache recipe of the
  * Super summary (section 4.3: FP16 cache, stochastic rounding driven by
  * Philox with 5 rounds).  x: device FP32 [n] (4-byte aligned); out: device

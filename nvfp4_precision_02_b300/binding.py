@@ -32,7 +32,7 @@ EXPORTS = ["nvfp4_sf_bytes", "nvfp4_sf_bytes_grouped", "nvfp4_sf_offset", "nvfp4
            "nvfp4_quantize_1d", "nvfp4_quantize_1d_grouped", "nvfp4_quantize_2d",
            "nvfp4_quantize_2d_fused_workspace", "nvfp4_quantize_2d_fused", "nvfp4_quantize_2d_fused_static",
            "nvfp4_rht_amax",
-           "nvfp4_rht_quantize", "nvfp4_sr_fp16", "nvfp4_group_k_capacity", "nvfp4_rht_quantize_grouped", "nvfp4_gemm",
+           "nvfp4_rht_quantize", "nvfp4_quantize_1d_mse", "nvfp4_sr_fp16", "nvfp4_group_k_capacity", "nvfp4_rht_quantize_grouped", "nvfp4_gemm",
            "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_k", "nvfp4_status_string",
            "nvfp4_last_error", "nvfp4_device_status", "nvfp4_launch_count", "nvfp4_debug_inject",
            "nvfp4_debug_wait_timeout"]
@@ -81,6 +81,7 @@ def lib():
             "nvfp4_grouped_gemm": (st, [TP, P, i32, TP, i64, P, i64, ctypes.c_int, P, P]),
             "nvfp4_group_k_capacity": (i64, [i64, i32]),
             "nvfp4_sr_fp16": (st, [P, i64, ctypes.c_uint64, P, P]),
+            "nvfp4_quantize_1d_mse": (st, [P, i64, i64, i64, P, TP, P]),
             "nvfp4_rht_quantize_grouped": (st, [P, i64, i64, i64, P, i32, i64, ctypes.c_uint16, ctypes.c_int,
                                                 ctypes.c_uint64, P, TP, P]),
             "nvfp4_grouped_gemm_k": (st, [TP, TP, P, i32, P, i64, ctypes.c_int, P, P]),
@@ -272,6 +273,16 @@ def rht_quantize(x: torch.Tensor, sign_mask: int, mode: int = RNE, seed: int = 0
     co = out.c()
     _check(lib().nvfp4_rht_quantize(_ptr(x), tokens, cols, ld, sign_mask, mode, seed, _ptr(amax_in),
                                     ctypes.byref(co), _stream(stream)))
+    return out
+
+
+def quantize_1d_mse(x: torch.Tensor, amax_in: Optional[torch.Tensor] = None, out: Optional[QTensor] = None,
+                    stream=None) -> QTensor:
+    """1x16 RNE quantisation with block scales chosen by minimum squared error (PTQ weights)."""
+    rows, cols, ld = _rows2d(x)
+    out = empty_qtensor(rows, cols, x.device) if out is None else out
+    co = out.c()
+    _check(lib().nvfp4_quantize_1d_mse(_ptr(x), rows, cols, ld, _ptr(amax_in), ctypes.byref(co), _stream(stream)))
     return out
 
 

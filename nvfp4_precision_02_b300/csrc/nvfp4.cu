@@ -487,6 +487,38 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t tokens, int64_t cols, int
     return NVFP4_OK;
 }
 
+nvfp4_status nvfp4_quantize_1d_mse(const void* x, int64_t rows, int64_t cols, int64_t ld, const float* amax_in,
+                                   nvfp4_tensor* out, nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    NVFP4_TRY(check_input(x, rows, cols, ld, 16, "x"));       // 16-byte aligned rows (vector loads)
+    NVFP4_TRY(check_out(out, rows, cols, true, "out"));
+    int sms = 0;
+    NVFP4_TRY(check_device(&sms));
+    const float* am = amax_in;
+    float* copy = nullptr;
+    if (am == nullptr) {
+        NVFP4_TRY(cuda_call(cudaMemsetAsync(out->amax, 0, sizeof(float), stream), "memset amax"));
+        if (rows > 0 && cols > 0) {
+            k_amax<<<dim3(amax_blocks(rows * cols / 8), 1), 256, 0, stream>>>((const uint16_t*)x, rows, cols, ld, 0,
+                                                                           out->amax);
+            NVFP4_TRY(launched("k_amax"));
+        }
+        am = out->amax;
+    } else if (amax_in != out->amax) {
+        copy = out->amax;
+    }
+    NVFP4_TRY(cuda_call(cudaMemsetAsync(out->sf, 0, nvfp4_sf_bytes(rows, cols), stream), "memset sf"));
+    if (rows == 0 || cols == 0) {
+        if (copy) NVFP4_TRY(cuda_call(cudaMemcpyAsync(copy, amax_in, 4, cudaMemcpyDeviceToDevice, stream), "amax copy"));
+        return NVFP4_OK;
+    }
+    const int64_t blocks = rows * (cols / 16);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(blocks, 256), (int64_t)sms * 16));
+    k_quant1d_mse<<<grid, 256, 0, stream>>>((const uint16_t*)x, rows, cols, ld, am, (uint8_t*)out->codes, out->sf,
+                                            copy);
+    return launched("k_quant1d_mse");
+}
+
 nvfp4_status nvfp4_sr_fp16(const float* x, int64_t n, uint64_t seed, uint16_t* out, nvfp4_stream_t stream) {
     NVFP4_INJECT_CHECK();
     if (n < 0) return fail(NVFP4_ERR_SHAPE, "n < 0");

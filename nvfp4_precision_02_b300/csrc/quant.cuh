@@ -631,6 +631,94 @@ __global__ void __launch_bounds__(Q2F_THREADS, 2) k_quant2d_fused(const uint16_t
     if (red_e >= 0) publish();
 }
 
+// ------------------------------------------------------------------ PTQ scales
+// 1x16 quantisation with each block's E4M3 scale chosen by minimum squared
+// error (the NVFP4 PTQ recipe of the "Nemotron 3 Super" summary,
+// papers.lianghsun.dev, section 4.2: weight scales calibrated by weight MSE,
+// not by the block maximum).  A block whose largest magnitude is 0 gets scale
+// 0; otherwise every finite positive E4M3 code c = 1 .. 126 is tried: codes
+// q_j = E2M1_RNE(x_j * (S_enc / e4m3(c))) and the FP32 error
+// sum_j (x_j - value(q_j) * (e4m3(c) * dec))^2, summed in element order with
+// one rounding per operation; the smallest error wins, the largest c on ties.
+// One thread per block (its 16 values in registers); the per-code element
+// multipliers and reconstruction steps are tables in shared memory.  The
+// scale buffer must be zero on entry (its padding stays zero).
+
+// FP32 value of an E2M1 code (sign in bit 3).
+__device__ __forceinline__ float e2m1_code_value(uint32_t code) {
+    const uint32_t m = code & 7u, e = m >> 1;
+    const uint32_t fb = e ? (((e + 126u) << 23) | ((m & 1u) << 22)) : ((m & 1u) ? 0x3F000000u : 0u);
+    return __uint_as_float(fb | ((code & 8u) << 28));
+}
+
+__global__ void __launch_bounds__(256) k_quant1d_mse(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                                                     int64_t ld, const float* __restrict__ amax,
+                                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                                     float* __restrict__ amax_copy) {
+    __shared__ float s_ratio[128], s_step[128];
+    const float s_enc = tensor_encode_scale(amax[0]);
+    const float dec = tensor_decode_scale(amax[0]);
+    if (threadIdx.x >= 1 && threadIdx.x <= 126) {
+        const float e = e4m3_to_float(threadIdx.x);
+        s_ratio[threadIdx.x] = __fdiv_rn(s_enc, e);
+        s_step[threadIdx.x] = __fmul_rn(e, dec);
+    }
+    if (amax_copy != nullptr && blockIdx.x == 0 && threadIdx.x == 0) amax_copy[0] = amax[0];
+    __syncthreads();
+    const int64_t nb = cols >> 4, total = rows * nb;
+    const bool vec = ((ld & 7) == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / nb, b = i - r * nb;
+        const uint16_t* src = x + r * ld + 16 * b;
+        float xv[16];
+        if (vec) {
+            const uint4 a0 = __ldg(reinterpret_cast<const uint4*>(src));
+            const uint4 a1 = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+            const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) { xv[2 * j] = bf16_lo(w[j]); xv[2 * j + 1] = bf16_hi(w[j]); }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xv[j] = __uint_as_float((uint32_t)__ldg(src + j) << 16);
+        }
+        float bamax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) bamax = fmaxf(bamax, fabsf(xv[j]));
+        uint32_t bestc = 0;
+        if (bamax != 0.0f) {
+            float best = 0.0f;
+            for (uint32_t c = 1; c <= 126; ++c) {
+                const float rc = s_ratio[c], st = s_step[c];
+                float f[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[j] = __fmul_rn(xv[j], rc);
+                const float lo8[8] = {f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]};
+                const float hi8[8] = {f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]};
+                const uint32_t q0 = e2m1x8_rne(lo8), q1 = e2m1x8_rne(hi8);
+                float err = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t q = ((j < 8 ? q0 : q1) >> (4 * (j & 7))) & 15u;
+                    const float d = __fsub_rn(xv[j], __fmul_rn(e2m1_code_value(q), st));
+                    err = __fadd_rn(err, __fmul_rn(d, d));
+                }
+                if (bestc == 0 || err <= best) { best = err; bestc = c; }
+            }
+        }
+        uint2 cw = make_uint2(0u, 0u);
+        if (bestc != 0) {
+            const float rc = s_ratio[bestc];
+            float lo8[8], hi8[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) { lo8[j] = __fmul_rn(xv[j], rc); hi8[j] = __fmul_rn(xv[8 + j], rc); }
+            cw = make_uint2(e2m1x8_rne(lo8), e2m1x8_rne(hi8));
+        }
+        // a code row is cols/2 bytes (a multiple of 8): 8-byte stores are aligned
+        *reinterpret_cast<uint2*>(codes + r * (cols >> 1) + 8 * b) = cw;
+        sf[sf_offset(r, b, cols)] = (uint8_t)bestc;
+    }
+}
+
 // ------------------------------------------------------------------ FP16 SR
 // FP32 -> FP16 with stochastic rounding by the Philox-5 word of each element
 // (the SSM-cache recipe of the "Nemotron 3 Super" summary, papers.lianghsun.dev,

@@ -241,3 +241,24 @@ def test_sr_fp16(B, orc, n):
         torch.cuda.synchronize()
         assert (got1.cpu().numpy().view(np.uint16) == orc.sr_fp16(x[1:], 0xC0FFEE)).all()
     assert B.device_status() == 0
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 16), (37, 64), (300, 1040)])
+def test_quantize_1d_mse(B, orc, rows, cols):
+    """PTQ block scales by minimum squared error: codes and scales equal the
+    oracle's bytes (all 126 scales tried per block), including an all-zero
+    block and outlier blocks; supplied amax gives the same bytes."""
+    g = torch.Generator().manual_seed(rows * 13 + cols)
+    x = torch.randn(rows, cols, generator=g) * torch.exp(torch.rand(rows, 1, generator=g) * 6 - 3)
+    x[0, :16] = 0.0
+    if cols >= 64:
+        x[rows // 2, 20] = 50.0
+    x = x.to(torch.bfloat16)
+    q = B.quantize_1d_mse(x.cuda())
+    torch.cuda.synchronize()
+    ref = orc.quantize_1d_mse(x)
+    _same(q, ref, rows, cols)
+    q2 = B.quantize_1d_mse(x.cuda(), amax_in=q.amax.clone())
+    torch.cuda.synchronize()
+    _same(q2, ref, rows, cols)
+    assert B.device_status() == 0
