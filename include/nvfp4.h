@@ -226,6 +226,20 @@ nvfp4_status nvfp4_quantize_2d_fused_static(const void *w, int64_t batch, int64_
 nvfp4_status nvfp4_rht_amax(const void *x, int64_t tokens, int64_t cols, int64_t ld,
                             uint16_t sign_mask, float *amax, nvfp4_stream_t stream);
 
+/* Both tensor amaxes of a gradient in one read: amax_plain = max |x| (the
+ * 1x16 SR quantiser of dgrad) and amax_rht = max |RHT(x)| along tokens (the
+ * RHT quantiser of wgrad), x: bf16 [tokens, cols], tokens % 16 == 0.  Each
+ * result is the one nvfp4_amax / nvfp4_rht_amax would give; pass them as
+ * amax_in.  amax_plain, amax_rht: device, 1 float each, zeroed by the call. */
+nvfp4_status nvfp4_dual_amax(const void *x, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask,
+                             float *amax_plain, float *amax_rht, nvfp4_stream_t stream);
+
+/* Number of E2M1 codes of magnitude zero (+0 and -0) in a quantised tensor
+ * (rows * cols codes): the zero-gradient fraction the pages monitor (Super
+ * summary "Infra design"; section 2.2: small gradients underflow to zero).
+ * count: device, one 64-bit word, zeroed by the call.  codes 16-byte aligned. */
+nvfp4_status nvfp4_count_zero_codes(const nvfp4_tensor *t, uint64_t *count, nvfp4_stream_t stream);
+
 /* RHT + 1D quantisation of a wgrad input (Super summary "Infra design";
  * Ultra report 2.2: RHT on the inputs of wgrad).  x: bf16 [tokens, cols],
  * row stride ld, tokens % 16 == 0.  The transform runs along tokens (the

@@ -32,7 +32,7 @@ EXPORTS = ["nvfp4_sf_bytes", "nvfp4_sf_bytes_grouped", "nvfp4_sf_offset", "nvfp4
            "nvfp4_quantize_1d", "nvfp4_quantize_1d_grouped", "nvfp4_quantize_2d",
            "nvfp4_quantize_2d_fused_workspace", "nvfp4_quantize_2d_fused", "nvfp4_quantize_2d_fused_static",
            "nvfp4_rht_amax",
-           "nvfp4_rht_quantize", "nvfp4_quantize_1d_mse", "nvfp4_sr_fp16", "nvfp4_group_k_capacity", "nvfp4_rht_quantize_grouped", "nvfp4_gemm",
+           "nvfp4_rht_quantize", "nvfp4_dual_amax", "nvfp4_count_zero_codes", "nvfp4_quantize_1d_mse", "nvfp4_sr_fp16", "nvfp4_group_k_capacity", "nvfp4_rht_quantize_grouped", "nvfp4_gemm",
            "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_k", "nvfp4_status_string",
            "nvfp4_last_error", "nvfp4_device_status", "nvfp4_launch_count", "nvfp4_debug_inject",
            "nvfp4_debug_wait_timeout"]
@@ -82,6 +82,8 @@ def lib():
             "nvfp4_group_k_capacity": (i64, [i64, i32]),
             "nvfp4_sr_fp16": (st, [P, i64, ctypes.c_uint64, P, P]),
             "nvfp4_quantize_1d_mse": (st, [P, i64, i64, i64, P, TP, P]),
+            "nvfp4_dual_amax": (st, [P, i64, i64, i64, ctypes.c_uint16, P, P, P]),
+            "nvfp4_count_zero_codes": (st, [TP, P, P]),
             "nvfp4_rht_quantize_grouped": (st, [P, i64, i64, i64, P, i32, i64, ctypes.c_uint16, ctypes.c_int,
                                                 ctypes.c_uint64, P, TP, P]),
             "nvfp4_grouped_gemm_k": (st, [TP, TP, P, i32, P, i64, ctypes.c_int, P, P]),
@@ -273,6 +275,24 @@ def rht_quantize(x: torch.Tensor, sign_mask: int, mode: int = RNE, seed: int = 0
     co = out.c()
     _check(lib().nvfp4_rht_quantize(_ptr(x), tokens, cols, ld, sign_mask, mode, seed, _ptr(amax_in),
                                     ctypes.byref(co), _stream(stream)))
+    return out
+
+
+def dual_amax(x: torch.Tensor, sign_mask: int, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """x: bf16 [tokens, cols] -> float32 [2]: (max |x|, max |RHT(x)|) from one read."""
+    tokens, cols, ld = _rows2d(x)
+    out = torch.empty(2, dtype=torch.float32, device=x.device) if out is None else out
+    assert out.dtype == torch.float32 and out.numel() >= 2
+    _check(lib().nvfp4_dual_amax(_ptr(x), tokens, cols, ld, sign_mask, _ptr(out), ctypes.c_void_p(out.data_ptr() + 4),
+                                 _stream(stream)))
+    return out
+
+
+def count_zero_codes(q: QTensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Number of zero-magnitude codes of a quantised tensor (int64 [1], on the device)."""
+    out = torch.empty(1, dtype=torch.int64, device=q.codes.device) if out is None else out
+    cq = q.c()
+    _check(lib().nvfp4_count_zero_codes(ctypes.byref(cq), _ptr(out), _stream(stream)))
     return out
 
 

@@ -445,6 +445,39 @@ nvfp4_status nvfp4_rht_amax(const void* x, int64_t tokens, int64_t cols, int64_t
     return launched("k_rht amax");
 }
 
+nvfp4_status nvfp4_dual_amax(const void* x, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask,
+                             float* amax_plain, float* amax_rht, nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    if (amax_plain == nullptr || amax_rht == nullptr) return fail(NVFP4_ERR_NULL, "amax_plain or amax_rht is NULL");
+    NVFP4_TRY(check_input(x, tokens, cols, ld, 1, "x", false));
+    if (tokens % 16 != 0) return fail(NVFP4_ERR_SHAPE, "tokens=%lld is not a multiple of 16", (long long)tokens);
+    if (cdiv(tokens, 64) > 65535) return fail(NVFP4_ERR_LIMIT, "tokens too large");
+    NVFP4_TRY(check_device());
+    NVFP4_TRY(cuda_call(cudaMemsetAsync(amax_plain, 0, sizeof(float), stream), "memset amax"));
+    NVFP4_TRY(cuda_call(cudaMemsetAsync(amax_rht, 0, sizeof(float), stream), "memset amax"));
+    if (tokens == 0 || cols == 0) return NVFP4_OK;
+    k_rht<3><<<dim3((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64)), 256, 0, stream>>>(
+        (const uint16_t*)x, tokens, cols, ld, sign_mask, amax_rht, 0, nullptr, nullptr, amax_plain);
+    return launched("k_rht dual amax");
+}
+
+nvfp4_status nvfp4_count_zero_codes(const nvfp4_tensor* t, uint64_t* count, nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    if (t == nullptr || count == nullptr) return fail(NVFP4_ERR_NULL, "t or count is NULL");
+    if (t->rows < 0 || t->cols < 0 || (t->cols & 1)) return fail(NVFP4_ERR_SHAPE, "bad tensor shape");
+    if (((uintptr_t)count & 7u) != 0) return fail(NVFP4_ERR_ALIGN, "count not 8-byte aligned");
+    int sms = 0;
+    NVFP4_TRY(check_device(&sms));
+    NVFP4_TRY(cuda_call(cudaMemsetAsync(count, 0, sizeof(uint64_t), stream), "memset count"));
+    const int64_t nbytes = t->rows * (t->cols / 2);
+    if (nbytes == 0) return NVFP4_OK;
+    if (t->codes == nullptr || !aligned16(t->codes)) return fail(NVFP4_ERR_ALIGN, "codes NULL or not 16-byte aligned");
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(nbytes, 256 * 16), (int64_t)sms * 8));
+    k_count_zero_codes<<<grid, 256, 0, stream>>>((const uint8_t*)t->codes, nbytes,
+                                                 reinterpret_cast<unsigned long long*>(count));
+    return launched("k_count_zero_codes");
+}
+
 nvfp4_status nvfp4_rht_quantize(const void* x, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask,
                                 nvfp4_round mode, uint64_t seed, const float* amax_in, nvfp4_tensor* out_t,
                                 nvfp4_stream_t stream) {

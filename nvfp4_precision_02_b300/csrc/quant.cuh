@@ -631,6 +631,33 @@ __global__ void __launch_bounds__(Q2F_THREADS, 2) k_quant2d_fused(const uint16_t
     if (red_e >= 0) publish();
 }
 
+// ------------------------------------------------------------------ zero codes
+// Number of E2M1 codes of magnitude 0 (+0 and -0) among n packed bytes:
+// for a nibble value v in 0..7 (sign dropped), v + 7 sets the nibble's bit 3
+// exactly when v != 0 and never carries into the next nibble, so the zero
+// nibbles are the clear bits 3 of (w & 0x77777777) + 0x77777777.  count
+// must be zero on entry.
+__device__ __forceinline__ uint32_t zero_nibbles(uint32_t w) {
+    return __popc(~((w & 0x77777777u) + 0x77777777u) & 0x88888888u);
+}
+
+__global__ void __launch_bounds__(256) k_count_zero_codes(const uint8_t* __restrict__ codes, int64_t nbytes,
+                                                          unsigned long long* __restrict__ count) {
+    unsigned long long c = 0;
+    const int64_t nv = nbytes >> 4;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x, nt = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = tid; i < nv; i += nt) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(codes) + i);
+        c += zero_nibbles(v.x) + zero_nibbles(v.y) + zero_nibbles(v.z) + zero_nibbles(v.w);
+    }
+    for (int64_t i = (nv << 4) + tid; i < nbytes; i += nt) {
+        const uint32_t b = codes[i];
+        c += ((b & 7u) == 0u) + (((b >> 4) & 7u) == 0u);
+    }
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+    if ((threadIdx.x & 31) == 0 && c != 0) atomicAdd(count, c);
+}
+
 // ------------------------------------------------------------------ PTQ scales
 // 1x16 quantisation with each block's E4M3 scale chosen by minimum squared
 // error (the NVFP4 PTQ recipe of the "Nemotron 3 Super" summary,
@@ -847,7 +874,7 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
         nvalid = left < 0 ? 0 : (left > 64 ? 64 : (int)left);
         nchunks = 4;
     } else {
-        if (MODE != 0 && amax_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
+        if (MODE != 0 && MODE != 3 && amax_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
             amax_copy[0] = amax[0];
         const int64_t left16 = (tokens - t0) >> 4;
         nchunks = left16 < 4 ? (int)left16 : 4;
@@ -879,19 +906,30 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
     __syncthreads();
     const int64_t c = c0 + tid;
     const bool active = c < cols;
-    if (MODE == 0) {
-        float m = 0.0f;
+    if (MODE == 0 || MODE == 3) {
+        // MODE 3 also takes the plain max |x| of the same values (one read
+        // gives both tensor amaxes of dY: the row quantiser's and the RHT's);
+        // amax_copy then receives the plain one
+        float m = 0.0f, mp = 0.0f;
         if (active) {
             for (int j = 0; j < nchunks; ++j) {
                 float v[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[16 * j + i][tid] << 16);
+                if (MODE == 3) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) mp = fmaxf(mp, fabsf(v[i]));
+                }
                 rht16(v, sign_mask);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
             }
         }
         block_max_atomic(__float_as_uint(m), amax + g);
+        if (MODE == 3) {
+            __syncthreads();                    // the reduction buffer is shared by both calls
+            block_max_atomic(__float_as_uint(mp), amax_copy);
+        }
         return;
     }
     if (!active) return;

@@ -262,3 +262,25 @@ def test_quantize_1d_mse(B, orc, rows, cols):
     torch.cuda.synchronize()
     _same(q2, ref, rows, cols)
     assert B.device_status() == 0
+
+
+@pytest.mark.parametrize("tokens,cols", [(16, 1), (80, 130), (1024, 300)])
+def test_dual_amax_and_zero_code_count(B, orc, tokens, cols):
+    """One read gives both tensor amaxes of a gradient (plain and after the
+    RHT), each equal to the oracle's; the zero-code count of the SR-quantised
+    gradient equals the count of zero-magnitude codes in the oracle's bytes."""
+    x = _x(tokens, cols, seed=tokens + cols, scale=1e-3, spread=6.0)
+    mask = 0x51C3
+    a = B.dual_amax(x.cuda(), mask)
+    torch.cuda.synchronize()
+    got = np_u8(a)
+    assert got[0] == np.float32(orc.amax(x)) and got[1] == np.float32(orc.rht_amax(x, mask))
+    if cols % 16 == 0:
+        q = B.quantize_1d(x.cuda(), mode=1, seed=3, amax_in=a[:1])
+        n0 = B.count_zero_codes(q)
+        torch.cuda.synchronize()
+        ref = orc.quantize_1d(x, mode=1, seed=3, amax_in=float(got[0]))
+        codes = ref["codes"]
+        want = int(((codes & 7) == 0).sum() + (((codes >> 4) & 7) == 0).sum())
+        assert int(n0.item()) == want
+    assert B.device_status() == 0
