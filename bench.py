@@ -56,24 +56,35 @@ def parse():
 GEMM_SOURCES = ("nvfp4_precision_02_b300/csrc/gemm.cuh",)
 
 
+def code_text(src: str) -> str:
+    """The code of a C/CUDA source without its comments and with whitespace
+    runs folded, so that editing a comment does not detach a profile from the
+    code it measured.  (String literals of the kernel sources hold no comment
+    markers.)"""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def source_hash(paths=GEMM_SOURCES) -> str:
     h = hashlib.sha256()
     for f in paths:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f)) as fh:
+            h.update(code_text(fh.read()).encode())
     return h.hexdigest()
 
 
 def profiled_traffic(summary: str):
     """DRAM bytes per launch from a committed ncu summary (lines
-    `dram_bytes_per_launch: N` and `kernel_source_sha256: H`), or None when the
-    summary is missing or the kernel sources changed after the capture."""
+    `dram_bytes_per_launch: N` and `kernel_code_sha256: H`, the hash of the
+    kernel source's code without comments), or None when the summary is
+    missing or the kernel code changed after the capture."""
     path = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(path):
         return None
     text = open(path).read()
     b = re.search(r"dram_bytes_per_launch:\s*(\d+)", text)
-    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    h = re.search(r"kernel_code_sha256:\s*([0-9a-f]{64})", text)
     if not b or not h or h.group(1) != source_hash():
         return None
     return int(b.group(1))

@@ -47,6 +47,12 @@
 //   rank 0's barriers, and rank 0's commits arrive on the barriers of both.
 //   The second m-tile of a pair may lie past its group's end: it is computed
 //   and not stored.
+// Groups along K (KGROUP, a compile-time variant; the wgrad of the expert
+// GEMMs): every group has all m-tiles of the shared M rows x all n-tiles; a
+// tile's K slice is the group's 64-padded token segment (TMA boxes at its
+// byte column, scale atoms at its atom column, a partial last stage issuing
+// fewer MMAs), its C rows start at g * M, and a group without tokens issues
+// no MMA and stores zeros.
 // Every wait is bounded (DEV_TIMEOUT in the status word, then a clean exit).
 #pragma once
 

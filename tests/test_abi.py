@@ -122,3 +122,35 @@ def test_status_strings(L):
     for s in range(8):
         assert L.nvfp4_status_string(s)
     assert L.nvfp4_status_string(0) == b"ok"
+
+
+def test_backward_and_next_row_entry_points_validation(L):
+    """Argument checks of the grouped backward, PTQ, FP16 SR and monitoring
+    entry points come before any device access."""
+    # capacity of the expert-segmented operand: every split fits
+    assert L.nvfp4_group_k_capacity(1000, 7) == ((1000 + 63 * 7 + 63) // 64) * 64
+    assert L.nvfp4_group_k_capacity(0, 1) == 64 and L.nvfp4_group_k_capacity(5, 0) == 0
+    cap = L.nvfp4_group_k_capacity(100, 4)
+    g = L.nvfp4_rht_quantize_grouped
+    assert g(FAKE, 100, 48, 48, None, 4, cap, 0, 0, 0, None, ctypes.byref(_t(48, cap)), None) == 1     # NULL offsets
+    assert g(FAKE, 100, 48, 48, FAKE, 0, cap, 0, 0, 0, None, ctypes.byref(_t(48, cap)), None) == 7     # no groups
+    assert g(FAKE, 100, 48, 48, FAKE, 4, cap - 64, 0, 0, 0, None, ctypes.byref(_t(48, cap - 64)), None) == 2
+    assert g(FAKE, 100, 48, 48, FAKE, 4, cap + 32, 0, 0, 0, None, ctypes.byref(_t(48, cap + 32)), None) == 2
+    assert g(FAKE, 100, 48, 48, FAKE, 4, cap, 0, 7, 0, None, ctypes.byref(_t(48, cap)), None) == 2     # bad mode
+    k = L.nvfp4_grouped_gemm_k
+    assert k(ctypes.byref(_t(64, 96)), ctypes.byref(_t(64, 96)), FAKE, 2, FAKE, 64, 0, None, None) == 2  # K % 64
+    assert k(ctypes.byref(_t(64, 128)), ctypes.byref(_t(64, 192)), FAKE, 2, FAKE, 64, 0, None, None) == 2
+    assert k(ctypes.byref(_t(64, 128)), ctypes.byref(_t(64, 128)), None, 2, FAKE, 64, 0, None, None) == 1
+    assert k(ctypes.byref(_t(64, 128)), ctypes.byref(_t(64, 128)), FAKE, 0, FAKE, 64, 0, None, None) == 7
+    assert k(ctypes.byref(_t(64, 128)), ctypes.byref(_t(64, 128)), FAKE, 2, FAKE, 32, 0, None, None) == 2  # ldc < N
+    s = L.nvfp4_sr_fp16
+    assert s(FAKE, -1, 0, FAKE, None) == 2 and s(None, 8, 0, FAKE, None) == 1 and s(FAKE, 8, 0, FAKE + 1, None) == 3
+    assert s(None, 0, 0, None, None) == 0                                                         # nothing to do
+    m = L.nvfp4_quantize_1d_mse
+    assert m(FAKE, 64, 24, 24, None, ctypes.byref(_t(64, 24)), None) == 2                          # cols % 16
+    assert m(FAKE + 8, 64, 32, 32, None, ctypes.byref(_t(64, 32)), None) == 3                      # misaligned rows
+    d = L.nvfp4_dual_amax
+    assert d(FAKE, 64, 32, 32, 0, None, FAKE, None) == 1 and d(FAKE, 60, 32, 32, 0, FAKE, FAKE, None) == 2
+    z = L.nvfp4_count_zero_codes
+    assert z(None, FAKE, None) == 1 and z(ctypes.byref(_t(4, 32)), None, None) == 1
+    assert z(ctypes.byref(_t(4, 32)), FAKE + 4, None) == 3                                        # count alignment
