@@ -230,29 +230,43 @@ class ClockSampler:
             self.proc.kill()
         self.f.flush()
         self.f.seek(0)
-        rows = [l.strip().split(", ") for l in self.f.read().splitlines() if l.strip()]
+        text = self.f.read()
         os.unlink(self.f.name)
-        sm = []
-        reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        smax = None
-        power = []
-        for r in rows:
-            if len(r) < 8:
-                continue
-            try:
-                sm.append(float(r[0]))
-                smax = float(r[1])
-                power.append(float(r[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, r[4:8]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power) if power else None}
+        return summarise_clocks(text)
+
+
+THROTTLE_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def summarise_clocks(text: str):
+    """Median SM clock, maximum SM clock, the throttle reasons seen Active and
+    the peak power from `nvidia-smi --query-gpu=<ClockSampler.FIELDS>
+    --format=csv,noheader,nounits` output; rows that do not parse are
+    skipped.  None when no row parses."""
+    sm, power = [], []
+    reasons = set()
+    smax = None
+    for line in text.splitlines():
+        r = [v.strip() for v in line.split(",")]
+        if len(r) < 8:
+            continue
+        try:
+            mhz, mx = float(r[0]), float(r[1])
+        except ValueError:
+            continue
+        sm.append(mhz)
+        smax = mx
+        try:
+            power.append(float(r[2]))
+        except ValueError:
+            pass
+        for n, v in zip(THROTTLE_NAMES, r[4:8]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+            "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
 # ---------------------------------------------------------------- CPU oracle timing

@@ -1,0 +1,103 @@
+"""Host-side logic of bench.py: the profile-to-code binding of the ncu
+traffic figure, the clock summary, and the JSON line of the reference arm
+(the CPU oracle), which needs no GPU."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_code_text_ignores_comments_and_whitespace():
+    a = "int f(int x) {  // twice\n  return 2 * x; /* doubled */\n}\n"
+    b = "/* header\n   comment */\nint f(int x) {\n\treturn 2 * x;\n}"
+    c = "int f(int x) { return 3 * x; }"
+    assert bench.code_text(a) == bench.code_text(b) == "int f(int x) { return 2 * x; }"
+    assert bench.code_text(c) != bench.code_text(a)
+
+
+def test_profiled_traffic_is_bound_to_the_kernel_code(tmp_path):
+    h = bench.source_hash()
+    good = tmp_path / "good.md"
+    good.write_text(f"x\ndram_bytes_per_launch: 123456\nkernel_code_sha256: {h}\n")
+    stale = tmp_path / "stale.md"
+    stale.write_text("dram_bytes_per_launch: 123456\nkernel_code_sha256: " + "0" * 64 + "\n")
+    partial = tmp_path / "partial.md"
+    partial.write_text(f"kernel_code_sha256: {h}\n")
+    assert bench.profiled_traffic(str(good)) == 123456
+    assert bench.profiled_traffic(str(stale)) is None
+    assert bench.profiled_traffic(str(partial)) is None
+    assert bench.profiled_traffic(str(tmp_path / "missing.md")) is None
+
+
+def test_committed_profile_parses():
+    """The committed fprop summary carries both keys the bench reads."""
+    text = open(os.path.join(ROOT, "profiles", "k_gemm_nvfp4_fprop_ultra.md")).read()
+    assert "dram_bytes_per_launch:" in text and "kernel_code_sha256:" in text
+
+
+def test_summarise_clocks():
+    rows = [
+        "1920, 2032, 1050.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "1905, 2032, 1099.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "garbage line",
+        "[N/A], 2032, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "1890, 2032, [N/A], 0x0000000000000008, Active, Not Active, Not Active, Not Active",
+    ]
+    s = bench.summarise_clocks("\n".join(rows))
+    assert s["samples"] == 3
+    assert s["sm_mhz"] == 1905 and s["sm_max_mhz"] == 2032
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert s["power_w_max"] == 1099.0
+    assert bench.summarise_clocks("") is None
+    assert bench.summarise_clocks("a, b, c\n") is None
+
+
+def test_workload_config_names_the_workload():
+    from nvfp4_precision_02_b300 import workloads as wl
+    m = wl.ULTRA_MOE
+    c = bench.workload_config("ultra", wl.ULTRA_DENSE, m, m.tokens * m.topk, 2)
+    assert c["workload"] == "ultra_full_step" and c["moe_rows"] == 360448
+    assert c["in_proj_out"] == 33024 and c["parallelism"] == "replicas x2"
+    assert "model" not in c
+
+
+def _run_bench(args, env_extra=None, timeout=300):
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, cwd=ROOT, env=env,
+                          capture_output=True, text=True, timeout=timeout)
+
+
+def test_reference_arm_json_line():
+    """`--impl reference` times the oracle on the host and prints one JSON
+    line with the contract's keys; value, cpu_baseline and e2e agree."""
+    r = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0", "--workload", "super"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"] == d["e2e"]["value"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "super_full_step"
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "0"],
+                   {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+if __name__ == "__main__":
+    sys.exit(pytest.main([__file__, "-q"]))
