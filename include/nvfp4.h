@@ -67,6 +67,12 @@
  *   and return instead of hanging.
  *   All device pointers must be 16-byte aligned; all leading dimensions are
  *   in elements and must make every row start 16-byte aligned.
+ *
+ * State kept by the library (all calls may come from any host thread):
+ *   a per-thread last-error string; a per-device cache of the device check
+ *   and kernel attributes (guarded by a mutex); a launch counter and a
+ *   one-shot failure-injection hook (atomics); in device memory, the status
+ *   word and the counters of nvfp4_quantize_2d_fused_static.
  */
 #ifndef NVFP4_H
 #define NVFP4_H
