@@ -33,15 +33,15 @@ def pack(codes) -> np.ndarray:
     return (c[0::2] | (c[1::2] << 4)).astype(np.uint8)
 
 
-def scale_rows(orc, sf: np.ndarray, rows, cols: int, base: int = 0) -> np.ndarray:
-    """Block scales [len(rows), cols/16] of the listed scale rows of a
-    swizzled buffer (atoms laid out for a [*, cols] operand, starting at byte
-    `base`)."""
-    nb = cols // 16
-    out = np.zeros((len(rows), nb), dtype=np.uint8)
+def scale_rows(orc, sf: np.ndarray, rows, cols: int, base: int = 0, b0: int = 0, b1=None) -> np.ndarray:
+    """Block scales [len(rows), b1-b0] (blocks b0 .. b1-1, all by default) of
+    the listed scale rows of a swizzled buffer (atoms laid out for a
+    [*, cols] operand, starting at byte `base`)."""
+    b1 = cols // 16 if b1 is None else b1
+    out = np.zeros((len(rows), b1 - b0), dtype=np.uint8)
     for i, r in enumerate(rows):
-        for b in range(nb):
-            out[i, b] = sf[base + orc.sf_offset(int(r), b, cols)]
+        for b in range(b0, b1):
+            out[i, b - b0] = sf[base + orc.sf_offset(int(r), b, cols)]
     return out
 
 
@@ -106,22 +106,34 @@ def rows_2d(orc, slab, row_ids, cols: int, amax: float) -> OracleRows:
 
 
 def rows_rht(orc, x_cols: np.ndarray, col_ids, tokens: int, amax: float, sign_mask: int, mode: int,
-             seed: int = 0) -> OracleRows:
+             seed: int = 0, index_stride: int = 0, index_offset: int = 0) -> OracleRows:
     """Rows `col_ids` of the RHT operand [cols, tokens] of x [tokens, cols]
     with RHT amax `amax`; x_cols: bf16 bits [tokens, n] of those columns.
     Each 16-token chunk is transformed and encoded as one block; the SR index
-    of output element (c, t) is c * tokens + t."""
+    of output element (c, t) is c * tokens + t, or c * index_stride +
+    index_offset + t for an expert segment placed at column index_offset of
+    an operand index_stride tokens wide."""
     out = OracleRows(len(col_ids), tokens, amax)
     s_enc = orc.tensor_scale(amax)
     xf = f32(x_cols)
+    stride = index_stride if index_stride else tokens
     for i, c in enumerate(col_ids):
         col = np.ascontiguousarray(xf[:, i])
         for t0 in range(0, tokens, 16):
             y = orc.rht16(col[t0:t0 + 16], sign_mask)
-            sfb, cd = orc.encode_block(y, s_enc, mode, seed, int(c) * tokens + t0)
+            sfb, cd = orc.encode_block(y, s_enc, mode, seed, int(c) * stride + index_offset + t0)
             out.scales[i, t0 // 16] = sfb
             out.codes[i, t0 // 2:t0 // 2 + 8] = pack(cd)
     return out
+
+
+def padded_segment(x_bits: np.ndarray, o0: int, o1: int, pad: int = 64) -> np.ndarray:
+    """Rows o0 .. o1-1 of x (bf16 bits) followed by zero rows up to a multiple of `pad`."""
+    n = o1 - o0
+    kp = (n + pad - 1) // pad * pad
+    seg = np.zeros((kp, x_bits.shape[1]), dtype=np.uint16)
+    seg[:n] = x_bits[o0:o1]
+    return seg
 
 
 def assert_rows_equal(name: str, orc_rows: OracleRows, gpu_codes: np.ndarray, gpu_scales: np.ndarray, row_ids):

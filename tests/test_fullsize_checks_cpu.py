@@ -36,11 +36,17 @@ def _deq(orc, q, rows, cols, amax, sf_row0=0, row_ids=None):
 
 
 class FakeB:
-    """The binding calls the full-size tests make, answered by the oracle."""
-    OUT_BF16 = 0
+    """The binding calls the full-size tests make, answered by the oracle.
+    A call named in `corrupt` returns a slightly wrong result."""
+    RNE, SR = 0, 1
+    OUT_BF16, OUT_FP32 = 0, 1
 
     def __init__(self, orc):
         self.orc = orc
+        self.corrupt = set()
+
+    def _bad(self, name, q):
+        return _flip_codes(q) if name in self.corrupt else q
 
     def sf_bytes(self, rows, cols):
         return self.orc.sf_bytes(rows, cols)
@@ -48,13 +54,58 @@ class FakeB:
     def device_status(self):
         return 0
 
-    def quantize_1d_grouped(self, x, offsets):
-        offs = offsets.numpy()
-        d = self.orc.quantize_1d_grouped(x, offs)
-        return _q(d, x.shape[0], x.shape[1])
+    def quantize_1d_grouped(self, x, offsets, mode=0, seed=0):
+        d = self.orc.quantize_1d_grouped(x, offsets.numpy(), mode=mode, seed=seed)
+        return self._bad("quantize_1d_grouped", _q(d, x.shape[0], x.shape[1]))
+
+    def quantize_2d(self, w, want_t=True):
+        d = self.orc.quantize_2d(w, want_t=want_t)
+        E, n, k = w.shape
+        qw = _q(d, n, k)
+        qt = _q(d, k, n, codes_key="codes_t", sf_key="sf_t") if want_t else None
+        return qw, self._bad("quantize_2d", qt) if want_t else None, None
 
     def grouped_gemm(self, qx, offsets, qw, n, out_dtype):
-        return _grouped(self.orc, qx, offsets.numpy(), qw, n)
+        out = _grouped(self.orc, qx, offsets.numpy(), qw, n)
+        return out * 1.01 if "grouped_gemm" in self.corrupt else out
+
+    def group_k_capacity(self, rows, groups):
+        return (rows + 63 * groups + 63) // 64 * 64
+
+    def rht_quantize_grouped(self, x, offsets, mask, mode, seed, kt):
+        d = self.orc.rht_quantize_grouped(x, offsets.numpy(), kt, mask, mode=mode, seed=seed)
+        q = _q(d, x.shape[1], kt)
+        return _flip_scales(q) if ("rht_quantize_grouped", mode) in self.corrupt else q
+
+    def grouped_gemm_k(self, qa, qb, offsets, out_dtype):
+        orc, offs = self.orc, offsets.numpy()
+        M, Nb, kt = qa.rows, qb.rows, qa.cols
+        out = torch.zeros((len(offs) - 1) * M, Nb, dtype=torch.float32)
+        for g in range(len(offs) - 1):
+            cnt = int(offs[g + 1] - offs[g])
+            if cnt == 0:
+                continue
+            ko, kp = orc.group_k_offset(offs, g), (cnt + 63) // 64 * 64
+            a = orc.dequantize_rows(qa.codes.numpy(), qa.sf.numpy(), kt, float(qa.amax[g]), np.arange(M))
+            b = orc.dequantize_rows(qb.codes.numpy(), qb.sf.numpy(), kt, float(qb.amax[g]), np.arange(Nb))
+            ref, _ = orc.gemm(a[:, ko:ko + kp], b[:, ko:ko + kp])
+            out[g * M:(g + 1) * M] = torch.from_numpy(ref)
+        return -out if "grouped_gemm_k" in self.corrupt else out
+
+    def quantize_1d_mse(self, w, amax_in):
+        q = _q(self.orc.quantize_1d_mse(w, amax_in=float(amax_in[0])), w.shape[0], w.shape[1])
+        return _flip_scales(q) if "quantize_1d_mse" in self.corrupt else q
+
+    def sr_fp16(self, x, seed):
+        b = self.orc.sr_fp16(x.numpy(), seed)
+        if "sr_fp16" in self.corrupt:
+            b = b ^ np.uint16(1)
+        return torch.from_numpy(b.view(np.float16))
+
+    def count_zero_codes(self, q):
+        c = q.codes.numpy()
+        n = int(((c & 7) == 0).sum()) + int((((c >> 4) & 7) == 0).sum())
+        return torch.tensor([n + ("count_zero_codes" in self.corrupt)], dtype=torch.int64)
 
 
 def _grouped(orc, qx, offs, qw, n):
@@ -114,12 +165,18 @@ def _fake_run(orc):
 
 
 TESTS = [full.test_fprop_full_size, full.test_dgrad_full_size, full.test_wgrad_full_size,
-         full.test_moe_up_full_size, full.test_moe_down_full_size]
+         full.test_moe_up_full_size, full.test_moe_down_full_size, full.test_expert_backward_full_size,
+         full.test_ptq_mse_scales_full_size, full.test_sr_fp16_full_size, full.test_zero_code_count_full_size]
 
 
 @pytest.fixture(scope="module")
 def fake(orc):
     return _fake_run(orc)
+
+
+@pytest.fixture(autouse=True)
+def small_ssm_cache(monkeypatch):
+    monkeypatch.setattr(full, "SSM_ELEMENTS", 6000)
 
 
 @pytest.mark.parametrize("test", TESTS, ids=lambda t: t.__name__)
@@ -156,6 +213,30 @@ PLANTS = [
     ("h", lambda y: y * 1.01, full.test_moe_up_full_size),
     ("qwd", _flip_codes, full.test_moe_down_full_size),
 ]
+
+
+CORRUPT = [
+    ("quantize_1d_grouped", full.test_expert_backward_full_size),
+    ("quantize_2d", full.test_expert_backward_full_size),
+    ("grouped_gemm", full.test_expert_backward_full_size),
+    (("rht_quantize_grouped", 0), full.test_expert_backward_full_size),
+    (("rht_quantize_grouped", 1), full.test_expert_backward_full_size),
+    ("grouped_gemm_k", full.test_expert_backward_full_size),
+    ("quantize_1d_mse", full.test_ptq_mse_scales_full_size),
+    ("sr_fp16", full.test_sr_fp16_full_size),
+    ("count_zero_codes", full.test_zero_code_count_full_size),
+]
+
+
+@pytest.mark.parametrize("call,test", CORRUPT, ids=[str(c[0]) for c in CORRUPT])
+def test_checks_reject_a_wrong_call_result(fake, orc, call, test):
+    fake.B.corrupt = {call}
+    fake.host.clear()
+    try:
+        with pytest.raises(AssertionError):
+            test(fake, orc)
+    finally:
+        fake.B.corrupt = set()
 
 
 @pytest.mark.parametrize("name,plant,test", PLANTS, ids=[p[0] for p in PLANTS])

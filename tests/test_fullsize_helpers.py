@@ -92,6 +92,31 @@ def test_rows_rht_equal_whole_tensor(orc, mode):
     fs.assert_rows_equal("rht", rows, q["codes"][ids], _whole_scales(orc, q["sf"], ids, 96), ids)
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_rows_rht_of_expert_segments_equal_whole_tensor(orc, mode):
+    """Expert-segmented RHT operand [cols, kt]: expert g's zero-padded
+    segment at column ko_g, its own RHT amax, SR index c * kt + ko_g + t."""
+    x = _bf16(230, 24, 11)
+    xb = fs.bits(x)
+    offsets = np.array([0, 30, 30, 100, 229, 230], dtype=np.int64)
+    counts = np.diff(offsets)
+    kt = int(((counts + 63) // 64 * 64).sum()) + 64
+    mask = 0x0F0F
+    q = orc.rht_quantize_grouped(x, offsets, kt, mask, mode=mode, seed=31)
+    for g in (0, 2, 3, 4):
+        o0, o1 = int(offsets[g]), int(offsets[g + 1])
+        seg = fs.padded_segment(xb, o0, o1)
+        kp, ko = seg.shape[0], orc.group_k_offset(offsets, g)
+        am = orc.rht_amax(seg, mask)
+        assert am == q["amax"][g]
+        ids = np.array([0, 5, 23])
+        rows = fs.rows_rht(orc, np.ascontiguousarray(seg[:, ids]), ids, kp, am, mask, mode, 31,
+                           index_stride=kt, index_offset=ko)
+        codes = q["codes"][ids][:, ko // 2:(ko + kp) // 2]
+        scales = fs.scale_rows(orc, q["sf"], ids, kt)[:, ko // 16:(ko + kp) // 16]
+        fs.assert_rows_equal(f"segment g{g}", rows, codes, scales, ids)
+
+
 def test_row_check_rejects_a_planted_mistake(orc):
     """A wrong SR index (the row's local index instead of its index in the
     whole output) or one flipped code is caught."""

@@ -192,3 +192,116 @@ def test_moe_down_full_size(run, orc):
     qh_sf = qh.sf.cpu().numpy()
     for g in _experts(counts, 8):
         _expert_check(run, orc, "down", h, qh, qh_sf, offsets, g, wk.w_down, wk.qwd, o, seed=20 + g)
+
+
+SSM_ELEMENTS = 256 * 256 * 64 * 128     # SSM cache: sequences x heads x head dim x state
+
+
+def test_expert_backward_full_size(run, orc):
+    """Grouped backward of the up-projection at full size on a seeded dH:
+    the grouped SR quantiser of dH, the grouped dgrad dA = dH . W_up against
+    the per-expert W_up^T of the batched 2D quantiser, the expert-segmented
+    RHT quantisers of dH (SR) and A (RNE), and the K-grouped FP32 wgrad
+    dW_up = RHT(dH)^T . RHT(A) per expert."""
+    from nvfp4_precision_02_b300 import workloads as wl
+    wk, B = run.wk, run.B
+    R, Hh, L, E = wk.R, wk.moe.expert_hidden, wk.moe.latent, wk.moe.experts
+    dh = wl.normal_bf16((R, Hh), 1e-3, 2025, device=wk.a.device)
+    qdh = B.quantize_1d_grouped(dh, wk.offsets, B.SR, wk.seed)
+    _, qwt, _ = B.quantize_2d(wk.w_up, want_t=True)
+    da = B.grouped_gemm(qdh, wk.offsets, qwt, L, B.OUT_BF16)
+    kt = B.group_k_capacity(R, E)
+    sdh = B.rht_quantize_grouped(dh, wk.offsets, wk.mask, B.SR, wk.wseed, kt=kt)
+    sa = B.rht_quantize_grouped(wk.a, wk.offsets, wk.mask, B.RNE, 0, kt=kt)
+    dw = B.grouped_gemm_k(sdh, sa, wk.offsets, B.OUT_FP32)
+    if dw.is_cuda:
+        torch.cuda.synchronize()
+    assert B.device_status() == 0
+    offsets = wk.routing.offsets.cpu().numpy().astype(np.int64)
+    counts = np.diff(offsets)
+    qdh_sf, sdh_sf, sa_sf = qdh.sf.cpu().numpy(), sdh.sf.cpu().numpy(), sa.sf.cpu().numpy()
+    nsf = B.sf_bytes(L, Hh)
+    for g in _experts(counts, 9):
+        o0, o1 = int(offsets[g]), int(offsets[g + 1])
+        dhb = fs.bits(dh[o0:o1])
+        # dgrad operands and outputs
+        am = orc.amax(dhb)
+        assert float(qdh.amax[g]) == am, g
+        loc = fs.sample_ids(o1 - o0, NS_E, 30 + g, must=BOUNDARY)
+        rows = loc + o0
+        dr = fs.rows_1d(orc, dhb[loc], rows, Hh, am, SR, wk.seed)
+        _check_rows(f"dH (grouped SR), expert {g}", orc, dr, qdh, rows, Hh, sf=qdh_sf,
+                    sf_rows=loc + orc.group_sf_row(offsets, g))
+        wub = fs.bits(wk.w_up[g])
+        aw = orc.amax(wub)
+        assert float(qwt.amax[g]) == aw, g
+        k_ids = fs.sample_ids(L, NS_E, 40 + g, must=BOUNDARY)
+        wtr = fs.rows_2d(orc, lambda k0: np.ascontiguousarray(wub[:, k0:k0 + 16].T), k_ids, Hh, aw)
+        _check_rows(f"W_up^T, expert {g}", orc, wtr, qwt, k_ids, Hh, batch=g,
+                    sf=qwt.sf[g * nsf:(g + 1) * nsf].cpu().numpy())
+        _check_gemm(f"grouped dgrad, expert {g}", orc, da, rows, k_ids, dr, wtr, bf16=True)
+        # wgrad operands (expert segments along K) and outputs
+        ko = orc.group_k_offset(offsets, g)
+        segh = fs.padded_segment(dhb, 0, o1 - o0)
+        sega = fs.padded_segment(fs.bits(wk.a[o0:o1]), 0, o1 - o0)
+        kp = segh.shape[0]
+        arh, ara = orc.rht_amax(segh, wk.mask), orc.rht_amax(sega, wk.mask)
+        assert float(sdh.amax[g]) == arh and float(sa.amax[g]) == ara, g
+        n_ids = fs.sample_ids(Hh, NS_E, 50 + g, must=BOUNDARY)
+        c_ids = fs.sample_ids(L, NS_E, 60 + g, must=BOUNDARY)
+        hr = fs.rows_rht(orc, np.ascontiguousarray(segh[:, n_ids]), n_ids, kp, arh, wk.mask, SR, wk.wseed,
+                         index_stride=kt, index_offset=ko)
+        ar = fs.rows_rht(orc, np.ascontiguousarray(sega[:, c_ids]), c_ids, kp, ara, wk.mask, RNE, 0,
+                         index_stride=kt, index_offset=ko)
+        for name, q, sf, ids, orows in (("RHT(dH)^T", sdh, sdh_sf, n_ids, hr), ("RHT(A)^T", sa, sa_sf, c_ids, ar)):
+            idx = torch.as_tensor(ids, device=q.codes.device)
+            codes = q.codes[idx].cpu().numpy()[:, ko // 2:(ko + kp) // 2]
+            scales = fs.scale_rows(orc, sf, ids, kt, b0=ko // 16, b1=(ko + kp) // 16)
+            fs.assert_rows_equal(f"{name} segment, expert {g}", orows, codes, scales, ids)
+        _check_gemm(f"K-grouped wgrad, expert {g}", orc, dw, g * Hh + n_ids, c_ids, hr, ar, bf16=False)
+
+
+def test_ptq_mse_scales_full_size(run, orc):
+    """Minimum-squared-error block scales of the in_proj weight at full size
+    (with the weight's tensor amax), on sampled rows."""
+    wk, B = run.wk, run.B
+    N, K = wk.dense.out, wk.dense.hidden
+    aw = orc.amax(_host(run, "w"))
+    amax_in = torch.tensor([aw], dtype=torch.float32, device=wk.w.device)
+    q = B.quantize_1d_mse(wk.w, amax_in=amax_in)
+    ids = fs.sample_ids(N, NS, 70, must=BOUNDARY)
+    wb = _host(run, "w")
+    orows = fs.OracleRows(len(ids), K, aw)
+    for i, n in enumerate(ids):
+        o = orc.quantize_1d_mse(np.ascontiguousarray(wb[n:n + 1]), amax_in=aw)
+        orows.codes[i] = o["codes"][0]
+        orows.scales[i] = fs.scale_rows(orc, o["sf"], [0], K)[0]
+    _check_rows("W (MSE block scales)", orc, orows, q, ids, K)
+
+
+def test_sr_fp16_full_size(run, orc):
+    """FP16 stochastic rounding of an SSM-cache-sized FP32 tensor: sampled
+    elements equal the oracle's rounding with the word of their index."""
+    B = run.B
+    dev = run.wk.a.device
+    g = torch.Generator(device=dev)
+    g.manual_seed(12)
+    x = torch.randn(SSM_ELEMENTS, generator=g, device=dev)
+    out = B.sr_fp16(x, 5)
+    e = fs.sample_ids(SSM_ELEMENTS, 4096, 13)
+    idx = torch.as_tensor(e, device=dev)
+    xs = x[idx].cpu().numpy()
+    got = out[idx].view(torch.int16).cpu().numpy().view(np.uint16)
+    exp = np.array([orc.fp16_sr(float(v), orc.sr_word(5, int(i))) for v, i in zip(xs, e)], dtype=np.uint16)
+    bad = np.flatnonzero(got != exp)
+    assert bad.size == 0, f"{bad.size} of {len(e)} sampled elements differ, first {e[bad[:4]].tolist()}"
+
+
+def test_zero_code_count_full_size(run, orc):
+    """The zero-code counter over the SR-quantised dY equals a count of the
+    zero-magnitude nibbles of the same codes."""
+    wk, B = run.wk, run.B
+    cnt = int(B.count_zero_codes(wk.qdy).item())
+    c = wk.qdy.codes.cpu().numpy()
+    assert cnt == int(((c & 7) == 0).sum()) + int((((c >> 4) & 7) == 0).sum())
+    assert 0 < cnt < c.size * 2
