@@ -172,6 +172,7 @@ class Workload:
             ("grouped_gemm down", "tensor", gem(R, L, Hh)),
         ]
         self.gemm_flops = sum(w_ for _, k, w_ in self.ops if k == "tensor")
+        self.gemm_bytes = gemm_bytes_table(d, m, R)
         self.input_tensors = [self.x, self.w, self.dy, self.a, self.w_up, self.w_down]
         self.output_tensors = [self.y, self.dx, self.dw, self.o]
 
@@ -197,6 +198,35 @@ class Workload:
                        c_amax=self.qh.amax); mk(11)
         B.quantize_1d_grouped(self.h, self.offsets, B.RNE, 0, amax_in=self.qh.amax, out=self.qh); mk(12)
         B.grouped_gemm(self.qh, self.offsets, self.qwd, self.moe.latent, B.OUT_BF16, out=self.o); mk(13)
+
+
+def gemm_bytes_table(d, m, R: int) -> dict:
+    """Algorithmic bytes of each GEMM of the step: FP4 operands read once
+    (0.5625 B per element: half a byte of code plus 1/16 B of block scale),
+    every expert's weight read once, the output written once (bf16, or FP32
+    for wgrad)."""
+    T, K, N = d.tokens, d.hidden, d.out
+    E, L, Hh = m.experts, m.latent, m.expert_hidden
+    fp4 = 0.5625
+    return {
+        "gemm fprop": fp4 * (T + N) * K + 2.0 * T * N,
+        "gemm dgrad": fp4 * (T + K) * N + 2.0 * T * K,
+        "gemm wgrad": fp4 * (N + K) * T + 4.0 * N * K,
+        "grouped_gemm up (+ per-expert amax of H)": fp4 * (R + E * Hh) * L + 2.0 * R * Hh,
+        "grouped_gemm down": fp4 * (R + E * L) * Hh + 2.0 * R * L,
+    }
+
+
+def gemm_roofline(flops: float, nbytes, ms: float, hbm_gbs: float, fp4_tflops: float) -> dict:
+    """The GEMM's roofline time max(bytes / HBM bandwidth, FLOPs / FP4 peak),
+    which of the two bounds it, and the measured time's fraction of it."""
+    if not nbytes or ms <= 0:
+        return {}
+    t_hbm = nbytes / (hbm_gbs * 1e9) * 1e3
+    t_tc = flops / (fp4_tflops * 1e12) * 1e3
+    t = max(t_hbm, t_tc)
+    return {"bytes": int(nbytes), "bound": "hbm" if t_hbm > t_tc else "tensor", "roofline_ms": round(t, 4),
+            "frac_roofline": round(t / ms, 4)}
 
 
 # ---------------------------------------------------------------- clocks
@@ -407,7 +437,8 @@ def main():
     for (n, k, w), t in zip(wk.ops, op_ms):
         if k == "tensor":
             ops[n] = {"ms": round(t, 4), "tflops": round(w / (t * 1e-3) / 1e12, 1),
-                      "frac_fp4_sustained": round(w / (t * 1e-3) / 1e12 / fp4_peak_sust, 4)}
+                      "frac_fp4_sustained": round(w / (t * 1e-3) / 1e12 / fp4_peak_sust, 4),
+                      **gemm_roofline(w, wk.gemm_bytes.get(n), t, pk["hbm_gbs"], fp4_peak_sust)}
         else:
             ops[n] = {"ms": round(t, 4), "gbs": round(w / (t * 1e-3) / 1e9, 1),
                       "frac_hbm": round(w / (t * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}

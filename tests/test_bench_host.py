@@ -99,5 +99,33 @@ def test_reference_arm_other_ranks_exit_quietly():
     assert r.returncode == 0 and r.stdout.strip() == ""
 
 
+
+def test_gemm_roofline_and_bytes_table():
+    from nvfp4_precision_02_b300 import workloads as wl
+    d, m = wl.ULTRA_DENSE, wl.ULTRA_MOE
+    R = m.tokens * m.topk
+    tab = bench.gemm_bytes_table(d, m, R)
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    ops_src = src[src.index("self.ops = ["):src.index("self.gemm_flops")]
+    for name in tab:                       # every key names a GEMM op of the step
+        assert f'("{name}", "tensor"' in ops_src, name
+    # fprop: (16384 + 33024) x 8192 FP4 operands and a bf16 16384 x 33024 output
+    assert tab["gemm fprop"] == 0.5625 * (16384 + 33024) * 8192 + 2 * 16384 * 33024
+    # up-projection: all 512 experts' 5120 x 2048 weights are read once
+    assert tab["grouped_gemm up (+ per-expert amax of H)"] == 0.5625 * (360448 + 512 * 5120) * 2048 + 2 * 360448 * 5120
+    # 1 GB at 1000 GB/s is 1 ms; 2 TFLOP at 1000 TFLOP/s is 2 ms: tensor-bound, 2 ms roof
+    r = bench.gemm_roofline(2e12, 1e9, 4.0, 1000.0, 1000.0)
+    assert r["bound"] == "tensor" and r["roofline_ms"] == 2.0 and r["frac_roofline"] == 0.5
+    r = bench.gemm_roofline(0.5e12, 1e9, 2.0, 1000.0, 1000.0)
+    assert r["bound"] == "hbm" and r["roofline_ms"] == 1.0 and r["frac_roofline"] == 0.5
+    assert bench.gemm_roofline(1e12, None, 1.0, 1.0, 1.0) == {}
+    # with the measured peaks the dense GEMMs are tensor-bound and the up-projection HBM-bound
+    hbm, fp4 = 6487.7, 1377.6 * 6
+    flops = 2.0 * 16384 * 33024 * 8192
+    assert bench.gemm_roofline(flops, tab["gemm fprop"], 1.7, hbm, fp4)["bound"] == "tensor"
+    up = 2.0 * R * m.expert_hidden * m.latent
+    assert bench.gemm_roofline(up, tab["grouped_gemm up (+ per-expert amax of H)"], 2.4, hbm, fp4)["bound"] == "hbm"
+
+
 if __name__ == "__main__":
     sys.exit(pytest.main([__file__, "-q"]))
