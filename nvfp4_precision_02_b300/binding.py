@@ -28,14 +28,13 @@ STATIC_MAX_BATCH = 4096
 STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_NULL", 2: "NVFP4_ERR_SHAPE", 3: "NVFP4_ERR_ALIGN",
           4: "NVFP4_ERR_DEVICE", 5: "NVFP4_ERR_CUDA", 6: "NVFP4_ERR_TIMEOUT", 7: "NVFP4_ERR_LIMIT"}
 
-EXPORTS = ["nvfp4_sf_bytes", "nvfp4_sf_bytes_grouped", "nvfp4_sf_offset", "nvfp4_amax",
-           "nvfp4_quantize_1d", "nvfp4_quantize_1d_grouped", "nvfp4_quantize_2d",
-           "nvfp4_quantize_2d_fused_workspace", "nvfp4_quantize_2d_fused", "nvfp4_quantize_2d_fused_static",
-           "nvfp4_rht_amax",
-           "nvfp4_rht_quantize", "nvfp4_dual_amax", "nvfp4_count_zero_codes", "nvfp4_quantize_1d_mse", "nvfp4_sr_fp16", "nvfp4_group_k_capacity", "nvfp4_rht_quantize_grouped", "nvfp4_gemm",
-           "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_k", "nvfp4_status_string",
-           "nvfp4_last_error", "nvfp4_device_status", "nvfp4_launch_count", "nvfp4_debug_inject",
-           "nvfp4_debug_wait_timeout"]
+EXPORTS = ["nvfp4_sf_bytes", "nvfp4_sf_bytes_grouped", "nvfp4_sf_offset", "nvfp4_amax", "nvfp4_quantize_1d",
+           "nvfp4_quantize_1d_grouped", "nvfp4_quantize_2d", "nvfp4_quantize_2d_fused_workspace",
+           "nvfp4_quantize_2d_fused", "nvfp4_quantize_2d_fused_static", "nvfp4_rht_amax",
+           "nvfp4_rht_quantize", "nvfp4_dual_amax", "nvfp4_count_zero_codes", "nvfp4_quantize_1d_mse",
+           "nvfp4_sr_fp16", "nvfp4_group_k_capacity", "nvfp4_rht_quantize_grouped", "nvfp4_gemm",
+           "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_k", "nvfp4_status_string", "nvfp4_last_error",
+           "nvfp4_device_status", "nvfp4_launch_count", "nvfp4_debug_inject", "nvfp4_debug_wait_timeout"]
 
 
 class Nvfp4Error(RuntimeError):
