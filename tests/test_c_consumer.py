@@ -101,3 +101,22 @@ def test_plain_c_program_against_the_library(tmp_path):
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.startswith("OK")
 
+
+
+def test_readme_c_example_compiles_and_links(tmp_path):
+    """The C example of README.md compiles as C11 against the header and
+    links against libnvfp4.so and the CUDA runtime (it is not run)."""
+    _need("gcc")
+    text = open(os.path.join(ROOT, "README.md")).read()
+    sec = text[text.index("## C\n"):text.index("## Tests")]
+    code = "\n".join(l[4:] for l in sec.splitlines() if l.startswith("    "))
+    assert "nvfp4_gemm(" in code
+    src = tmp_path / "example.c"
+    src.write_text(code + "\nint main(void) { return 0; }\n")
+    cuda_inc, cuda_lib = "/usr/local/cuda/include", "/usr/local/cuda/lib64"
+    if not os.path.exists(os.path.join(cuda_inc, "cuda_runtime.h")):
+        pytest.skip("CUDA headers not installed")
+    r = subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", f"-I{INC}", f"-I{cuda_inc}", str(src),
+                        "-o", str(tmp_path / "example"), f"-L{PKG}", "-lnvfp4", f"-L{cuda_lib}", "-lcudart",
+                        f"-Wl,-rpath,{PKG}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
