@@ -36,8 +36,13 @@
  *      output; round up iff (u >> 8) < p * 2^24.
  *   R5 RHT           16-point Sylvester Hadamard along the quantised K axis,
  *      y = 0.25 * H * (s .* x), FP32 butterfly with stages 1, 2, 4, 8.
- *   R6 layouts       codes packed two per byte (even index in the low
- *      nibble); block scales in 128x4 atoms (see oracle_sf_offset).
+ *   R8 grouped       one tensor amax per expert (oracle_quantize_1d_grouped,
+ *      the batched oracle_quantize_2d).
+ *   R9 2D tiles      rows and columns of a 2D-quantised weight are multiples
+ *      of 16.
+ *   Layouts (not a reading of the method): codes packed two per byte (even
+ *      index in the low nibble); block scales in 128x4 atoms (see
+ *      oracle_sf_offset).
  *   R14 expert segments of the grouped wgrad (oracle_rht_quantize_grouped).
  *   R15 FP16 SR of the SSM cache (oracle_fp16_sr).
  *   R16 PTQ block scales by minimum squared error (oracle_quantize_1d_mse).
