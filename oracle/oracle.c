@@ -240,7 +240,7 @@ void oracle_encode_block(const float *x, int n, float s_enc, int mode,
 }
 
 /* ------------------------------------------------------------------ */
-/* Layouts (R6).                                                        */
+/* Layouts.                                                             */
 /* ------------------------------------------------------------------ */
 
 static float bf16_to_float(uint16_t h)
