@@ -229,6 +229,26 @@ def gemm_roofline(flops: float, nbytes, ms: float, hbm_gbs: float, fp4_tflops: f
             "frac_roofline": round(t / ms, 4)}
 
 
+# integer-ALU operations per element of the SR quantisers, counted from the
+# source: about 18 for the rounding decision, 2.5 for Philox's three-input
+# XORs (its multiplies run on the FMA pipe) and 3 to unpack and pack
+SR_ALU_OPS_PER_ELEMENT = 24
+ALU_LANES_PER_SM = 64          # integer/logic lanes per SM per clock (4 partitions x 16)
+
+
+def alu_roofline(elements: int, ms: float, sm_mhz, sms: int, ops_per_element: int = SR_ALU_OPS_PER_ELEMENT):
+    """ALU roof of an integer-bound kernel from a source-level operation count:
+    elements x ops / (lanes per SM x SMs x SM clock), against the measured time."""
+    if not sm_mhz or ms <= 0 or sms <= 0:
+        return None
+    peak = ALU_LANES_PER_SM * sms * sm_mhz * 1e6            # lane-operations per second
+    achieved = elements * ops_per_element / (ms * 1e-3)
+    return {"bound": "alu", "unit": "Gop/s", "achieved": round(achieved / 1e9, 1), "peak": round(peak / 1e9, 1),
+            "frac": round(achieved / peak, 4), "ops_per_element": ops_per_element,
+            "floor_ms": round(elements * ops_per_element / peak * 1e3, 4),
+            "note": "operation count estimated from the source, clock = median SM clock of the timed region"}
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -462,7 +482,9 @@ def main():
                   "unit": "GB/s", "frac": round(wk.ops[qi][2] / (q_dy * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                   "peak_note": "HBM copy bandwidth (measured); the kernel itself is held back by the integer ALU pipe "
                                "(SR decision and Philox), not by HBM",
-                  "traffic": None}
+                  "traffic": None,
+                  "alu_estimate": alu_roofline(wk.dense.tokens * wk.dense.out, q_dy,
+                                               clk["sm_mhz"] if clk else None, props.multi_processor_count)}
 
     supplied = measure_supplied_amax(wk, pk["hbm_gbs"])
     zeros = int(B.count_zero_codes(wk.qdy).item())
