@@ -484,7 +484,7 @@ def main():
                                "(SR decision and Philox), not by HBM",
                   "traffic": None,
                   "alu_estimate": alu_roofline(wk.dense.tokens * wk.dense.out, q_dy,
-                                               clk["sm_mhz"] if clk else None, props.multi_processor_count)}
+                                               (clk or {}).get("sm_mhz"), getattr(props, "multi_processor_count", 0))}
 
     supplied = measure_supplied_amax(wk, pk["hbm_gbs"])
     zeros = int(B.count_zero_codes(wk.qdy).item())
