@@ -36,9 +36,20 @@ if ROOT not in sys.path:
 
 METRIC = "NVFP4 GEMM TFLOPS (% dense FP4 peak); quantize GB/s (% HBM) on 1 B300"
 FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense FP4 : BF16 tensor throughput on B300
+FP4_DATASHEET_TFLOPS = 13500.0   # nominal dense NVFP4 figure of a B300 (HGX class), unverified
+# FP4 FLOP per SM per clock.  ncu's peak for
+# sm__ops_path_tensor_op_utcomma_src_fp4_dst_fp32_sparsity_off is 7,274,496
+# FLOP per cycle over 148 SMs (49152 per SM); back-to-back issue of the
+# block-scaled MMA this library uses (kind::mxf4nvf4, scale_vec::4X, E4M3
+# scales), with no data movement, completes one 128x256x64 MMA per 128 SM
+# cycles on B300 (32768 FLOP per SM per cycle) for single CTAs and CTA pairs,
+# N = 128 and 256 alike, at any number of active SMs.
+FP4_FLOP_PER_CLK_SM_COUNTER = 49152
+FP4_FLOP_PER_CLK_SM = 32768
+HBM_NOMINAL_GBS = 8000.0         # the ~8 TB/s nominal HBM3e figure the quantiser target is stated against
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=100)
@@ -48,7 +59,10 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=2)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    return p.parse_args()
+    p.add_argument("--no-configs", action="store_true", help="skip the per-config measurements (c1-c4)")
+    p.add_argument("--launch-check", action="store_true",
+                   help="start the ranks, time an empty region and print the line (no GPU work; CPU ranks use gloo)")
+    return p.parse_args(argv)
 
 
 # Source of the GEMM kernel; the ncu traffic figure committed under
@@ -86,6 +100,25 @@ def profiled_traffic(summary: str):
     b = re.search(r"dram_bytes_per_launch:\s*(\d+)", text)
     h = re.search(r"kernel_code_sha256:\s*([0-9a-f]{64})", text)
     if not b or not h or h.group(1) != source_hash():
+        return None
+    return int(b.group(1))
+
+
+# Sources of the quantiser kernels (a quantiser profile is tied to these).
+QUANT_SOURCES = ("nvfp4_precision_02_b300/csrc/quant.cuh", "nvfp4_precision_02_b300/csrc/common.cuh")
+
+
+def profiled_quant_traffic(summary: str, kernel: str):
+    """DRAM bytes per launch of a quantiser from a committed ncu summary
+    (`dram_bytes_per_launch: N`, `kernel_code_sha256: H` over the quantiser
+    sources), or None when missing or stale."""
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    b = re.search(r"dram_bytes_per_launch:\s*(\d+)", text)
+    h = re.search(r"kernel_code_sha256:\s*([0-9a-f]{64})", text)
+    if not b or not h or h.group(1) != source_hash(QUANT_SOURCES):
         return None
     return int(b.group(1))
 
@@ -386,11 +419,158 @@ def oracle_sample(which: str, budget_s: float):
 
 
 # ---------------------------------------------------------------- main
-def main():
-    args = parse()
+def relaunch_ranks(n: int, argv) -> int:
+    """Start n ranks of this script on this node with torch.distributed.run
+    (rendezvous on 127.0.0.1) and return their exit status; used when
+    --gpus N > 1 is given without a launcher (no WORLD_SIZE in the
+    environment)."""
+    import socket
+    with socket.socket() as s_:
+        s_.bind(("127.0.0.1", 0))
+        port = s_.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
+def fp4_peaks(pk: dict, sms: int, sm_mhz) -> dict:
+    """Dense FP4 denominators of the GEMM fractions: the measured bf16 burst
+    and sustained rates x 6 (the nominal FP4:BF16 ratio), the 13.5 PFLOP/s
+    datasheet figure, and, at the median SM clock of the timed region, the
+    measured issue rate of the block-scaled MMA and ncu's counter peak."""
+    out = {"burst_x6": pk["bf16_burst"] * FP4_OVER_BF16, "sustained_x6": pk["bf16_sustained"] * FP4_OVER_BF16,
+           "datasheet": FP4_DATASHEET_TFLOPS}
+    if sm_mhz and sms:
+        out["mma_issue_at_clock"] = FP4_FLOP_PER_CLK_SM * sms * sm_mhz * 1e6 / 1e12
+        out["counter_at_clock"] = FP4_FLOP_PER_CLK_SM_COUNTER * sms * sm_mhz * 1e6 / 1e12
+    return out
+
+
+def gemm_fracs(tflops: float, fp4: dict) -> dict:
+    return {f"frac_fp4_{k}": round(tflops / v, 4) for k, v in fp4.items()}
+
+
+def hbm_fracs(gbs: float, pk: dict) -> dict:
+    return {"frac_hbm": round(gbs / pk["hbm_gbs"], 4), "frac_hbm_nominal_8tbs": round(gbs / HBM_NOMINAL_GBS, 4)}
+
+
+def op_entry(kind: str, work: float, ms: float, pk: dict, fp4: dict, nbytes=None) -> dict:
+    """One op's time and rate with its fractions: TFLOP/s against every FP4
+    denominator (and its roofline when its bytes are known) for a GEMM, GB/s
+    against the measured and the nominal HBM bandwidth for a quantiser."""
+    if kind == "tensor":
+        tf = work / (ms * 1e-3) / 1e12
+        e = {"ms": round(ms, 4), "tflops": round(tf, 1), **gemm_fracs(tf, fp4)}
+        if nbytes:
+            e.update(gemm_roofline(work, nbytes, ms, pk["hbm_gbs"], fp4["burst_x6"]))
+        return e
+    gbs = work / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 4), "gbs": round(gbs, 1), **hbm_fracs(gbs, pk)}
+
+
+def time_ops(wk, steps: int = 5):
+    """Median CUDA-event time of each op of wk's step over `steps` steps."""
+    import torch
+    nops = len(wk.ops)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for s_ in range(steps):
+        ev[s_][0].record()
+        wk.step(marks=lambda i, s_=s_: ev[s_][i + 1].record())
+    torch.cuda.synchronize()
+    return [statistics.median(ev[s_][i].elapsed_time(ev[s_][i + 1]) for s_ in range(steps)) for i in range(nops)]
+
+
+# the ops of the Workload step that make up each stated configuration
+CONFIG_OPS = {"c2": (0, 3), "c3": (3, 9), "c4": (9, 14)}
+
+
+def measure_configs(dev, pk: dict, fp4: dict, super_wk=None, steps: int = 5) -> dict:
+    """Configurations 1-4 timed on their own shapes after the timed region:
+    c1 the 256 x 256 tiny fprop (1D RNE A, 16x16 W, GEMM); c2-c4 the ops of a
+    Super-shaped step -- c2 the in_proj fprop (X 8192 x 6144 with outliers,
+    W 18560 x 6144), c3 its backward (SR dY, dgrad, RHT wgrad), c4 the
+    LatentMoE (1024 -> 2688 -> 1024, 180224 routed rows).  Each op's median
+    CUDA-event time with its rate and fractions; each config's total."""
+    import torch
+    from nvfp4_precision_02_b300 import binding as B, workloads as wl
+    out = {}
+    a, w = (t.to(dev) for t in wl.tiny_inputs())
+    qa = B.quantize_1d(a)
+    qw = B.quantize_2d(w)[0]
+    y = torch.empty(256, 256, dtype=torch.bfloat16, device=dev)
+    tiny = [("quantize_1d A (amax+RNE)", "hbm", 4.5625 * 256 * 256, lambda: B.quantize_1d(a, out=qa)),
+            ("quantize_2d W (amax+W)", "hbm", 4.5625 * 256 * 256, lambda: B.quantize_2d(w, want_t=False, out=qw)),
+            ("gemm fprop", "tensor", 2.0 * 256 ** 3, lambda: B.gemm(qa, qw, B.OUT_BF16, out=y))]
+    c1 = {}
+    for name, kind, work, fn in tiny:
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(50):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        c1[name] = op_entry(kind, work, e0.elapsed_time(e1) / 50, pk, fp4,
+                            0.5625 * 512 * 256 + 2 * 256 * 256 if kind == "tensor" else None)
+    out["c1_tiny_fprop_256"] = {"ops": c1, "ms": round(sum(v["ms"] for v in c1.values()), 4),
+                                "note": "launch-bound: 50 back-to-back calls per op"}
+    own = super_wk is None
+    wk = Workload("super", dev) if own else super_wk
+    wk.step()
+    torch.cuda.synchronize()
+    ms = time_ops(wk, steps)
+    names = {"c2": "c2_super_in_proj_fprop", "c3": "c3_super_backward", "c4": "c4_super_latent_moe"}
+    for key, (i0, i1) in CONFIG_OPS.items():
+        ops = {}
+        for i in range(i0, i1):
+            n, kind, work = wk.ops[i]
+            ops[n] = op_entry(kind, work, ms[i], pk, fp4, wk.gemm_bytes.get(n))
+        flops = sum(wk.ops[i][2] for i in range(i0, i1) if wk.ops[i][1] == "tensor")
+        t = sum(ms[i0:i1])
+        out[names[key]] = {"ops": ops, "ms": round(t, 4), "gemm_tflops_incl_quantisers": round(flops / (t * 1e-3) / 1e12, 1)}
+    out["c5_ultra_full_step"] = "the step of this line (ops, roofline)"
+    if own:
+        del wk
+        torch.cuda.empty_cache()
+    return out
+
+
+def launch_check(args, world: int, rank: int) -> int:
+    """The multi-rank launch path without GPU work: every rank joins the
+    process group (gloo without CUDA), meets the others at a barrier, times
+    an empty region, and rank 0 prints n_gpus = the ranks that ran."""
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("gloo")
+        dist.barrier()
+    t0 = time.perf_counter()
+    if world > 1:
+        dist.barrier()
+    ms = max_over_ranks((time.perf_counter() - t0) * 1e3 + rank, world, "cpu")
+    n = world
+    if world > 1:
+        t = torch.tensor([1.0])
+        dist.all_reduce(t)
+        n = int(t.item())
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps({"launch_check": True, "n_gpus": n, "world_size": world, "max_ms": round(ms, 3)}), flush=True)
+    return 0
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
+    args = parse(argv)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return relaunch_ranks(args.gpus, argv)
+    if args.launch_check:
+        return launch_check(args, world, rank)
 
     if args.impl == "reference":
         if rank != 0:
@@ -418,6 +598,7 @@ def main():
     nops = len(wk.ops)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)] for _ in range(args.steps)]
     props = torch.cuda.get_device_properties(dev)
+    sms = getattr(props, "multi_processor_count", 0)
     uuid = str(getattr(props, "uuid", ""))
     if uuid and not uuid.startswith("GPU-"):
         uuid = "GPU-" + uuid
@@ -447,49 +628,45 @@ def main():
     status = B.device_status()
 
     pk = peaks()
-    fp4_peak_sust = pk["bf16_sustained"] * FP4_OVER_BF16
-    fp4_peak_burst = pk["bf16_burst"] * FP4_OVER_BF16
+    sm_mhz = (clk or {}).get("sm_mhz")
+    fp4 = fp4_peaks(pk, sms, sm_mhz)
     value = wk.gemm_flops * world / (ms_step * 1e-3) / 1e12
     gemm_ms = sum(t for (n, k, _), t in zip(wk.ops, op_ms) if k == "tensor")
     quant_ms = sum(t for (n, k, _), t in zip(wk.ops, op_ms) if k == "hbm")
     quant_bytes = sum(w for _, k, w in wk.ops if k == "hbm")
-    ops = {}
-    for (n, k, w), t in zip(wk.ops, op_ms):
-        if k == "tensor":
-            ops[n] = {"ms": round(t, 4), "tflops": round(w / (t * 1e-3) / 1e12, 1),
-                      "frac_fp4_sustained": round(w / (t * 1e-3) / 1e12 / fp4_peak_sust, 4),
-                      **gemm_roofline(w, wk.gemm_bytes.get(n), t, pk["hbm_gbs"], fp4_peak_sust)}
-        else:
-            ops[n] = {"ms": round(t, 4), "gbs": round(w / (t * 1e-3) / 1e9, 1),
-                      "frac_hbm": round(w / (t * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+    ops = {n: op_entry(k, w, t, pk, fp4, wk.gemm_bytes.get(n)) for (n, k, w), t in zip(wk.ops, op_ms)}
     # dominant kernel: k_gemm_nvfp4; its roofline is given for the fprop launch
     fprop_i = [n for n, _, _ in wk.ops].index("gemm fprop")
     fprop_flops = wk.ops[fprop_i][2]
     achieved = fprop_flops / (op_ms[fprop_i] * 1e-3) / 1e12
     traffic = profiled_traffic(f"k_gemm_nvfp4_fprop_{args.workload}.md")
     roofline = {"kernel": "k_gemm_nvfp4 (fprop launch)", "bound": "tensor",
-                "achieved": round(achieved, 1), "peak": round(fp4_peak_sust, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / fp4_peak_sust, 4),
-                "peak_note": f"{pk['source']} sustained bf16 x {FP4_OVER_BF16:g} (nominal FP4:BF16)",
-                "frac_of_burst": round(achieved / fp4_peak_burst, 4),
+                "achieved": round(achieved, 1), "peak": round(fp4["burst_x6"], 1), "unit": "TFLOP/s",
+                "frac": round(achieved / fp4["burst_x6"], 4),
+                "peak_note": f"{pk['source']} burst bf16 x {FP4_OVER_BF16:g} (nominal dense FP4:BF16); "
+                             "frac_fp4_* give the same launch against the other denominators",
+                **gemm_fracs(achieved, fp4),
+                "clock_mhz_median": sm_mhz,
                 "traffic": traffic, "traffic_unit": "bytes per launch (ncu dram read + write)",
                 "algorithmic_bytes": int(0.5625 * (wk.dense.tokens + wk.dense.out) * wk.dense.hidden
                                          + 2 * wk.dense.tokens * wk.dense.out)}
     qi = [n for n, _, _ in wk.ops].index("quantize_1d dY (SR)")
     q_dy = op_ms[qi]
+    q_gbs = wk.ops[qi][2] / (q_dy * 1e-3) / 1e9
     roofline_q = {"kernel": "k_quant1d<SR> (dY 1x16 SR, amax supplied)", "bound": "hbm",
-                  "achieved": round(wk.ops[qi][2] / (q_dy * 1e-3) / 1e9, 1), "peak": pk["hbm_gbs"],
-                  "unit": "GB/s", "frac": round(wk.ops[qi][2] / (q_dy * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
-                  "peak_note": "HBM copy bandwidth (measured); the kernel itself is held back by the integer ALU pipe "
-                               "(SR decision and Philox), not by HBM",
-                  "traffic": None,
-                  "alu_estimate": alu_roofline(wk.dense.tokens * wk.dense.out, q_dy,
-                                               (clk or {}).get("sm_mhz"), getattr(props, "multi_processor_count", 0))}
+                  "achieved": round(q_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                  "frac": round(q_gbs / pk["hbm_gbs"], 4), "frac_hbm_nominal_8tbs": round(q_gbs / HBM_NOMINAL_GBS, 4),
+                  "peak_note": "HBM copy bandwidth (measured)",
+                  "traffic": profiled_quant_traffic(f"k_quant1d_sr_{args.workload}.md", "k_quant1d"),
+                  "alu_estimate": alu_roofline(wk.dense.tokens * wk.dense.out, q_dy, sm_mhz, sms)}
 
-    supplied = measure_supplied_amax(wk, pk["hbm_gbs"])
+    supplied = measure_supplied_amax(wk, pk)
     zeros = int(B.count_zero_codes(wk.qdy).item())
     zero_frac = zeros / float(wk.dense.tokens * wk.dense.out)
-    next_rows = measure_next_rows(wk, pk["hbm_gbs"], fp4_peak_sust)
+    next_rows = measure_next_rows(wk, pk, fp4)
+    configs = None
+    if not args.no_configs:
+        configs = measure_configs(dev, pk, fp4, super_wk=wk if args.workload == "super" else None)
 
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
@@ -510,8 +687,11 @@ def main():
         "gemm_tflops": round(wk.gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
         "quantize_gbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9, 1),
         "quantize_frac_hbm": round(quant_bytes / (quant_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+        "quantize_frac_hbm_nominal_8tbs": round(quant_bytes / (quant_ms * 1e-3) / 1e9 / HBM_NOMINAL_GBS, 4),
+        "fp4_peaks_tflops": {k: round(v, 1) for k, v in fp4.items()},
         "ops": ops, "roofline": roofline, "roofline_quantize": roofline_q,
         "quantize_supplied_amax": supplied,
+        "configs": configs,
         "dy_zero_code_fraction": round(zero_frac, 6),
         "next_rows": next_rows,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk,
@@ -537,7 +717,7 @@ def host_mem_available() -> int:
     return 0
 
 
-def measure_supplied_amax(wk: Workload, hbm_gbs: float, iters: int = 5):
+def measure_supplied_amax(wk: Workload, pk: dict, iters: int = 5):
     """Each quantiser of the step with its amax supplied (the step's own
     amaxes, already in the output tensors), timed alone after the timed
     region: one HBM read of the input, so the algorithmic bytes are 2.5625 per
@@ -575,12 +755,11 @@ def measure_supplied_amax(wk: Workload, hbm_gbs: float, iters: int = 5):
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / iters
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        out[name] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4)}
+        out[name] = op_entry("hbm", nbytes, ms, pk, {})
     return out
 
 
-def measure_next_rows(wk: Workload, hbm_gbs: float, fp4_peak: float, iters: int = 3):
+def measure_next_rows(wk: Workload, pk: dict, fp4: dict, iters: int = 3):
     """The grouped backward of the LatentMoE up-projection, timed alone after
     the timed region (not part of the step): dgrad dA = dH . W_up per expert
     (W_up^T from the batched 2D quantiser, dH in 1x16 SR) and wgrad
@@ -622,12 +801,7 @@ def measure_next_rows(wk: Workload, hbm_gbs: float, fp4_peak: float, iters: int 
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / iters
-        if kind == "tensor":
-            tf = work / (ms * 1e-3) / 1e12
-            out[name] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_fp4_sustained": round(tf / fp4_peak, 4)}
-        else:
-            gbs = work / (ms * 1e-3) / 1e9
-            out[name] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4)}
+        out[name] = op_entry(kind, work, ms, pk, fp4)
     # PTQ block scales by minimum squared error (next row f3) on the in_proj weight
     qptq = B.empty_qtensor(wk.dense.out, wk.dense.hidden, dev)
     B.quantize_1d_mse(wk.w, amax_in=wk.qw.amax, out=qptq)
@@ -655,15 +829,13 @@ def measure_next_rows(wk: Workload, hbm_gbs: float, fp4_peak: float, iters: int 
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / iters
-    gbs = 6.0 * ssm.numel() / (ms * 1e-3) / 1e9
-    out["sr_fp16 SSM cache (FP32 -> FP16, 6 B / element)"] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
-                                                              "frac_hbm": round(gbs / hbm_gbs, 4)}
+    out["sr_fp16 SSM cache (FP32 -> FP16, 6 B / element)"] = op_entry("hbm", 6.0 * ssm.numel(), ms, pk, fp4)
     del ssm, ssm16
     # the wgrad writes E * Hh * L FP32 outputs: its HBM roof
     w = out["grouped_gemm_k wgrad (dW_up, FP32)"]
     wbytes = 4.0 * E * Hh * L + 0.5625 * (Hh + L) * kt
     w["hbm_gbs"] = round(wbytes / (w["ms"] * 1e-3) / 1e9, 1)
-    w["frac_hbm"] = round(w["hbm_gbs"] / hbm_gbs, 4)
+    w["frac_hbm"] = round(w["hbm_gbs"] / pk["hbm_gbs"], 4)
     del qdh, qwt, da, sdh, sa, dw
     torch.cuda.empty_cache()
     return out
@@ -724,13 +896,12 @@ def reference_arm(args):
     sec = statistics.mean(secs)
     value = flops / sec / 1e12
     config = workload_config(args.workload, d, m, R, 1)
-    config["sample_wall_s_per_step"] = round(statistics.mean(walls), 2)
     line = {"metric": METRIC, "value": round(value, 9), "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference", "config": config,
             "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": th, "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, "sample_wall_s_per_step": round(statistics.mean(walls), 2)},
             "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0

@@ -137,5 +137,46 @@ def test_alu_roofline():
     assert bench.alu_roofline(100, 1.0, None, 148) is None
 
 
+def test_fp4_peaks_and_fractions():
+    pk = {"hbm_gbs": 6500.0, "bf16_burst": 1700.0, "bf16_sustained": 1300.0, "source": "measured"}
+    fp4 = bench.fp4_peaks(pk, 148, 2000.0)
+    assert fp4["burst_x6"] == 10200.0 and fp4["sustained_x6"] == 7800.0 and fp4["datasheet"] == 13500.0
+    # 32768 (measured MMA issue) and 49152 (counter) FLOP per SM per clock x 148 SMs x 2 GHz
+    assert abs(fp4["mma_issue_at_clock"] - 32768 * 148 * 2.0e9 / 1e12) < 1e-6
+    assert abs(fp4["counter_at_clock"] - 49152 * 148 * 2.0e9 / 1e12) < 1e-6
+    assert "mma_issue_at_clock" not in bench.fp4_peaks(pk, 148, None)
+    f = bench.gemm_fracs(5100.0, fp4)
+    assert f["frac_fp4_burst_x6"] == 0.5 and f["frac_fp4_datasheet"] == round(5100 / 13500, 4)
+    e = bench.op_entry("hbm", 6.5e9, 1.0, pk, fp4)      # 6.5 GB in 1 ms
+    assert e["gbs"] == 6500.0 and e["frac_hbm"] == 1.0 and e["frac_hbm_nominal_8tbs"] == round(6500 / 8000, 4)
+    g = bench.op_entry("tensor", 10.2e12, 1.0, pk, fp4, nbytes=1e9)
+    assert g["tflops"] == 10200.0 and g["frac_fp4_burst_x6"] == 1.0 and g["bound"] == "tensor"
+
+
+def test_config_ops_cover_the_step():
+    """c2-c4 partition the step's ops: fprop, backward, LatentMoE."""
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    ops_src = src[src.index("self.ops = ["):src.index("self.gemm_flops")]
+    names = [l.split('"')[1] for l in ops_src.splitlines() if l.strip().startswith('("')]
+    spans = sorted(bench.CONFIG_OPS.values())
+    assert spans[0][0] == 0 and spans[-1][1] == len(names)
+    assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+    c2, c3, c4 = (names[i0:i1] for i0, i1 in (bench.CONFIG_OPS[k] for k in ("c2", "c3", "c4")))
+    assert c2[-1] == "gemm fprop" and "gemm dgrad" in c3 and "gemm wgrad" in c3
+    assert c4[-1] == "grouped_gemm down"
+
+
+def test_gpus_n_starts_n_ranks():
+    """`bench.py --gpus 2` without a launcher starts two ranks itself
+    (torch.distributed.run on 127.0.0.1); the launch check joins them with
+    gloo on CPU and rank 0 reports n_gpus = 2."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--launch-check"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1 and lines[0]["n_gpus"] == 2 and lines[0]["world_size"] == 2
+
+
 if __name__ == "__main__":
     sys.exit(pytest.main([__file__, "-q"]))

@@ -1,6 +1,13 @@
-"""Full-size parity: one step of the Ultra-shaped workload, in exactly the
-launch configuration the benchmark times (its Workload object, CTA-pair
-GEMMs), checked against the oracle on sampled rows and outputs.
+"""Full-size parity: one step of the Super-shaped and of the Ultra-shaped
+workload, in exactly the launch configuration the benchmark times (its
+Workload object, CTA-pair GEMMs), checked against the oracle on sampled rows
+and outputs.  The Super step covers the Super in_proj fprop (X 8192 x 6144
+with outlier channels, W 18560 x 6144), its backward (dY 8192 x 18560 with
+SR, dgrad over K = 18560, RHT wgrad over 8192 tokens) and the Super LatentMoE
+(latent 1024 -> expert hidden 2688 -> 1024, 180224 routed rows); the Ultra
+step covers the same rows at the Ultra shapes.  Sampled rows and columns
+include the 128-row and 256-row tile edges and the last, possibly partial,
+tile of every axis (N = 18560 and 2688 end on half a 256-column tile).
 
 - Tensor amaxes (X, W, dY, max |RHT(dY)|, RHT(X), every sampled expert) equal
   the oracle's over the whole operand.
@@ -30,14 +37,24 @@ NS_E = 8           # sampled rows per operand of one expert
 BOUNDARY = (127, 128, 255, 256, 257)     # rows at 128-row tile and 256-row pair-tile edges
 
 
-@pytest.fixture(scope="module")
-def run(orc):
+def edges(n: int):
+    """BOUNDARY plus the indices around the start of the last 128- and
+    256-wide tile of an axis of length n, and its last index."""
+    out = set(BOUNDARY) | {n - 1}
+    for t in (128, 256):
+        last = (n - 1) // t * t
+        out |= {last - 1, last}
+    return tuple(sorted(i for i in out if 0 <= i < n))
+
+
+@pytest.fixture(scope="module", params=["super", "ultra"])
+def run(orc, request):
     from nvfp4_precision_02_b300 import binding as B, build
     build.build()
     B.lib()
     assert torch.cuda.is_available()
     import bench
-    wk = bench.Workload("ultra", torch.device("cuda", 0))
+    wk = bench.Workload(request.param, torch.device("cuda", 0))
     wk.step()
     torch.cuda.synchronize()
     assert B.device_status() == 0
@@ -85,8 +102,8 @@ def test_fprop_full_size(run, orc):
     xb, wb = _host(run, "x"), _host(run, "w")
     ax, aw = orc.amax(xb), orc.amax(wb)
     assert float(wk.qx.amax[0]) == ax and float(wk.qw.amax[0]) == aw
-    m_ids = fs.sample_ids(T, NS, 1, must=BOUNDARY)
-    n_ids = fs.sample_ids(N, NS, 2, must=BOUNDARY)
+    m_ids = fs.sample_ids(T, NS, 1, must=edges(T))
+    n_ids = fs.sample_ids(N, NS, 2, must=edges(N))
     xr = fs.rows_1d(orc, xb[m_ids], m_ids, K, ax, RNE)
     wr = fs.rows_2d(orc, lambda n0: wb[n0:n0 + 16], n_ids, K, aw)
     _check_rows("X (1x16 RNE)", orc, xr, wk.qx, m_ids, K)
@@ -100,8 +117,8 @@ def test_dgrad_full_size(run, orc):
     dyb, wb = _host(run, "dy"), _host(run, "w")
     ady, aw = orc.amax(dyb), orc.amax(wb)
     assert float(wk.dy_amax[0]) == ady and float(wk.qdy.amax[0]) == ady
-    m_ids = fs.sample_ids(T, NS, 3, must=BOUNDARY)
-    k_ids = fs.sample_ids(K, NS, 4, must=BOUNDARY)
+    m_ids = fs.sample_ids(T, NS, 3, must=edges(T))
+    k_ids = fs.sample_ids(K, NS, 4, must=edges(K))
     dyr = fs.rows_1d(orc, dyb[m_ids], m_ids, N, ady, SR, wk.seed)
     wtr = fs.rows_2d(orc, lambda k0: np.ascontiguousarray(wb[:, k0:k0 + 16].T), k_ids, N, aw)
     _check_rows("dY (1x16 SR)", orc, dyr, wk.qdy, m_ids, N)
@@ -116,8 +133,8 @@ def test_wgrad_full_size(run, orc):
     ardy, arx = orc.rht_amax(dyb, wk.mask), orc.rht_amax(xb, wk.mask)
     assert float(wk.dy_amax[1]) == ardy and float(wk.sdy.amax[0]) == ardy
     assert float(wk.sx.amax[0]) == arx
-    n_ids = fs.sample_ids(N, NS, 5, must=BOUNDARY)
-    k_ids = fs.sample_ids(K, NS, 6, must=BOUNDARY)
+    n_ids = fs.sample_ids(N, NS, 5, must=edges(N))
+    k_ids = fs.sample_ids(K, NS, 6, must=edges(K))
     sdyr = fs.rows_rht(orc, np.ascontiguousarray(dyb[:, n_ids]), n_ids, T, ardy, wk.mask, SR, wk.wseed)
     sxr = fs.rows_rht(orc, np.ascontiguousarray(xb[:, k_ids]), k_ids, T, arx, wk.mask, RNE, 0)
     _check_rows("RHT(dY)^T (SR)", orc, sdyr, wk.sdy, n_ids, T)
@@ -144,7 +161,7 @@ def _expert_check(run, orc, name, x, qx, qx_sf, offsets, g, w_e, qw, out, seed):
     xb = fs.bits(x[o0:o1])
     am = orc.amax(xb)
     assert float(qx.amax[g]) == am, (name, g)
-    loc = fs.sample_ids(o1 - o0, NS_E, seed, must=BOUNDARY)
+    loc = fs.sample_ids(o1 - o0, NS_E, seed, must=edges(o1 - o0))
     rows = loc + o0
     xr = fs.rows_1d(orc, xb[loc], rows, cols, am, RNE)
     p = orc.group_sf_row(offsets, g)
@@ -153,7 +170,7 @@ def _expert_check(run, orc, name, x, qx, qx_sf, offsets, g, w_e, qw, out, seed):
     n_out = wb.shape[0]
     aw = orc.amax(wb)
     assert float(qw.amax[g]) == aw, (name, g)
-    n_ids = fs.sample_ids(n_out, NS_E, seed + 1, must=BOUNDARY)
+    n_ids = fs.sample_ids(n_out, NS_E, seed + 1, must=edges(n_out))
     wr = fs.rows_2d(orc, lambda n0: wb[n0:n0 + 16], n_ids, cols, aw)
     nsf = B.sf_bytes(n_out, cols)
     _check_rows(f"{name} weight, expert {g}", orc, wr, qw, n_ids, cols, batch=g,
@@ -227,7 +244,7 @@ def test_expert_backward_full_size(run, orc):
         # dgrad operands and outputs
         am = orc.amax(dhb)
         assert float(qdh.amax[g]) == am, g
-        loc = fs.sample_ids(o1 - o0, NS_E, 30 + g, must=BOUNDARY)
+        loc = fs.sample_ids(o1 - o0, NS_E, 30 + g, must=edges(o1 - o0))
         rows = loc + o0
         dr = fs.rows_1d(orc, dhb[loc], rows, Hh, am, SR, wk.seed)
         _check_rows(f"dH (grouped SR), expert {g}", orc, dr, qdh, rows, Hh, sf=qdh_sf,
@@ -235,7 +252,7 @@ def test_expert_backward_full_size(run, orc):
         wub = fs.bits(wk.w_up[g])
         aw = orc.amax(wub)
         assert float(qwt.amax[g]) == aw, g
-        k_ids = fs.sample_ids(L, NS_E, 40 + g, must=BOUNDARY)
+        k_ids = fs.sample_ids(L, NS_E, 40 + g, must=edges(L))
         wtr = fs.rows_2d(orc, lambda k0: np.ascontiguousarray(wub[:, k0:k0 + 16].T), k_ids, Hh, aw)
         _check_rows(f"W_up^T, expert {g}", orc, wtr, qwt, k_ids, Hh, batch=g,
                     sf=qwt.sf[g * nsf:(g + 1) * nsf].cpu().numpy())
@@ -247,8 +264,8 @@ def test_expert_backward_full_size(run, orc):
         kp = segh.shape[0]
         arh, ara = orc.rht_amax(segh, wk.mask), orc.rht_amax(sega, wk.mask)
         assert float(sdh.amax[g]) == arh and float(sa.amax[g]) == ara, g
-        n_ids = fs.sample_ids(Hh, NS_E, 50 + g, must=BOUNDARY)
-        c_ids = fs.sample_ids(L, NS_E, 60 + g, must=BOUNDARY)
+        n_ids = fs.sample_ids(Hh, NS_E, 50 + g, must=edges(Hh))
+        c_ids = fs.sample_ids(L, NS_E, 60 + g, must=edges(L))
         hr = fs.rows_rht(orc, np.ascontiguousarray(segh[:, n_ids]), n_ids, kp, arh, wk.mask, SR, wk.wseed,
                          index_stride=kt, index_offset=ko)
         ar = fs.rows_rht(orc, np.ascontiguousarray(sega[:, c_ids]), c_ids, kp, ara, wk.mask, RNE, 0,
@@ -269,7 +286,7 @@ def test_ptq_mse_scales_full_size(run, orc):
     aw = orc.amax(_host(run, "w"))
     amax_in = torch.tensor([aw], dtype=torch.float32, device=wk.w.device)
     q = B.quantize_1d_mse(wk.w, amax_in=amax_in)
-    ids = fs.sample_ids(N, NS, 70, must=BOUNDARY)
+    ids = fs.sample_ids(N, NS, 70, must=edges(N))
     wb = _host(run, "w")
     orows = fs.OracleRows(len(ids), K, aw)
     for i, n in enumerate(ids):

@@ -583,3 +583,17 @@ def test_mse_block_scales_minimise_the_error(orc):
             kk = _e2m1_rne_np(blk * float(np.float32(s_enc) / np.float32(e4m3[c])))
             assert ((codes[r, 16 * b:16 * b + 16] & 7) == kk).all()
     assert differs > 0                                               # the search does change scales
+
+
+def test_mse_block_scale_ties_keep_the_largest(orc):
+    """Hand-worked blocks where several E4M3 scales rebuild the block exactly
+    (error 0 in FP32): the oracle keeps the largest of them (R16), not the
+    smallest or the first found."""
+    with open(os.path.join(GOLD, "mse_ties.json")) as f:
+        gold = json.load(f)
+    for blk in gold["blocks"]:
+        x = _bf16(np.array([blk["x"]], dtype=np.float64))
+        q = orc.quantize_1d_mse(x, amax_in=blk["amax"])
+        sf = int(q["sf"][orc.sf_offset(0, 0, 16)])
+        assert sf == blk["sf"] != blk["smallest_tied_sf"], (blk["name"], sf)
+        assert _unpack(q["codes"], 16)[0].tolist() == blk["codes"], blk["name"]
