@@ -75,7 +75,8 @@ constexpr int G2_B_BYTES = G_B_BYTES / 2;                                       
 constexpr int G2_STAGE_BYTES = G_A_BYTES + G2_B_BYTES + G_SFA_BYTES + G_SFB_BYTES;  // 38912
 constexpr int G_W_TMA = 0, G_W_MMA = 1, G_W_SF0 = 2, G_W_EPI0 = 6;
 constexpr int G_EPI_WARPS = 16;
-constexpr int G_THREADS = (G_W_EPI0 + G_EPI_WARPS) * 32;   // 704
+constexpr int G_W_SFP = G_W_EPI0 + G_EPI_WARPS;             // 22: scale-atom producer
+constexpr int G_THREADS = (G_W_SFP + 1) * 32;               // 736
 constexpr int G_TMEM_COLS = 512;
 constexpr int G_SF_COL0 = 256;
 constexpr int G_SF_COLS_PER_STAGE = 48;
@@ -307,6 +308,53 @@ __device__ __forceinline__ void tc_mma4(uint32_t d, uint64_t a, uint64_t b, uint
     else NVFP4_MMA4_ASM(1);
 }
 #undef NVFP4_MMA4_ASM
+
+// One whole K stage from one asm block: the four MMAs of tc_mma4, then the
+// commit of the stage to its empty barrier (in both CTAs of a pair), and,
+// between the first and the second MMA, a non-blocking test of the next
+// stage's two barriers (full and sf_full, parity ph_next).  Returns 1 when
+// both had completed.  The tensor pipe accepts an MMA only shortly before it
+// can start it, so the issuing thread spends most of a stage blocked in MMA
+// issue; testing the next stage's barriers there hides their latency, which
+// would otherwise be idle tensor time between stages.
+#define NVFP4_MMA4_PEEK_ASM(CG, COMMIT)                                                                      \
+    asm volatile(                                                                                            \
+        "{\n\t.reg .pred p, t, f1, f2;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"                             \
+        ".reg .b32 sa1, sa2, sa3, sb1, sb2, sb3;\n\t"                                                        \
+        "setp.ne.b32 p, %5, 0;\n\t"                                                                          \
+        "setp.eq.u32 t, 0, 0;\n\t"                                                                           \
+        "add.s64 a1, %2, 2;\n\tadd.s64 a2, %2, 4;\n\tadd.s64 a3, %2, 6;\n\t"                                \
+        "add.s64 b1, %3, 2;\n\tadd.s64 b2, %3, 4;\n\tadd.s64 b3, %3, 6;\n\t"                                \
+        "add.u32 sa1, %6, 4;\n\tadd.u32 sa2, %6, 8;\n\tadd.u32 sa3, %6, 12;\n\t"                            \
+        "add.u32 sb1, %7, 8;\n\tadd.u32 sb2, %7, 16;\n\tadd.u32 sb3, %7, 24;\n\t"                           \
+        "tcgen05.mma.cta_group::" #CG ".kind::mxf4nvf4.block_scale.scale_vec::4X [%1], %2, %3, %4, [%6], [%7], p;\n\t" \
+        "mbarrier.test_wait.parity.shared::cta.b64 f1, [%9], %11;\n\t"                                        \
+        "mbarrier.test_wait.parity.shared::cta.b64 f2, [%10], %11;\n\t"                                       \
+        "tcgen05.mma.cta_group::" #CG ".kind::mxf4nvf4.block_scale.scale_vec::4X [%1], a1, b1, %4, [sa1], [sb1], t;\n\t" \
+        "tcgen05.mma.cta_group::" #CG ".kind::mxf4nvf4.block_scale.scale_vec::4X [%1], a2, b2, %4, [sa2], [sb2], t;\n\t" \
+        "tcgen05.mma.cta_group::" #CG ".kind::mxf4nvf4.block_scale.scale_vec::4X [%1], a3, b3, %4, [sa3], [sb3], t;\n\t" \
+        COMMIT                                                                                               \
+        "and.pred f1, f1, f2;\n\t"                                                                           \
+        "selp.u32 %0, 1, 0, f1;\n\t}"                                                                        \
+        : "=r"(ready)                                                                                        \
+        : "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb), "r"(empty_bar),             \
+          "r"(full_next), "r"(sff_next), "r"(ph_next)                                                        \
+        : "memory")
+
+template <bool PAIR>
+__device__ __forceinline__ uint32_t tc_mma4_commit_peek(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                                        uint32_t sfa, uint32_t sfb, uint32_t accumulate,
+                                                        uint32_t empty_bar, uint32_t full_next, uint32_t sff_next,
+                                                        uint32_t ph_next) {
+    uint32_t ready;
+    if (PAIR)
+        NVFP4_MMA4_PEEK_ASM(2, "{\n\t.reg .b16 msk;\n\tmov.b16 msk, 3;\n\t"
+                               "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%8], msk;\n\t}\n\t");
+    else
+        NVFP4_MMA4_PEEK_ASM(1, "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t");
+    return ready;
+}
+#undef NVFP4_MMA4_PEEK_ASM
 
 // ------------------------------------------------------------------ CTA pairs
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -665,26 +713,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 // PAIR: this CTA loads B rows 128 * rank .. + 127 of the 256-row tile
                 const int32_t brow0 =
                     (int32_t)(tc.g * b_rows_per_group + (int64_t)tc.nt * G_BN + (PAIR ? 128 * (int64_t)rank : 0));
-                const uint8_t* sfb_g = p.sfb + (int64_t)tc.g * p.sfb_group_stride;
-                const bool rb2 = (tc.nt * 2 + 1) < nrb;
-                const int ka = tile_atoms(tc), kst = (ka + 3) / 4, kc0 = tc.k0 / 64;
+                const int ka = tile_atoms(tc), kst = (ka + 3) / 4;
                 for (int ks = 0; ks < kst; ++ks) {
                     if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) { ok = false; break; }
-                    const int na = min(4, ka - 4 * ks);
-                    const uint32_t sfbytes = (uint32_t)na * 512u;
                     const uint32_t st = smem_u32(stages + s * STAGE_BYTES);
-                    // the scales first, on their own barrier: they are small, land
-                    // ahead of A and B, and the scale warps move them into TMEM
-                    // while A and B are still arriving
-                    const uint32_t sbar = sfl0 + 8 * s;
-                    mbar_expect_tx(sbar, sfbytes * (rb2 ? 3u : 2u));
-                    const uint32_t ssf = st + G_A_BYTES + L::B_BYTES;
-                    bulk_load(ssf, p.sfa + ((int64_t)tc.mtg * katoms + kc0 + 4 * ks) * 512, sfbytes, sbar);
-                    bulk_load(ssf + G_SFA_BYTES, sfb_g + ((int64_t)(tc.nt * 2) * katoms + kc0 + 4 * ks) * 512, sfbytes,
-                              sbar);
-                    if (rb2)
-                        bulk_load(ssf + G_SFA_BYTES + 2048,
-                                  sfb_g + ((int64_t)(tc.nt * 2 + 1) * katoms + kc0 + 4 * ks) * 512, sfbytes, sbar);
                     const int32_t kx = tc.k0 / 2 + ks * 128;     // byte column of the K stage
                     if (PAIR) {
                         // A and B of both CTAs complete on rank 0's full barrier
@@ -709,22 +741,67 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 // gives its copies a fixed millisecond instead)
                 volatile int never = 0;
                 for (int i = 0; i < G_STAGES; ++i)
-                    if ((issued >> i) & 1u) {
-                        mbar_wait(sfl0 + 8 * i, (issued_ph >> i) & 1u, &never);
-                        if (rank == 0) mbar_wait(full0 + 8 * i, (issued_ph >> i) & 1u, &never);
-                    }
+                    if (((issued >> i) & 1u) && rank == 0) mbar_wait(full0 + 8 * i, (issued_ph >> i) & 1u, &never);
                 if (PAIR && rank != 0) {
                     const uint64_t t0 = globaltimer_ns();
                     while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
                 }
             }
         }
+    } else if (warp == G_W_SFP) {
+        // ------------------------------------------------ scale-atom producer
+        // The stage's scale atoms (A: 4 atoms of its m-tile, B: 4 atoms of each
+        // of the tile's two 128-row blocks) by cp.async.bulk on the stage's
+        // landing barrier.  A thread of its own: copy issue takes tens of
+        // nanoseconds per copy on this part, and the A/B producer's two tensor
+        // copies per stage already take a good part of a stage.
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, issued = 0, issued_ph = 0;
+            bool ok = true;
+            for (int64_t t = t_first; t < total && ok; t += t_step) {
+                const TileCoord tc = tile_at(t);
+                const uint8_t* sfb_g = p.sfb + (int64_t)tc.g * p.sfb_group_stride;
+                const bool rb2 = (tc.nt * 2 + 1) < nrb;
+                const int ka = tile_atoms(tc), kst = (ka + 3) / 4, kc0 = tc.k0 / 64;
+                const uint8_t* sa = p.sfa + ((int64_t)tc.mtg * katoms + kc0) * 512;
+                const uint8_t* sb = sfb_g + ((int64_t)(tc.nt * 2) * katoms + kc0) * 512;
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) { ok = false; break; }
+                    const int na = min(4, ka - 4 * ks);
+                    const uint32_t sfbytes = (uint32_t)na * 512u;
+                    const uint32_t ssf = smem_u32(stages + s * STAGE_BYTES) + G_A_BYTES + L::B_BYTES;
+                    const uint32_t sbar = sfl0 + 8 * s;
+                    mbar_expect_tx(sbar, sfbytes * (rb2 ? 3u : 2u));
+                    bulk_load(ssf, sa + 2048 * ks, sfbytes, sbar);
+                    bulk_load(ssf + G_SFA_BYTES, sb + 2048 * ks, sfbytes, sbar);
+                    if (rb2) bulk_load(ssf + G_SFA_BYTES + 2048, sb + (int64_t)katoms * 512 + 2048 * ks, sfbytes, sbar);
+                    issued |= 1u << s;
+                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                    if (++s == G_STAGES) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) {
+                volatile int never = 0;
+                for (int i = 0; i < G_STAGES; ++i)
+                    if ((issued >> i) & 1u) mbar_wait(sfl0 + 8 * i, (issued_ph >> i) & 1u, &never);
+            }
+        }
     } else if (warp == G_W_MMA) {
         // ------------------------------------------------ MMA issuer (rank 0 of a pair)
+        // A stage may start when its full barrier (A and B landed, both CTAs'
+        // in a pair) and its sf_full barrier (scales in TMEM) have completed.
+        // The tensor pipe holds little work ahead of the issuing thread, so
+        // every cycle this thread spends between stages is an idle tensor
+        // cycle: a whole stage is one asm block that also tests the next
+        // stage's barriers while the MMAs issue (`ready`), and the blocking
+        // waits run only when that test found them incomplete.
         if (lane == 0 && rank == 0) {
             const uint32_t idesc = mxf4nvf4_idesc(PAIR ? 2 * G_BM : G_BM, G_BN);
+            const uint64_t ad0 = smem_desc(smem_u32(stages), 16, 1024, 2);
+            const uint64_t bd0 = smem_desc(smem_u32(stages) + G_A_BYTES, 16, 1024, 2);
             int s = 0;
-            uint32_t ph = 0, it = 0;
+            uint32_t ph = 0, it = 0, ready = 0;
             bool ok = true;
             for (int64_t t = t_first; t < total && ok; t += t_step, ++it) {
                 if (!mbar_wait(acc_empty, (it & 1u) ^ 1u, abort_flag)) { ok = false; break; }
@@ -733,27 +810,32 @@ __global__ void __launch_bounds__(G_THREADS, 1)
                 // epilogue writes zeros
                 const int ka = KGROUP ? tile_at(t).ka : katoms, kst = (ka + 3) / 4;
                 for (int ks = 0; ks < kst; ++ks) {
-                    if (!mbar_wait(full0 + 8 * s, ph, abort_flag) || !mbar_wait(sff0 + 8 * s, ph, abort_flag)) {
+                    if (!ready && (!mbar_wait(full0 + 8 * s, ph, abort_flag) || !mbar_wait(sff0 + 8 * s, ph, abort_flag))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const int na = min(4, ka - 4 * ks);
-                    const uint32_t st = smem_u32(stages + s * STAGE_BYTES);
+                    // descriptor start addresses are in 16-byte units (bits 0-13)
+                    const uint64_t soff = (uint64_t)((s * STAGE_BYTES) >> 4);
+                    const uint64_t ad = ad0 + soff, bd = bd0 + soff;
                     const uint32_t sfa_t = tmem + G_SF_COL0 + s * G_SF_COLS_PER_STAGE;
                     const uint32_t sfb_t = sfa_t + 16;
-                    const uint64_t ad = smem_desc(st, 16, 1024, 2);
-                    const uint64_t bd = smem_desc(st + G_A_BYTES, 16, 1024, 2);
+                    const int sn = s + 1 == G_STAGES ? 0 : s + 1;
+                    const uint32_t phn = s + 1 == G_STAGES ? ph ^ 1u : ph;
                     if (na == 4) {
-                        tc_mma4<PAIR>(tmem, ad, bd, idesc, sfa_t, sfb_t, ks != 0 ? 1u : 0u);
+                        ready = tc_mma4_commit_peek<PAIR>(tmem, ad, bd, idesc, sfa_t, sfb_t, ks != 0 ? 1u : 0u,
+                                                          empty0 + 8 * s, full0 + 8 * sn, sff0 + 8 * sn, phn);
                     } else {
                         for (int j = 0; j < na; ++j)
                             tc_mma<PAIR>(tmem, ad + 2 * j, bd + 2 * j, idesc, sfa_t + 4 * j, sfb_t + 8 * j,
                                          (ks | j) != 0 ? 1u : 0u);
+                        if (PAIR) tc_commit_pair(empty0 + 8 * s, 3);
+                        else tc_commit(empty0 + 8 * s);
+                        ready = 0;
                     }
-                    if (PAIR) tc_commit_pair(empty0 + 8 * s, 3);
-                    else tc_commit(empty0 + 8 * s);
-                    if (++s == G_STAGES) { s = 0; ph ^= 1u; }
+                    s = sn;
+                    ph = phn;
                 }
                 if (!ok) break;
                 if (PAIR) tc_commit_pair(acc_full, 3);
@@ -767,12 +849,12 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         }
     } else if (warp < G_W_EPI0) {
         // ------------------------------------------------ scale factors -> TMEM
-        // The producer lands the stage's scale atoms in shared memory next to
-        // A and B (on their own barrier, ahead of A and B).  Lane i of every
-        // quarter copies the 16 bytes at offset 16*i of each 512-byte atom (the
-        // 4 scales of rows i, i+32, i+64, i+96) into the atom's 4 TMEM columns.
+        // The scale producer lands the stage's scale atoms in shared memory
+        // next to A and B (on their own barrier).  Lane i of every quarter
+        // copies the 16 bytes at offset 16*i of each 512-byte atom (the 4
+        // scales of rows i, i+32, i+64, i+96) into the atom's 4 TMEM columns.
         // The stage's TMEM columns are free once its data has landed: the
-        // producer refilled it only after the MMAs of its previous use
+        // producers refilled it only after the MMAs of its previous use
         // completed.  In a CTA pair each CTA writes its own A scales and all
         // 256 rows of B scales into its own TMEM.
         const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
