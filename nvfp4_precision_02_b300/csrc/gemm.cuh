@@ -84,18 +84,24 @@ constexpr int G_BAND = 16;                                   // m-tiles per rast
 constexpr uint64_t G_WAIT_NS = 4000000000ull;                // bounded waits: 4 s
 constexpr int G_BAR_BYTES = 256;                             // barriers, TMEM slot, abort flag
 
-constexpr int G_STORE_WARP_BYTES = 2048;                     // bf16 staging of one epilogue warp: 32 x 32
+constexpr int G_STORE_WARP_BYTES = 2048;   // staging of one epilogue warp: 32 rows x 64 bytes (32 bf16 or 16 FP32)
+
+// Tile schedules (a compile-time parameter of the kernel): one dense GEMM,
+// groups along M (the routed-expert GEMM: per-expert rows and weights), or
+// groups along K (the expert wgrad: per-expert token segments).
+constexpr int G_DENSE = 0, G_MGROUP = 1, G_KGROUP = 2;
 
 // Shared-memory layout of one CTA (after 1 KB alignment): the stage ring,
-// the bf16 store staging (TMA-store epilogue only), barriers, group tables.
-// The TMA-store epilogue gives up one stage for the 32 KB staging: it pays
-// when K is short (the epilogue of a tile is then as long as its mainloop),
-// while long-K GEMMs keep four stages and store directly.
-template <bool TMA_STORE, bool PAIR = false>
+// the output staging of the TMA-store epilogue, barriers, group tables.
+// A CTA pair keeps five stages with the 32 KB staging when its group tables
+// are small (dense GEMMs); the 512-expert tables of a grouped GEMM leave room
+// for four.  A single CTA's 54 KB stages leave room for three beside the
+// staging, four without it.
+template <bool TMA_STORE, bool PAIR = false, bool DENSE = false>
 struct GemmLayout {
     static constexpr int STAGE_BYTES = PAIR ? G2_STAGE_BYTES : G_STAGE_BYTES;
     static constexpr int B_BYTES = PAIR ? G2_B_BYTES : G_B_BYTES;
-    static constexpr int STAGES = PAIR ? (TMA_STORE ? 4 : 5) : (TMA_STORE ? 3 : 4);
+    static constexpr int STAGES = PAIR ? ((TMA_STORE && !DENSE) ? 4 : 5) : (TMA_STORE ? 3 : 4);
     static constexpr int STORE_OFF = STAGES * STAGE_BYTES;
     static constexpr int STORE_BYTES = TMA_STORE ? G_EPI_WARPS * G_STORE_WARP_BYTES : 0;
     static constexpr int BAR_OFF = STORE_OFF + STORE_BYTES;
@@ -104,15 +110,16 @@ struct GemmLayout {
 
 // dynamic shared memory: 1 KB alignment slack, layout, group tables (row
 // offsets, 128-row padded offsets and, for CTA pairs, 256-row padded offsets)
-__host__ __device__ constexpr int gemm_smem_bytes(bool tma_store, int groups, bool pair = false) {
+__host__ __device__ constexpr int gemm_smem_bytes(bool tma_store, int groups, bool pair, bool dense) {
     return 1024 +
-           (pair ? (tma_store ? GemmLayout<true, true>::TAB_OFF : GemmLayout<false, true>::TAB_OFF)
+           (pair ? (tma_store ? (dense ? GemmLayout<true, true, true>::TAB_OFF : GemmLayout<true, true>::TAB_OFF)
+                              : GemmLayout<false, true>::TAB_OFF)
                  : (tma_store ? GemmLayout<true>::TAB_OFF : GemmLayout<false>::TAB_OFF)) +
            (pair ? 3 : 2) * 4 * (groups + 1);
 }
-
-// K below which a bf16 GEMM takes the TMA-store epilogue.
-constexpr int64_t G_TMA_STORE_MAX_K = 8192;
+static_assert(gemm_smem_bytes(true, 1, true, true) <= 227 * 1024, "dense pair layout exceeds shared memory");
+static_assert(gemm_smem_bytes(true, 512, true, false) <= 227 * 1024, "grouped pair layout exceeds shared memory");
+static_assert(gemm_smem_bytes(true, 512, false, false) <= 227 * 1024, "grouped layout exceeds shared memory");
 
 struct GemmParams {
     int64_t M;                  // rows of A (dense) / total rows R (grouped)
@@ -599,14 +606,16 @@ __device__ __forceinline__ TileCoord decode_kgroup_tile(int64_t t, int mt, int n
 __device__ __forceinline__ uint4 ldg_u4(const uint8_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
 // ------------------------------------------------------------------ kernel
-// OUT_FP32: FP32 output (stored directly); otherwise bf16.  TMA_STORE (bf16
-// only): the output leaves through tm_c (rows 16-byte aligned).
-template <bool OUT_FP32, bool TMA_STORE, bool PAIR, bool KGROUP = false>
+// OUT_FP32: FP32 output, otherwise bf16.  TMA_STORE: the output leaves
+// through tm_c (rows 16-byte aligned) in boxes of 32 rows x 64 bytes staged
+// in shared memory; otherwise it is stored directly.  SCHED: G_DENSE,
+// G_MGROUP or G_KGROUP.
+template <bool OUT_FP32, bool TMA_STORE, bool PAIR, int SCHED = G_DENSE>
 __global__ void __launch_bounds__(G_THREADS, 1)
     k_gemm_nvfp4(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                  const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
-    static_assert(!(OUT_FP32 && TMA_STORE), "the TMA-store epilogue is bf16 only");
-    using L = GemmLayout<TMA_STORE, PAIR>;
+    constexpr bool KGROUP = SCHED == G_KGROUP;
+    using L = GemmLayout<TMA_STORE, PAIR, SCHED == G_DENSE>;
     constexpr int G_STAGES = L::STAGES;
     constexpr int STAGE_BYTES = L::STAGE_BYTES;
     static_assert(G_SF_COL0 + G_STAGES * G_SF_COLS_PER_STAGE <= G_TMEM_COLS, "scale columns exceed TMEM");
@@ -922,7 +931,96 @@ __global__ void __launch_bounds__(G_THREADS, 1)
             const uint32_t vmask = (KGROUP && tc.ka == 0) ? 0u : 0xFFFFFFFFu;
             const int64_t row = crow0 + r;
             const int64_t col0 = (int64_t)tc.nt * G_BN + chunk * 64;
-            if (OUT_FP32) {
+            if (TMA_STORE) {
+                // Boxes of 32 rows x 64 bytes (32 bf16 or 16 FP32 columns): load the
+                // box's columns from TMEM, scale (and round), then store the box
+                // through this warp's 64B-swizzled staging buffer.  The accumulator
+                // is released after the last box's load.  A box whose 32 rows all
+                // belong to the tile leaves by TMA store; other rows (an expert's
+                // last rows in a grouped GEMM) are stored directly.
+                constexpr int BOXES = OUT_FP32 ? 4 : 2, BOX_COLS = OUT_FP32 ? 16 : 32, ESZ = OUT_FP32 ? 4 : 2;
+                const bool rows_full = (q * 32 + 31) < tc.rows;
+                const uint32_t stage_buf = smem_u32(smem + L::STORE_OFF + (warp - G_W_EPI0) * G_STORE_WARP_BYTES);
+#pragma unroll
+                for (int b = 0; b < BOXES; ++b) {
+                    uint32_t w[16];
+                    if (OUT_FP32) {
+                        tc_ld_32x32b_x16(taddr + 16 * b, w);
+                        tc_wait_ld();
+                        if (b == BOXES - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) { if (PAIR) mbar_arrive_cluster(acc_release); else mbar_arrive(acc_empty); }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(w[i] & vmask)));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            uint32_t v[16];
+                            tc_ld_32x32b_x16(taddr + 32 * b + 16 * k, v);
+                            tc_wait_ld();
+                            if (b == BOXES - 1 && k == 1) {
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) { if (PAIR) mbar_arrive_cluster(acc_release); else mbar_arrive(acc_empty); }
+                            }
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(v[2 * j] & vmask)),
+                                                                                __fmul_rn(alpha, __uint_as_float(v[2 * j + 1] & vmask)));
+                                w[8 * k + j] = *reinterpret_cast<const uint32_t*>(&b2);
+                            }
+                        }
+                    }
+                    const int64_t cstart = col0 + b * BOX_COLS;
+                    if (cstart >= p.N) continue;
+                    if (p.c_amax != nullptr) {
+                        const int valid = r < tc.rows ? (int)(p.N - cstart >= BOX_COLS ? BOX_COLS : p.N - cstart) : 0;
+                        if (OUT_FP32) {
+                            uint32_t m = 0;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) m = max(m, i < valid ? (w[i] & 0x7FFFFFFFu) : 0u);
+                            amax_run = max(amax_run, m);
+                        } else {
+                            amax_run = max(amax_run, bf16_absmax(w, valid) << 16);
+                        }
+                    }
+                    if (rows_full) {
+                        // the staging buffer is free once the previous box has been read
+                        if (lane == 0) bulk_wait_read0();
+                        __syncwarp();
+                        // row `lane`, 16-byte chunk j at lane*64 + 16*(j ^ ((lane >> 1) & 3))
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t addr = stage_buf + lane * 64 + 16 * (j ^ ((lane >> 1) & 3));
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * j]),
+                                         "r"(w[4 * j + 1]), "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tm_c, stage_buf, (int32_t)cstart, (int32_t)(crow0 + q * 32));
+                            bulk_commit();
+                        }
+                    } else if (r < tc.rows) {
+                        uint8_t* out = reinterpret_cast<uint8_t*>(p.c) + (row * p.ldc + cstart) * ESZ;
+                        if (cstart + BOX_COLS <= p.N) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                reinterpret_cast<uint4*>(out)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < BOX_COLS; ++i) {
+                                if (cstart + i >= p.N) continue;
+                                if (OUT_FP32) reinterpret_cast<uint32_t*>(out)[i] = w[i];
+                                else reinterpret_cast<uint16_t*>(out)[i] = (uint16_t)(w[i / 2] >> (16 * (i & 1)));
+                            }
+                        }
+                    }
+                }
+            } else if (OUT_FP32) {
                 // two 32-column halves: load, scale, store; release after the second load
                 const bool live = r < tc.rows && col0 < p.N;
 #pragma unroll
@@ -958,71 +1056,6 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             if (cstart + i < p.N) out[i] = __uint_as_float(v[i]);
-                    }
-                }
-            } else if (TMA_STORE) {
-                // two 32-column halves: load, scale, round; release after the second load.
-                // A half whose 32 rows all belong to the tile goes out as one TMA
-                // store box (32 x 32 bf16) from this warp's 64B-swizzled staging
-                // buffer; other rows are stored directly.
-                const bool rows_full = (q * 32 + 31) < tc.rows;
-                const uint32_t stage_buf = smem_u32(smem + L::STORE_OFF + (warp - G_W_EPI0) * G_STORE_WARP_BYTES);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        uint32_t v[16];
-                        tc_ld_32x32b_x16(taddr + 32 * h + 16 * k, v);
-                        tc_wait_ld();
-                        if (h == 1 && k == 1) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) { if (PAIR) mbar_arrive_cluster(acc_release); else mbar_arrive(acc_empty); }
-                        }
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(alpha, __uint_as_float(v[2 * j] & vmask)),
-                                                                            __fmul_rn(alpha, __uint_as_float(v[2 * j + 1] & vmask)));
-                            w[8 * k + j] = *reinterpret_cast<const uint32_t*>(&b2);
-                        }
-                    }
-                    const int64_t cstart = col0 + 32 * h;
-                    if (cstart >= p.N) continue;
-                    if (p.c_amax != nullptr) {
-                        const int valid = r < tc.rows ? (int)(p.N - cstart >= 32 ? 32 : p.N - cstart) : 0;
-                        amax_run = max(amax_run, bf16_absmax(w, valid) << 16);
-                    }
-                    if (rows_full) {
-                        // the staging buffer is free once the previous box has been read
-                        if (lane == 0) bulk_wait_read0();
-                        __syncwarp();
-                        // row `lane`, 16-byte chunk j at lane*64 + 16*(j ^ ((lane >> 1) & 3))
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t addr = stage_buf + lane * 64 + 16 * (j ^ ((lane >> 1) & 3));
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * j]),
-                                         "r"(w[4 * j + 1]), "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
-                                         : "memory");
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tm_c, stage_buf, (int32_t)cstart, (int32_t)(crow0 + q * 32));
-                            bulk_commit();
-                        }
-                    } else if (r < tc.rows) {
-                        uint16_t* out = reinterpret_cast<uint16_t*>(p.c) + row * p.ldc + cstart;
-#pragma unroll
-                        for (int i = 0; i < 32; i += 8) {
-                            if (cstart + i + 8 <= p.N) {
-                                *reinterpret_cast<uint4*>(out + i) = make_uint4(w[i / 2], w[i / 2 + 1], w[i / 2 + 2], w[i / 2 + 3]);
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 8; ++j)
-                                    if (cstart + i + j < p.N) out[i + j] = (uint16_t)(w[(i + j) / 2] >> (16 * ((i + j) & 1)));
-                            }
-                        }
                     }
                 }
             } else {

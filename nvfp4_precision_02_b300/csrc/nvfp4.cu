@@ -640,10 +640,10 @@ static bool use_pair() {
     return !(e != nullptr && e[0] == '0');
 }
 
-template <bool F32, bool TS, bool PAIR, bool KG = false>
+template <bool F32, bool TS, bool PAIR, int SCHED>
 static nvfp4_status launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                                const GemmParams& p, int grid, int smem, nvfp4_stream_t stream) {
-    auto kern = k_gemm_nvfp4<F32, TS, PAIR, KG>;
+    auto kern = k_gemm_nvfp4<F32, TS, PAIR, SCHED>;
     if (!PAIR) {
         kern<<<grid, G_THREADS, smem, stream>>>(ma, mb, mc, p);
         return launched("k_gemm_nvfp4");
@@ -664,26 +664,37 @@ static nvfp4_status launch_one(const CUtensorMap& ma, const CUtensorMap& mb, con
     return launched("k_gemm_nvfp4 pair");
 }
 
-template <bool F32, bool TS, bool PAIR, bool KG = false>
+template <bool F32, bool TS, bool PAIR, int SCHED>
 static nvfp4_status set_gemm_attr() {
-    NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<F32, TS, PAIR, KG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             gemm_smem_bytes(TS, NVFP4_MAX_GROUPS, PAIR)),
+    const int groups = SCHED == G_DENSE ? 1 : NVFP4_MAX_GROUPS;
+    NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<F32, TS, PAIR, SCHED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             gemm_smem_bytes(TS, groups, PAIR, SCHED == G_DENSE)),
                         "smem attr"));
     if (PAIR)
-        NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<F32, TS, PAIR, KG>,
+        NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_gemm_nvfp4<F32, TS, PAIR, SCHED>,
                                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 0),
                             "cluster attr"));
     return NVFP4_OK;
 }
 
-// Largest number of co-resident CTA pairs of the pair kernel (the grid is
-// sized to it: the kernel is persistent over tiles).
-template <bool F32, bool TS>
-static nvfp4_status pair_clusters(int smem, int* out) {
+// Attributes of the four output modes (bf16 / FP32, direct / TMA store) of
+// one schedule and CTA arrangement.
+template <bool PAIR, int SCHED>
+static nvfp4_status set_gemm_attrs() {
+    NVFP4_TRY((set_gemm_attr<false, false, PAIR, SCHED>()));
+    NVFP4_TRY((set_gemm_attr<false, true, PAIR, SCHED>()));
+    NVFP4_TRY((set_gemm_attr<true, false, PAIR, SCHED>()));
+    NVFP4_TRY((set_gemm_attr<true, true, PAIR, SCHED>()));
+    return NVFP4_OK;
+}
+
+// Largest number of co-resident CTA pairs of the pair kernel in its largest
+// layout (the grid is sized to it: the kernel is persistent over tiles).
+static nvfp4_status pair_clusters(int* out) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2);
     cfg.blockDim = dim3(G_THREADS);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = std::max(gemm_smem_bytes(true, 1, true, true), gemm_smem_bytes(true, NVFP4_MAX_GROUPS, true, false));
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -692,84 +703,83 @@ static nvfp4_status pair_clusters(int smem, int* out) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    NVFP4_TRY(cuda_call(cudaOccupancyMaxActiveClusters(&n, k_gemm_nvfp4<F32, TS, true>, &cfg), "cluster occupancy"));
+    NVFP4_TRY(cuda_call(cudaOccupancyMaxActiveClusters(&n, k_gemm_nvfp4<false, true, true, G_DENSE>, &cfg),
+                        "cluster occupancy"));
     *out = n;
     return NVFP4_OK;
 }
 
+template <bool PAIR, int SCHED>
+static nvfp4_status launch_mode(bool f32, bool ts, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                                const GemmParams& p, int grid, int smem, nvfp4_stream_t stream) {
+    if (f32) return ts ? launch_one<true, true, PAIR, SCHED>(ma, mb, mc, p, grid, smem, stream)
+                       : launch_one<true, false, PAIR, SCHED>(ma, mb, mc, p, grid, smem, stream);
+    return ts ? launch_one<false, true, PAIR, SCHED>(ma, mb, mc, p, grid, smem, stream)
+              : launch_one<false, false, PAIR, SCHED>(ma, mb, mc, p, grid, smem, stream);
+}
+
 // tiles_1cta: output tiles of 128 x 256 (grid bound of the single-CTA
-// kernel); pair_tiles: tiles of 256 x 256.  kgroup: groups split K (the
-// expert wgrad; FP32 or TMA-stored bf16 outputs).
+// kernel); pair_tiles: tiles of 256 x 256.  sched: G_DENSE, G_MGROUP or
+// G_KGROUP.  tma_store: C's rows are 16-byte aligned and mc maps it.
 static nvfp4_status launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                                 const GemmParams& p, int64_t tiles_1cta, int64_t pair_tiles, int sms,
                                 nvfp4_out_dtype dt, bool tma_store, bool pair, nvfp4_stream_t stream, int dev,
-                                bool kgroup = false) {
+                                int sched) {
     const bool f32 = dt == NVFP4_OUT_FP32;
-    const int smem = gemm_smem_bytes(tma_store, p.groups, pair);
+    const int smem = gemm_smem_bytes(tma_store, p.groups, pair, sched == G_DENSE);
     int clusters = 0;
     {
         std::lock_guard<std::mutex> lk(g_dev_mu);
         if (!g_dev[dev].gemm_attr) {
-            NVFP4_TRY((set_gemm_attr<false, false, false>()));
-            NVFP4_TRY((set_gemm_attr<false, true, false>()));
-            NVFP4_TRY((set_gemm_attr<true, false, false>()));
-            NVFP4_TRY((set_gemm_attr<false, false, true>()));
-            NVFP4_TRY((set_gemm_attr<false, true, true>()));
-            NVFP4_TRY((set_gemm_attr<true, false, true>()));
-            NVFP4_TRY((set_gemm_attr<true, false, false, true>()));
-            NVFP4_TRY((set_gemm_attr<false, true, false, true>()));
-            NVFP4_TRY((set_gemm_attr<true, false, true, true>()));
-            NVFP4_TRY((set_gemm_attr<false, true, true, true>()));
-            const int full = gemm_smem_bytes(true, NVFP4_MAX_GROUPS, true);   // the largest pair layout
-            int c0 = 0, c1 = 0, c2 = 0;
-            NVFP4_TRY((pair_clusters<false, false>(full, &c0)));
-            NVFP4_TRY((pair_clusters<false, true>(full, &c1)));
-            NVFP4_TRY((pair_clusters<true, false>(full, &c2)));
-            g_dev[dev].pair_clusters = std::min(c0, std::min(c1, c2));
+            NVFP4_TRY((set_gemm_attrs<false, G_DENSE>()));
+            NVFP4_TRY((set_gemm_attrs<false, G_MGROUP>()));
+            NVFP4_TRY((set_gemm_attrs<false, G_KGROUP>()));
+            NVFP4_TRY((set_gemm_attrs<true, G_DENSE>()));
+            NVFP4_TRY((set_gemm_attrs<true, G_MGROUP>()));
+            NVFP4_TRY((set_gemm_attrs<true, G_KGROUP>()));
+            int c = 0;
+            NVFP4_TRY(pair_clusters(&c));
+            g_dev[dev].pair_clusters = c;
             g_dev[dev].gemm_attr = true;
         }
         clusters = g_dev[dev].pair_clusters;
     }
-    if (kgroup && !f32 && !tma_store) return fail(NVFP4_ERR_ALIGN, "bf16 output of a K-grouped GEMM needs 16-byte rows");
+    if (sched == G_KGROUP && !f32 && !tma_store)
+        return fail(NVFP4_ERR_ALIGN, "bf16 output of a K-grouped GEMM needs 16-byte rows");
     if (!pair) {
         const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_1cta, sms));
-        if (kgroup) {
-            if (f32) return launch_one<true, false, false, true>(ma, mb, mc, p, grid, smem, stream);
-            return launch_one<false, true, false, true>(ma, mb, mc, p, grid, smem, stream);
-        }
-        if (f32) return launch_one<true, false, false>(ma, mb, mc, p, grid, smem, stream);
-        if (tma_store) return launch_one<false, true, false>(ma, mb, mc, p, grid, smem, stream);
-        return launch_one<false, false, false>(ma, mb, mc, p, grid, smem, stream);
+        if (sched == G_KGROUP) return launch_mode<false, G_KGROUP>(f32, tma_store, ma, mb, mc, p, grid, smem, stream);
+        if (sched == G_MGROUP) return launch_mode<false, G_MGROUP>(f32, tma_store, ma, mb, mc, p, grid, smem, stream);
+        return launch_mode<false, G_DENSE>(f32, tma_store, ma, mb, mc, p, grid, smem, stream);
     }
     if (clusters < 1) return fail(NVFP4_ERR_CUDA, "the CTA-pair GEMM cannot be resident");
     const int grid = 2 * (int)std::max<int64_t>(1, std::min<int64_t>(pair_tiles, clusters));
-    if (kgroup) {
-        if (f32) return launch_one<true, false, true, true>(ma, mb, mc, p, grid, smem, stream);
-        return launch_one<false, true, true, true>(ma, mb, mc, p, grid, smem, stream);
-    }
-    if (f32) return launch_one<true, false, true>(ma, mb, mc, p, grid, smem, stream);
-    if (tma_store) return launch_one<false, true, true>(ma, mb, mc, p, grid, smem, stream);
-    return launch_one<false, false, true>(ma, mb, mc, p, grid, smem, stream);
+    if (sched == G_KGROUP) return launch_mode<true, G_KGROUP>(f32, tma_store, ma, mb, mc, p, grid, smem, stream);
+    if (sched == G_MGROUP) return launch_mode<true, G_MGROUP>(f32, tma_store, ma, mb, mc, p, grid, smem, stream);
+    return launch_mode<true, G_DENSE>(f32, tma_store, ma, mb, mc, p, grid, smem, stream);
 }
 
 extern "C" {
 
-// Store tensor map of a bf16 output [rows, n] with row stride ldc: boxes of
-// 32 x 32 elements (64-byte rows) with 64-byte swizzle.  Only built when C
-// rows are 16-byte aligned; otherwise the kernel stores directly.
-static nvfp4_status make_store_map(CUtensorMap* map, void* c, int64_t rows, int64_t n, int64_t ldc, bool* enabled) {
+// Store tensor map of a bf16 or FP32 output [rows, n] with row stride ldc:
+// boxes of 32 rows x 64 bytes (32 bf16 or 16 FP32 columns) with 64-byte
+// swizzle.  Only built when C's rows are 16-byte aligned; otherwise the
+// kernel stores directly.
+static nvfp4_status make_store_map(CUtensorMap* map, void* c, int64_t rows, int64_t n, int64_t ldc, bool f32,
+                                   bool* enabled) {
     std::memset(map, 0, sizeof(*map));
     *enabled = false;
-    if (!aligned16(c) || (ldc * 2) % 16 != 0) return NVFP4_OK;
+    const int esz = f32 ? 4 : 2;
+    if (!aligned16(c) || (ldc * esz) % 16 != 0) return NVFP4_OK;
     auto fn = encode_fn();
     if (fn == nullptr) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)(ldc * 2)};
-    cuuint32_t box[2] = {32u, 32u};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldc * esz)};
+    cuuint32_t box[2] = {f32 ? 16u : 32u, 32u};
     cuuint32_t estr[2] = {1u, 1u};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled (store) failed (%d)", (int)r);
     *enabled = true;
     return NVFP4_OK;
@@ -811,10 +821,10 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* c, i
     CUtensorMap mc;
     bool tma_store = false;
     std::memset(&mc, 0, sizeof(mc));
-    if (c_dtype == NVFP4_OUT_BF16 && K < G_TMA_STORE_MAX_K) NVFP4_TRY(make_store_map(&mc, c, M, N, ldc, &tma_store));
+    NVFP4_TRY(make_store_map(&mc, c, M, N, ldc, c_dtype == NVFP4_OUT_FP32, &tma_store));
     const int64_t tiles = cdiv(M, G_BM) * cdiv(N, G_BN);
     const int64_t pair_tiles = cdiv(M, 2 * G_BM) * cdiv(N, G_BN);
-    return launch_gemm(ma, mb, mc, p, tiles, pair_tiles, sms, c_dtype, tma_store, pair, stream, dev);
+    return launch_gemm(ma, mb, mc, p, tiles, pair_tiles, sms, c_dtype, tma_store, pair, stream, dev, G_DENSE);
 }
 
 nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, int32_t num_groups,
@@ -858,9 +868,9 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, i
     CUtensorMap mc;
     bool tma_store = false;
     std::memset(&mc, 0, sizeof(mc));
-    if (c_dtype == NVFP4_OUT_BF16 && K < G_TMA_STORE_MAX_K) NVFP4_TRY(make_store_map(&mc, c, R, n, ldc, &tma_store));
+    NVFP4_TRY(make_store_map(&mc, c, R, n, ldc, c_dtype == NVFP4_OUT_FP32, &tma_store));
     // tiles depend on the group sizes (device data): the grid is the SM count
-    return launch_gemm(ma, mb, mc, p, sms, sms / 2, sms, c_dtype, tma_store, pair, stream, dev);
+    return launch_gemm(ma, mb, mc, p, sms, sms / 2, sms, c_dtype, tma_store, pair, stream, dev, G_MGROUP);
 }
 
 nvfp4_status nvfp4_grouped_gemm_k(const nvfp4_tensor* a, const nvfp4_tensor* b, const int64_t* offsets,
@@ -904,11 +914,10 @@ nvfp4_status nvfp4_grouped_gemm_k(const nvfp4_tensor* a, const nvfp4_tensor* b, 
     CUtensorMap mc;
     bool tma_store = false;
     std::memset(&mc, 0, sizeof(mc));
-    // the tokens of one expert are few: the short-K epilogue
-    if (c_dtype == NVFP4_OUT_BF16) NVFP4_TRY(make_store_map(&mc, c, M * num_groups, N, ldc, &tma_store));
+    NVFP4_TRY(make_store_map(&mc, c, M * num_groups, N, ldc, c_dtype == NVFP4_OUT_FP32, &tma_store));
     const int64_t tiles = (int64_t)num_groups * cdiv(M, G_BM) * cdiv(N, G_BN);
     const int64_t pair_tiles = (int64_t)num_groups * cdiv(M, 2 * G_BM) * cdiv(N, G_BN);
-    return launch_gemm(ma, mb, mc, p, tiles, pair_tiles, sms, c_dtype, tma_store, pair, stream, dev, true);
+    return launch_gemm(ma, mb, mc, p, tiles, pair_tiles, sms, c_dtype, tma_store, pair, stream, dev, G_KGROUP);
 }
 
 nvfp4_status nvfp4_device_status(int32_t* flags) {
