@@ -59,9 +59,22 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t b) {
     return __uint_as_float(((e + 120u) << 23) | (m << 20));         // 2^(e-7) * (1 + m/8)
 }
 
-// Block scale byte of a block with largest magnitude bamax.
+// RN(x / 6) without a division for x >= 2^-125: q0 = RN(x * RN(1/6)),
+// r = x - 6 q0 (exact, one fused multiply-add), q = RN(q0 + r * RN(1/6)).
+// It equals the IEEE quotient for every float in [2^-125, FLT_MAX] (checked
+// exhaustively on the host against x / 6.0f); smaller x take the division.
+__device__ __forceinline__ float div6_rn(float x) {
+    if (x < 2.35098870e-38f) return __fdiv_rn(x, 6.0f);        // 2^-125
+    const float c = 0.16666667f;                              // RN(1/6)
+    const float q0 = __fmul_rn(x, c);
+    const float r = __fmaf_rn(-q0, 6.0f, x);
+    return __fmaf_rn(r, c, q0);
+}
+
+// Block scale byte of a block with largest magnitude bamax: RN(RN(bamax / 6)
+// * S_enc) converted to E4M3.
 __device__ __forceinline__ uint32_t block_scale(float bamax, float s_enc) {
-    return e4m3_from_float(__fmul_rn(__fdiv_rn(bamax, 6.0f), s_enc));
+    return e4m3_from_float(__fmul_rn(div6_rn(bamax), s_enc));
 }
 
 // Per-element multiplier S_enc / sf (only used when sf != 0).
@@ -112,6 +125,75 @@ __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u) {
     const uint32_t x = __float2uint_ru(fabsf(v) * 33554432.0f);    // ceil(|v| * 2^25)
     const uint32_t c = mb >= 0x3F000000u ? c_up : (u < (x << 8) ? 1u : 0u);
     return ((bits >> 28) & 8u) | c;
+}
+
+// Eight E2M1 codes (RNE) of the 8 bf16 values of v (element 2j in the low
+// half of word j) times ratio: per word the two values become FP32 exactly
+// (shift / mask), one packed f32x2 multiply rounds each product once (as
+// __fmul_rn would), and one hardware conversion encodes the pair.
+__device__ __forceinline__ uint32_t e2m1x8_rne_bf16(const uint4 v, float ratio) {
+    uint32_t out;
+    asm("{\n\t.reg .b64 rr, x0, x1, x2, x3;\n\t.reg .b32 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+        ".reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b64 rr, {%5, %5};\n\t"
+        "shl.b32 l0, %1, 16;\n\tand.b32 h0, %1, 0xFFFF0000;\n\tmov.b64 x0, {l0, h0};\n\t"
+        "shl.b32 l1, %2, 16;\n\tand.b32 h1, %2, 0xFFFF0000;\n\tmov.b64 x1, {l1, h1};\n\t"
+        "shl.b32 l2, %3, 16;\n\tand.b32 h2, %3, 0xFFFF0000;\n\tmov.b64 x2, {l2, h2};\n\t"
+        "shl.b32 l3, %4, 16;\n\tand.b32 h3, %4, 0xFFFF0000;\n\tmov.b64 x3, {l3, h3};\n\t"
+        "mul.rn.f32x2 x0, x0, rr;\n\tmul.rn.f32x2 x1, x1, rr;\n\t"
+        "mul.rn.f32x2 x2, x2, rr;\n\tmul.rn.f32x2 x3, x3, rr;\n\t"
+        "mov.b64 {l0, h0}, x0;\n\tmov.b64 {l1, h1}, x1;\n\tmov.b64 {l2, h2}, x2;\n\tmov.b64 {l3, h3}, x3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, h0, l0;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, h1, l1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, h2, l2;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, h3, l3;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(out)
+        : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "f"(ratio));
+    return out;
+}
+
+// The 8 products bf16(v) * ratio of a half-block, each rounded once (packed
+// f32x2 multiplies), for the stochastic encoder.
+__device__ __forceinline__ void scale8_bf16(const uint4 v, float ratio, float (&f)[8]) {
+    asm("{\n\t.reg .b64 rr, x0, x1, x2, x3;\n\t.reg .b32 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+        "mov.b64 rr, {%12, %12};\n\t"
+        "shl.b32 l0, %8, 16;\n\tand.b32 h0, %8, 0xFFFF0000;\n\tmov.b64 x0, {l0, h0};\n\t"
+        "shl.b32 l1, %9, 16;\n\tand.b32 h1, %9, 0xFFFF0000;\n\tmov.b64 x1, {l1, h1};\n\t"
+        "shl.b32 l2, %10, 16;\n\tand.b32 h2, %10, 0xFFFF0000;\n\tmov.b64 x2, {l2, h2};\n\t"
+        "shl.b32 l3, %11, 16;\n\tand.b32 h3, %11, 0xFFFF0000;\n\tmov.b64 x3, {l3, h3};\n\t"
+        "mul.rn.f32x2 x0, x0, rr;\n\tmul.rn.f32x2 x1, x1, rr;\n\t"
+        "mul.rn.f32x2 x2, x2, rr;\n\tmul.rn.f32x2 x3, x3, rr;\n\t"
+        "mov.b64 {%0, %1}, x0;\n\tmov.b64 {%2, %3}, x1;\n\tmov.b64 {%4, %5}, x2;\n\tmov.b64 {%6, %7}, x3;\n\t}"
+        : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]), "=f"(f[4]), "=f"(f[5]), "=f"(f[6]), "=f"(f[7])
+        : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "f"(ratio));
+}
+
+// Largest |x| of 16 bf16 values (two uint4 of bf16 pairs) as the 15 magnitude
+// bits: seven packed abs-max operations and one final halving.
+__device__ __forceinline__ uint32_t bf16x16_absmax(const uint4 a, const uint4 b) {
+    uint32_t m;
+    asm("{\n\t.reg .b32 t0, t1, t2, t3, u0, u1;\n\t"
+        "max.xorsign.abs.bf16x2 t0, %1, %2;\n\t"
+        "max.xorsign.abs.bf16x2 t1, %3, %4;\n\t"
+        "max.xorsign.abs.bf16x2 t2, %5, %6;\n\t"
+        "max.xorsign.abs.bf16x2 t3, %7, %8;\n\t"
+        "max.xorsign.abs.bf16x2 u0, t0, t1;\n\t"
+        "max.xorsign.abs.bf16x2 u1, t2, t3;\n\t"
+        "max.xorsign.abs.bf16x2 %0, u0, u1;\n\t}"
+        : "=r"(m)
+        : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
+    m &= 0x7FFF7FFFu;
+    return max(m & 0xFFFFu, m >> 16);
+}
+
+// 32 bytes (16 bf16) from global memory in one 256-bit load that bypasses
+// L1 (streamed data, read once): a warp's 32 lanes read 1 KB contiguous
+// with every 32-byte sector used by one instruction.  p: 32-byte aligned.
+__device__ __forceinline__ void ldg32_stream(const void* p, uint4& a, uint4& b) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(p));
 }
 
 // ------------------------------------------------------------------ Philox

@@ -166,6 +166,35 @@ int quant_blocks(int64_t rows, int sms) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(b, (int64_t)sms * 8));
 }
 
+// Scale buffers above this size are written in band order by k_quant1d
+// (the 126 MB L2 keeps smaller ones until their sectors are complete).
+constexpr int64_t G_QUANT_SF_L2_BYTES = 48ll << 20;
+
+// Blocks of 8 warps for k_quant1d: one warp per 512-element segment at most,
+// and no more blocks than can be resident at once (the kernel splits its
+// segments statically over the warps of the grid, so a second wave would be
+// a tail).
+template <bool SR, bool GROUPED, bool BAND>
+int quant1d_blocks(int64_t rows, int64_t cols, int sms, size_t smem) {
+    static int per_sm[64][2] = {};      // per device; [0]: computed, [1]: blocks per SM
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (!per_sm[dev][0]) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_quant1d<SR, GROUPED, BAND>, 256, smem) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = 1;
+        }
+        per_sm[dev][1] = n;
+        per_sm[dev][0] = 1;
+    }
+    // segments: 128 scale rows per band, 32 blocks per segment (grouped: one
+    // partial band per expert at most)
+    const int64_t segs = (cdiv(rows, 128) + (GROUPED ? NVFP4_MAX_GROUPS : 0)) * 128 * cdiv(cols / 16, 32);
+    return (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(segs, 8), (int64_t)sms * per_sm[dev][1]));
+}
+
 int amax_blocks(int64_t units) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(units, 256 * 8), 4096));
 }
@@ -246,20 +275,17 @@ nvfp4_status nvfp4_quantize_1d(const void* x, int64_t rows, int64_t cols, int64_
         if (copy) NVFP4_TRY(cuda_call(cudaMemcpyAsync(copy, amax_in, 4, cudaMemcpyDeviceToDevice, stream), "amax copy"));
         return NVFP4_OK;
     }
-    const int nb = quant_blocks(rows, sms);
+    const bool band = (int64_t)sf_bytes(rows, cols) > G_QUANT_SF_L2_BYTES;
+    const bool sr = mode == NVFP4_ROUND_SR;
     uint8_t* codes = (uint8_t*)out->codes;
-    if (mode == NVFP4_ROUND_SR)
-        k_quant1d<true, false><<<nb, 256, 0, stream>>>((const uint16_t*)x, rows, cols, ld, am, seed, codes, out->sf,
-                                                       nullptr, 0, copy);
-    else
-        k_quant1d<false, false><<<nb, 256, 0, stream>>>((const uint16_t*)x, rows, cols, ld, am, seed, codes, out->sf,
-                                                        nullptr, 0, copy);
-    NVFP4_TRY(launched("k_quant1d"));
-    if (rows % 128 != 0) {
-        k_zero_pad_rows<<<64, 256, 0, stream>>>(out->sf, rows, cols, nullptr, 0);
-        NVFP4_TRY(launched("k_zero_pad_rows"));
-    }
-    return NVFP4_OK;
+    const uint16_t* xp = (const uint16_t*)x;
+#define NVFP4_Q1D(SR_, BAND_)                                                                              \
+    k_quant1d<SR_, false, BAND_><<<quant1d_blocks<SR_, false, BAND_>(rows, cols, sms, 0), 256, 0, stream>>>( \
+        xp, rows, cols, ld, am, seed, codes, out->sf, nullptr, 0, copy)
+    if (sr) { if (band) NVFP4_Q1D(true, true); else NVFP4_Q1D(true, false); }
+    else { if (band) NVFP4_Q1D(false, true); else NVFP4_Q1D(false, false); }
+#undef NVFP4_Q1D
+    return launched("k_quant1d");       // it also writes the zero scales of the padding rows
 }
 
 nvfp4_status nvfp4_quantize_1d_grouped(const void* x, int64_t rows, int64_t cols, int64_t ld, const int64_t* offsets,
@@ -293,17 +319,19 @@ nvfp4_status nvfp4_quantize_1d_grouped(const void* x, int64_t rows, int64_t cols
             NVFP4_TRY(cuda_call(cudaMemcpyAsync(copy, amax_in, 4 * num_groups, cudaMemcpyDeviceToDevice, stream), "amax copy"));
         return NVFP4_OK;
     }
-    const int nb = quant_blocks(rows, sms);
+    // the group tables are sized for NVFP4_MAX_GROUPS in the occupancy query
+    const size_t tab_max = sizeof(int32_t) * 2 * (NVFP4_MAX_GROUPS + 1);
+    const bool band = (int64_t)sf_bytes(rows + 127 * (int64_t)num_groups, cols) > G_QUANT_SF_L2_BYTES;
+    const bool sr = mode == NVFP4_ROUND_SR;
     uint8_t* codes = (uint8_t*)out->codes;
-    if (mode == NVFP4_ROUND_SR)
-        k_quant1d<true, true><<<nb, 256, tab, stream>>>((const uint16_t*)x, rows, cols, ld, am, seed, codes, out->sf,
-                                                        offsets, num_groups, copy);
-    else
-        k_quant1d<false, true><<<nb, 256, tab, stream>>>((const uint16_t*)x, rows, cols, ld, am, seed, codes, out->sf,
-                                                         offsets, num_groups, copy);
-    NVFP4_TRY(launched("k_quant1d grouped"));
-    k_zero_pad_rows<<<std::min(num_groups, 256), 256, tab, stream>>>(out->sf, rows, cols, offsets, num_groups);
-    return launched("k_zero_pad_rows grouped");
+    const uint16_t* xp = (const uint16_t*)x;
+#define NVFP4_Q1G(SR_, BAND_)                                                                                   \
+    k_quant1d<SR_, true, BAND_><<<quant1d_blocks<SR_, true, BAND_>(rows, cols, sms, tab_max), 256, tab, stream>>>( \
+        xp, rows, cols, ld, am, seed, codes, out->sf, offsets, num_groups, copy)
+    if (sr) { if (band) NVFP4_Q1G(true, true); else NVFP4_Q1G(true, false); }
+    else { if (band) NVFP4_Q1G(false, true); else NVFP4_Q1G(false, false); }
+#undef NVFP4_Q1G
+    return launched("k_quant1d grouped");   // it also writes the zero scales of each expert's padding rows
 }
 
 nvfp4_status nvfp4_quantize_2d(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ld,

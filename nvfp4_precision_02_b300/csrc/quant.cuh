@@ -237,11 +237,9 @@ template <bool SR>
 __device__ __forceinline__ uint32_t encode8(const uint4 v, float ratio, bool zero, const PhiloxKeys& key,
                                             uint64_t e0) {
     if (zero) return 0u;
-    const float f[8] = {__fmul_rn(bf16_lo(v.x), ratio), __fmul_rn(bf16_hi(v.x), ratio),
-                        __fmul_rn(bf16_lo(v.y), ratio), __fmul_rn(bf16_hi(v.y), ratio),
-                        __fmul_rn(bf16_lo(v.z), ratio), __fmul_rn(bf16_hi(v.z), ratio),
-                        __fmul_rn(bf16_lo(v.w), ratio), __fmul_rn(bf16_hi(v.w), ratio)};
-    if (!SR) return e2m1x8_rne(f);
+    if (!SR) return e2m1x8_rne_bf16(v, ratio);
+    float f[8];
+    scale8_bf16(v, ratio, f);
     const uint4 w0 = sr_words(key, e0 >> 2);
     const uint4 w1 = sr_words(key, (e0 >> 2) + 1);
     const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -251,12 +249,46 @@ __device__ __forceinline__ uint32_t encode8(const uint4 v, float ratio, bool zer
     return out;
 }
 
-// One warp walks a contiguous range of rows; in each row lane pairs own
-// 16-element blocks (lane 2j: first 8 elements, lane 2j+1: last 8), four
-// 16-byte loads per lane in flight.
+// Element multipliers S_enc / e4m3(c) of every scale code c (entry 0 unused)
+// in a warp's 128-float slice of shared memory: lane l computes codes l,
+// l + 32, l + 64, l + 96 with the same correctly rounded division as
+// element_ratio, so a lookup gives the same bits.
+__device__ __forceinline__ void fill_ratio_table(float* tab, float s_enc) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t c = (uint32_t)(lane + 32 * i);
+        tab[c] = (c >= 1 && c <= 126) ? element_ratio(s_enc, c) : 0.0f;
+    }
+    __syncwarp();
+}
+
+// Work is cut into segments of 32 blocks (512 elements) of one row.  The
+// segments are ordered by 128-row band of the scale layout (groups start on
+// a band), and inside a band either row by row (row order: each warp then
+// streams contiguous memory) or, when the scale buffer is larger than L2
+// can keep half-written (BAND), by 32-block column and then by rows
+// i, i+32, i+64, i+96 in turn: those four rows share each 16-byte slot of
+// the scale atoms, so every 32-byte scale sector is complete within eight
+// segments instead of being written back half-filled.  Band rows past the
+// tensor's or the group's end are the padding rows of the scale layout:
+// their scale words are written as zeros.
+// Warp w of W takes the contiguous range [S*w/W, S*(w+1)/W) of the S
+// segments, walks it with a (band, column, row-in-band) counter, and keeps
+// the next two segments' loads in flight while it encodes one.  Lane l owns block l
+// of a segment: its 16 elements (one 256-bit load), the block amax in
+// registers, 8 code bytes; every fourth lane stores the 4 scale bytes of its
+// block and the next three as one word (zeros past the row's last block
+// fill the scale padding of the last atom column).  The element multiplier
+// of a block is looked up in the warp's table of the 127 scale codes,
+// refilled when the tensor scale changes (a new expert).
 // x: bf16 [rows, cols] (row stride ld); codes [rows, cols/2]; sf swizzled.
 // amax: 1 value (or one per group when GROUPED).  SR index e = r*cols + c.
-template <bool SR, bool GROUPED>
+struct Seg16 {
+    uint4 a, b;
+};
+
+template <bool SR, bool GROUPED, bool BAND>
 __global__ void __launch_bounds__(256) k_quant1d(const uint16_t* __restrict__ x, int64_t rows,
                                                  int64_t cols, int64_t ld,
                                                  const float* __restrict__ amax, uint64_t seed,
@@ -264,67 +296,142 @@ __global__ void __launch_bounds__(256) k_quant1d(const uint16_t* __restrict__ x,
                                                  const int64_t* __restrict__ offsets, int32_t groups,
                                                  float* __restrict__ amax_copy) {
     extern __shared__ int32_t s_tab[];
+    __shared__ float s_ratio[8][128];
     GroupTables t{s_tab, s_tab + (GROUPED ? groups + 1 : 0)};
     if (GROUPED) build_group_tables(offsets, groups, rows, t);
     if (amax_copy != nullptr && blockIdx.x == 0) {
         const int n = GROUPED ? groups : 1;
         for (int i = threadIdx.x; i < n; i += blockDim.x) amax_copy[i] = amax[i];
     }
-    constexpr int U = 4;                               // 16-byte units per lane per step
     const int lane = threadIdx.x & 31;
-    const int upr = (int)(cols >> 3);
-    const int64_t nc = cols >> 4, pc = ((nc + 3) >> 2) << 2;
-    int64_t r0, r1;
-    warp_rows(rows, r0, r1);
-    int g = 0;
-    int32_t g_begin = 0, g_end = (int32_t)rows, sf_row0 = 0;
-    float s_enc = GROUPED ? 1.0f : tensor_encode_scale(amax[0]);
+    float* ratio_tab = s_ratio[threadIdx.x >> 5];
+    const int64_t nb = cols >> 4;                       // blocks of a row
+    const int64_t nseg = (nb + 31) >> 5;                // 32-block columns
+    const int64_t bands = GROUPED ? (int64_t)(t.pad[groups] >> 7) : (rows + 127) >> 7;
+    const int64_t S = bands * nseg * 128;
+    const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t s0 = S * w / nw, s1 = S * (w + 1) / nw;
+    if (s0 >= s1) return;
     const PhiloxKeys key = philox_keys(seed);
-    bool have_g = false;
-    for (int64_t r = r0; r < r1; ++r) {
-        if (GROUPED) {
-            if (r < t.off[0] || r >= t.off[groups]) continue;
-            if (!have_g || r >= g_end || r < g_begin) {
-                g = find_group(t.off, groups, (int32_t)r);
-                g_begin = t.off[g];
-                g_end = t.off[g + 1];
-                sf_row0 = t.pad[g];
-                s_enc = tensor_encode_scale(amax[g]);
-                have_g = true;
+    // one 256-bit load per lane when every block starts 32-byte aligned
+    const bool vec32 = ((reinterpret_cast<uintptr_t>(x) & 31) == 0) && ((ld & 15) == 0);
+    float s_enc = 1.0f;
+    if (!GROUPED) {
+        s_enc = tensor_encode_scale(amax[0]);
+        fill_ratio_table(ratio_tab, s_enc);
+    }
+    // The walk: band k, 32-block column j, row rib of the band.
+    int64_t k, j;
+    int rib;
+    if (BAND) {
+        rib = 32 * (int)(s0 & 3) + (int)((s0 >> 2) & 31);
+        const int64_t kj = s0 >> 7;
+        k = kj / nseg;
+        j = kj - k * nseg;
+    } else {
+        k = s0 / (nseg * 128);
+        const int64_t rem = s0 - k * nseg * 128;
+        rib = (int)(rem / nseg);
+        j = rem - (int64_t)rib * nseg;
+    }
+    // the expert whose scale rows hold band k (grouped): pad[g] <= 128 k < pad[g+1]
+    int gk = -1, g = 0;
+    int32_t g_lo = 0, g_hi = 0, g_pad = 0;
+    auto band_group = [&]() {
+        if (GROUPED && k != gk) {
+            int lo = 0, hi = groups;
+            const int32_t key_row = (int32_t)(k * 128);
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (t.pad[mid] <= key_row) lo = mid; else hi = mid;
+            }
+            g = lo;
+            g_lo = t.off[g];
+            g_hi = t.off[g + 1];
+            g_pad = t.pad[g];
+            gk = (int)k;
+        }
+    };
+    // A segment in flight: its data, data row (-1: a padding row of the scale
+    // layout), scale row, 32-block column and expert (rows and scale rows are
+    // below 2^31: host checks).
+    struct InFlight {
+        Seg16 v;
+        int32_t r, srow, j, g;
+    };
+    auto fetch = [&]() {
+        InFlight f;
+        band_group();
+        f.srow = (int32_t)(k * 128 + rib);
+        f.r = GROUPED ? ((g_lo + (f.srow - g_pad)) < g_hi ? g_lo + (f.srow - g_pad) : -1)
+                      : (f.srow < rows ? f.srow : -1);
+        f.j = (int32_t)j;
+        f.g = g;
+        const int64_t fb = j * 32 + lane;
+        f.v = Seg16{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (f.r >= 0 && fb < nb) {
+            const uint16_t* src = x + (int64_t)f.r * ld + 16 * fb;
+            if (vec32) {
+                ldg32_stream(src, f.v.a, f.v.b);
+            } else {
+                f.v.a = __ldg(reinterpret_cast<const uint4*>(src));
+                f.v.b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
             }
         }
-        const int64_t sr = GROUPED ? sf_row0 + (r - g_begin) : r;
-        const uint16_t* row = x + r * ld;
-        uint8_t* crow = codes + r * (cols >> 1);
-        for (int base = 0; base < upr; base += 32 * U) {
-            uint4 v[U];
-#pragma unroll
-            for (int i = 0; i < U; ++i) {
-                const int u = base + i * 32 + lane;
-                v[i] = u < upr ? __ldg(reinterpret_cast<const uint4*>(row + u * 8)) : make_uint4(0, 0, 0, 0);
+        if (BAND) {
+            // rib: 0, 32, 64, 96, 1, 33, 65, 97, ..., 31, 63, 95, 127, then the next column
+            if (rib < 96) rib += 32;
+            else if (rib < 127) rib -= 95;
+            else { rib = 0; if (++j == nseg) { j = 0; ++k; } }
+        } else if (++j == nseg) {
+            j = 0;
+            if (++rib == 128) { rib = 0; ++k; }
+        }
+        return f;
+    };
+    // two segments in flight ahead of the one being encoded
+    InFlight cur = fetch(), nxt;
+    nxt.r = -1;
+    if (s0 + 1 < s1) nxt = fetch();
+    int cur_g = -1;
+    for (int64_t sg = s0; sg < s1; ++sg) {
+        InFlight nxt2;
+        nxt2.r = -1;
+        if (sg + 2 < s1) nxt2 = fetch();
+        const int64_t b = (int64_t)cur.j * 32 + lane;
+        uint32_t sc = 0;
+        if (cur.r >= 0) {
+            if (GROUPED && cur.g != cur_g) {
+                cur_g = cur.g;
+                s_enc = tensor_encode_scale(amax[cur_g]);
+                fill_ratio_table(ratio_tab, s_enc);
             }
-#pragma unroll
-            for (int i = 0; i < U; ++i) {
-                const int u = base + i * 32 + lane;
-                uint32_t m = absmax_bits(v[i], 0u);
-                m = max(m & 0xFFFFu, m >> 16);
-                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-                const float bamax = __uint_as_float(m << 16);
-                const uint32_t sc = block_scale(bamax, s_enc);
-                const float ratio = sc ? element_ratio(s_enc, sc) : 0.0f;
-                if (u < upr) {
-                    const uint32_t packed = encode8<SR>(v[i], ratio, sc == 0, key,
-                                                        (uint64_t)r * (uint64_t)cols + (uint64_t)u * 8);
-                    *reinterpret_cast<uint32_t*>(crow + u * 4) = packed;
-                    if ((lane & 1) == 0) {
-                        const int64_t c = u >> 1;
-                        sf[sf_offset(sr, c, cols)] = (uint8_t)sc;
-                        if (c == nc - 1)
-                            for (int64_t cc = nc; cc < pc; ++cc) sf[sf_offset(sr, cc, cols)] = 0;
-                    }
+            const uint32_t m = bf16x16_absmax(cur.v.a, cur.v.b);
+            sc = block_scale(__uint_as_float(m << 16), s_enc);
+            const float ratio = ratio_tab[sc];
+            uint32_t lo = 0, hi = 0;
+            if (sc != 0) {
+                if (SR) {
+                    const uint64_t e0 = (uint64_t)(uint32_t)cur.r * (uint64_t)cols + (uint64_t)b * 16;
+                    lo = encode8<true>(cur.v.a, ratio, false, key, e0);
+                    hi = encode8<true>(cur.v.b, ratio, false, key, e0 + 8);
+                } else {
+                    lo = e2m1x8_rne_bf16(cur.v.a, ratio);
+                    hi = e2m1x8_rne_bf16(cur.v.b, ratio);
                 }
             }
+            if (b < nb) *reinterpret_cast<uint2*>(codes + (int64_t)cur.r * (cols >> 1) + 8 * b) = make_uint2(lo, hi);
         }
+        // four consecutive blocks' scales in one word (lanes past the row's end,
+        // and every lane of a padding row, hold 0)
+        const uint32_t scv = b < nb ? sc : 0u;
+        const uint32_t word = scv | (__shfl_down_sync(0xFFFFFFFFu, scv, 1) << 8) |
+                              (__shfl_down_sync(0xFFFFFFFFu, scv, 2) << 16) |
+                              (__shfl_down_sync(0xFFFFFFFFu, scv, 3) << 24);
+        if (b < nb && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(cur.srow, b, cols)) = word;
+        cur = nxt;
+        nxt = nxt2;
     }
 }
 
