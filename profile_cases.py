@@ -18,6 +18,7 @@ the input):
   quant1d_sr        k_quant1d<SR>: dY [T, N]
   quant2d           k_quant2d: W with W^T
   quant2d_moe       k_quant2d: the batched expert up-projection weights
+  quant2d_moe_fused k_quant2d_fused: the same weights with their per-expert amax in one launch
   dual_amax         k_rht<3>: max |dY| and max |RHT(dY)| in one read
   rht_sr            k_rht<2>: RHT(dY)^T with SR
   rht_rne           k_rht<1>: RHT(X)^T with RNE
@@ -47,7 +48,7 @@ if ROOT not in sys.path:
 from nvfp4_precision_02_b300 import binding as B  # noqa: E402
 from nvfp4_precision_02_b300 import workloads as wl  # noqa: E402
 
-OPS = ["amax", "quant1d_rne", "quant1d_sr", "quant2d", "quant2d_moe", "dual_amax", "rht_sr", "rht_rne",
+OPS = ["amax", "quant1d_rne", "quant1d_sr", "quant2d", "quant2d_moe", "quant2d_moe_fused", "dual_amax", "rht_sr", "rht_rne",
        "amax_grouped", "quant1d_grouped_a", "quant1d_grouped_h", "rht_grouped_sr", "quant1d_mse", "sr_fp16",
        "count_zero", "gemm_fprop", "gemm_dgrad", "gemm_wgrad", "grouped_up", "grouped_down", "grouped_dgrad",
        "grouped_wgrad"]
@@ -93,9 +94,12 @@ def prepare(op: str, which: str, dev):
             q = B.empty_qtensor(N, K, dev)
             return lambda: B.quantize_1d_mse(w, amax_in=qw.amax, out=q)
         return lambda: B.quantize_2d(w, want_t=True, amax_in=qw.amax, out=qw, out_t=qwt)
-    if op == "quant2d_moe":
+    if op in ("quant2d_moe", "quant2d_moe_fused"):
         w = wl.batched_normal_bf16(m.experts, m.expert_hidden, m.latent, 0.02, wl.SEEDS[which + "_moe_w"], dev)
         qw = B.empty_qtensor(m.expert_hidden, m.latent, dev, batch=m.experts, n_amax=m.experts)
+        if op == "quant2d_moe_fused":
+            ws = torch.empty(B.quantize_2d_fused_workspace(m.experts), dtype=torch.uint8, device=dev)
+            return lambda: B.quantize_2d_fused(w, workspace=ws, out=qw)
         B.quantize_2d(w, want_t=False, out=qw)
         return lambda: B.quantize_2d(w, want_t=False, amax_in=qw.amax, out=qw)
     if op == "sr_fp16":
