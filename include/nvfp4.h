@@ -314,8 +314,11 @@ nvfp4_status nvfp4_rht_quantize_grouped(const void *x, int64_t rows, int64_t col
 /* C[m, n] = alpha * sum_k a_k * sa * b_k * sb with FP32 accumulation, where
  * alpha = dec(a->amax) * dec(b->amax) in FP32 -- the fprop / dgrad / wgrad
  * NVFP4 GEMMs (Super summary "Infra design"; Ultra report 2.2).
- * a: [M, K], b: [N, K] (both K-major, a->cols == b->cols == K, K % 32 == 0
- * so that code rows are 16-byte multiples).  c: device [M, N], row stride
+ * a: [M, K], b: [N, K] (both K-major, a->cols == b->cols == K, K % 16 == 0,
+ * the 16-element micro-block of the recipe; K % 16 != 0 returns
+ * NVFP4_ERR_SHAPE).  When K % 32 == 16 the K/2-byte code rows are not the
+ * 16-byte multiple a TMA tensor map needs: the kernel then copies the code
+ * rows into shared memory itself, on single CTAs.  c: device [M, N], row stride
  * ldc elements, bf16 (one RNE rounding of the FP32 result) or FP32.
  * M, N >= 1 arbitrary.  c_amax (device, 1 float, nullable): receives
  * max |c| over the written outputs (of the stored bf16 values for a bf16 c),
@@ -332,7 +335,7 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor *a, const nvfp4_tensor *b, void *c, i
 /* Grouped GEMM of the LatentMoE routed experts: for every group g,
  * C[offsets[g] .. offsets[g+1]-1, :] = alpha_g * A_g * W_g^T with
  * alpha_g = dec(a->amax[g]) * dec(b->amax[g]).  a: grouped operand from
- * nvfp4_quantize_1d_grouped ([R, K], K % 32 == 0).  b: batched operand from
+ * nvfp4_quantize_1d_grouped ([R, K], K % 16 == 0, as for nvfp4_gemm).  b: batched operand from
  * nvfp4_quantize_2d with batch == num_groups, b->rows == n per expert,
  * b->cols == K.  offsets: device int64 [num_groups+1] as for the grouped
  * quantiser.  Rows of C outside [offsets[0], offsets[num_groups]) are not

@@ -136,7 +136,31 @@ struct GemmParams {
     int64_t ldc;
     float* c_amax;              // nullable: max |C| over the written outputs, per group (zeroed by the host)
     bool vec_store;             // rows of C start 16-byte aligned: vector stores
+    // K % 32 == 16: code rows of K/2 bytes are not a 16-byte multiple, which
+    // a tensor map's row stride must be; the producer warp then copies the
+    // stage's rows itself (single-CTA kernel only)
+    bool copy_ab;
+    const uint8_t* a_codes;     // copy_ab: A codes [a_rows, K/2]
+    const uint8_t* b_codes;     // copy_ab: B codes [b_rows, K/2]
+    int64_t a_rows, b_rows;
 };
+
+// A stage's 128-byte K window of `nrows` operand rows from row0, copied by
+// the 32 lanes of a warp into the layout a 128B-swizzled TMA box gives
+// (16-byte chunk c of row r at chunk c ^ (r & 7) of the row's 128 bytes),
+// 8 bytes at a time (rows are 8-byte aligned when K % 16 == 0); bytes past
+// the row's end or rows past `rows` are zero, as a TMA load fills them.
+__device__ __forceinline__ void copy_stage_rows(uint8_t* dst, const uint8_t* __restrict__ src, int64_t rows,
+                                                int64_t row_bytes, int64_t row0, int nrows, int64_t kx) {
+    const int lane = threadIdx.x & 31;
+    for (int it = lane; it < nrows * 16; it += 32) {
+        const int r = it >> 4, h = it & 15;
+        const int64_t gr = row0 + r, gb = kx + 8 * h;
+        uint2 v = make_uint2(0u, 0u);
+        if (gr < rows && gb + 8 <= row_bytes) v = __ldg(reinterpret_cast<const uint2*>(src + gr * row_bytes + gb));
+        *reinterpret_cast<uint2*>(dst + r * 128 + (((h >> 1) ^ (r & 7)) << 4) + 8 * (h & 1)) = v;
+    }
+}
 
 // ------------------------------------------------------------------ PTX
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -655,7 +679,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == G_W_TMA && lane == 0) {
+    if (warp == G_W_TMA && lane == 0 && !p.copy_ab) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_a)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b)) : "memory");
         if (TMA_STORE) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_c)) : "memory");
@@ -711,7 +735,31 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int nrb = (int)((p.N + 127) / 128);            // 128-row scale blocks of one B operand
     const int64_t b_rows_per_group = (p.offsets != nullptr && !KGROUP) ? p.N : 0;
 
-    if (warp == G_W_TMA) {
+    if (warp == G_W_TMA && !PAIR && p.copy_ab) {
+        // ------------------------------------------------ copy producer (A, B; K % 32 == 16)
+        int s = 0;
+        uint32_t ph = 0;
+        for (int64_t t = t_first; t < total; t += t_step) {
+            const TileCoord tc = tile_at(t);
+            const int64_t brow0 = tc.g * b_rows_per_group + (int64_t)tc.nt * G_BN;
+            const int ka = tile_atoms(tc), kst = (ka + 3) / 4;
+            bool ok = true;
+            for (int ks = 0; ks < kst; ++ks) {
+                bool free_ = true;
+                if (lane == 0) free_ = mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag);
+                if (!__shfl_sync(0xFFFFFFFFu, free_, 0)) { ok = false; break; }
+                uint8_t* st = stages + s * STAGE_BYTES;
+                const int64_t kx = tc.k0 / 2 + ks * 128;
+                copy_stage_rows(st, p.a_codes, p.a_rows, p.K / 2, tc.row0, G_BM, kx);
+                copy_stage_rows(st + G_A_BYTES, p.b_codes, p.b_rows, p.K / 2, brow0, G_BN, kx);
+                fence_proxy_async_smem();         // generic writes, read by the tensor cores
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full0 + 8 * s);
+                if (++s == G_STAGES) { s = 0; ph ^= 1u; }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == G_W_TMA) {
         // ------------------------------------------------ TMA producer (A, B)
         if (lane == 0) {
             int s = 0;

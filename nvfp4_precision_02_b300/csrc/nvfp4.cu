@@ -820,7 +820,7 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* c, i
     NVFP4_TRY(check_operand(b, "b"));
     const int64_t M = a->rows, N = b->rows, K = a->cols;
     if (b->cols != K) return fail(NVFP4_ERR_SHAPE, "a->cols=%lld != b->cols=%lld", (long long)K, (long long)b->cols);
-    if (K % 32 != 0 || K == 0) return fail(NVFP4_ERR_SHAPE, "K=%lld must be a positive multiple of 32", (long long)K);
+    if (K % 16 != 0 || K == 0) return fail(NVFP4_ERR_SHAPE, "K=%lld must be a positive multiple of 16", (long long)K);
     if (c_dtype != NVFP4_OUT_BF16 && c_dtype != NVFP4_OUT_FP32) return fail(NVFP4_ERR_SHAPE, "bad output dtype");
     if (ldc < N) return fail(NVFP4_ERR_SHAPE, "ldc < N");
     if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) return fail(NVFP4_ERR_LIMIT, "M or N >= 2^31");
@@ -830,11 +830,21 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, void* c, i
     if (((uintptr_t)c % esz) != 0) return fail(NVFP4_ERR_ALIGN, "c is not aligned to its element size");
     int sms = 0, dev = 0;
     NVFP4_TRY(check_device(&sms, &dev));
-    const bool pair = use_pair();
+    // K % 32 == 16: code rows are not a 16-byte multiple (no tensor map); the
+    // single-CTA kernel copies them
+    const bool copy_ab = K % 32 != 0;
+    const bool pair = use_pair() && !copy_ab;
     CUtensorMap ma, mb;
-    NVFP4_TRY(make_code_map(&ma, a->codes, M, K / 2, G_BM));
-    NVFP4_TRY(make_code_map(&mb, b->codes, N, K / 2, pair ? G_BN / 2 : G_BN));
+    std::memset(&ma, 0, sizeof(ma));
+    std::memset(&mb, 0, sizeof(mb));
+    if (!copy_ab) {
+        NVFP4_TRY(make_code_map(&ma, a->codes, M, K / 2, G_BM));
+        NVFP4_TRY(make_code_map(&mb, b->codes, N, K / 2, pair ? G_BN / 2 : G_BN));
+    }
     GemmParams p{};
+    p.copy_ab = copy_ab;
+    p.a_codes = (const uint8_t*)a->codes; p.b_codes = (const uint8_t*)b->codes;
+    p.a_rows = M; p.b_rows = N;
     p.M = M; p.N = N; p.K = K;
     p.offsets = nullptr; p.groups = 1;
     p.sfa = a->sf; p.sfb = b->sf; p.sfb_group_stride = 0;
@@ -865,7 +875,7 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, i
     if (num_groups < 1 || num_groups > NVFP4_MAX_GROUPS) return fail(NVFP4_ERR_LIMIT, "num_groups must be in [1, %d]", NVFP4_MAX_GROUPS);
     const int64_t R = a->rows, K = a->cols;
     if (b->rows != n || b->cols != K) return fail(NVFP4_ERR_SHAPE, "b must be [n, K] per expert");
-    if (K % 32 != 0 || K == 0) return fail(NVFP4_ERR_SHAPE, "K=%lld must be a positive multiple of 32", (long long)K);
+    if (K % 16 != 0 || K == 0) return fail(NVFP4_ERR_SHAPE, "K=%lld must be a positive multiple of 16", (long long)K);
     if (n < 1) return fail(NVFP4_ERR_SHAPE, "n must be >= 1");
     if (c_dtype != NVFP4_OUT_BF16 && c_dtype != NVFP4_OUT_FP32) return fail(NVFP4_ERR_SHAPE, "bad output dtype");
     if (ldc < n) return fail(NVFP4_ERR_SHAPE, "ldc < n");
@@ -877,11 +887,19 @@ nvfp4_status nvfp4_grouped_gemm(const nvfp4_tensor* a, const int64_t* offsets, i
     if (((uintptr_t)c % esz) != 0) return fail(NVFP4_ERR_ALIGN, "c is not aligned to its element size");
     int sms = 0, dev = 0;
     NVFP4_TRY(check_device(&sms, &dev));
-    const bool pair = use_pair();
+    const bool copy_ab = K % 32 != 0;     // as for nvfp4_gemm
+    const bool pair = use_pair() && !copy_ab;
     CUtensorMap ma, mb;
-    NVFP4_TRY(make_code_map(&ma, a->codes, R, K / 2, G_BM));
-    NVFP4_TRY(make_code_map(&mb, b->codes, n * num_groups, K / 2, pair ? G_BN / 2 : G_BN));
+    std::memset(&ma, 0, sizeof(ma));
+    std::memset(&mb, 0, sizeof(mb));
+    if (!copy_ab) {
+        NVFP4_TRY(make_code_map(&ma, a->codes, R, K / 2, G_BM));
+        NVFP4_TRY(make_code_map(&mb, b->codes, n * num_groups, K / 2, pair ? G_BN / 2 : G_BN));
+    }
     GemmParams p{};
+    p.copy_ab = copy_ab;
+    p.a_codes = (const uint8_t*)a->codes; p.b_codes = (const uint8_t*)b->codes;
+    p.a_rows = R; p.b_rows = n * num_groups;
     p.M = R; p.N = n; p.K = K;
     p.offsets = offsets; p.groups = num_groups;
     p.sfa = a->sf; p.sfb = b->sf; p.sfb_group_stride = sf_bytes(n, K);

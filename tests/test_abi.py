@@ -78,7 +78,9 @@ def test_other_entry_points_validation(L):
     assert L.nvfp4_rht_amax(FAKE, 32, 8, 8, 1, None, None) == 1
     a, b = _t(64, 64), _t(48, 64)
     assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(_t(48, 80)), FAKE, 48, 0, None, None) == 2      # K mismatch
-    assert L.nvfp4_gemm(ctypes.byref(_t(64, 48)), ctypes.byref(_t(48, 48)), FAKE, 48, 0, None, None) == 2  # K % 32
+    assert L.nvfp4_gemm(ctypes.byref(_t(64, 40)), ctypes.byref(_t(48, 40)), FAKE, 48, 0, None, None) == 2  # K % 16
+    # K % 16 == 0 passes the shape checks (then no sm_103 device here: NVFP4_ERR_DEVICE)
+    assert L.nvfp4_gemm(ctypes.byref(_t(64, 48)), ctypes.byref(_t(48, 48)), FAKE, 48, 0, None, None) == 4
     assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), FAKE, 40, 0, None, None) == 2              # ldc < N
     assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), FAKE + 1, 48, 0, None, None) == 3          # c misaligned
     assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), None, 48, 0, None, None) == 1

@@ -67,7 +67,10 @@ def _check(out, ref, absum, bf16):
 SHAPES = [(256, 256, 256),    # the tiny fprop workload shape
           (1, 1, 32), (17, 33, 64), (128, 256, 256), (129, 257, 288), (300, 520, 1024),
           (256, 384, 96), (64, 1000, 512), (520, 130, 2048),
-          (136, 264, 8192)]   # K >= 8192: the four-stage epilogue with direct bf16 stores
+          (136, 264, 8192),   # K >= 8192
+          # K % 32 == 16: code rows of K/2 bytes are not a 16-byte multiple (the
+          # producer copies them; single-CTA kernel)
+          (64, 96, 16), (130, 300, 48), (200, 256, 80), (129, 520, 272)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -159,9 +162,10 @@ def test_dgrad_and_wgrad_operands(B, orc):
     assert rel < 0.25
 
 
+@pytest.mark.parametrize("K", [256, 48])
 @pytest.mark.parametrize("fp32", [False, True])
-def test_grouped_gemm(B, orc, fp32):
-    K, n = 256, 304          # last N tile ragged; its second 128-row scale block is absent
+def test_grouped_gemm(B, orc, fp32, K):
+    n = 304                  # last N tile ragged; its second 128-row scale block is absent
     offsets = np.array([0, 0, 1, 130, 130, 400, 656, 657, 800], dtype=np.int64)   # empty and 1-row groups
     E = len(offsets) - 1
     R = int(offsets[-1])
