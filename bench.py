@@ -181,6 +181,7 @@ class Workload:
         self.qa = q(R, L, dev, n_amax=E, sf_size=B.sf_bytes_grouped(R, L, E))
         self.qh = q(R, Hh, dev, n_amax=E, sf_size=B.sf_bytes_grouped(R, Hh, E))
         self.dy_amax = torch.empty(2, dtype=torch.float32, device=dev)
+        self.dy_zeros = torch.empty(1, dtype=torch.int64, device=dev)
         self.y = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
         self.dx = torch.empty(T, K, dtype=torch.bfloat16, device=dev)
         self.dw = torch.empty(N, K, dtype=torch.float32, device=dev)
@@ -193,9 +194,8 @@ class Workload:
             ("quantize_2d W (amax+W,W^T)", "hbm", 5.125 * N * K),
             ("gemm fprop", "tensor", gem(T, N, K)),
             ("dual amax dY (max |dY| and max |RHT(dY)|, one read)", "hbm", 2.0 * T * N),
-            ("quantize_1d dY (SR)", "hbm", 2.5625 * T * N),
+            ("dual_sr_quantize dY (1x16 SR rows + RHT SR columns, one read)", "hbm", 3.125 * T * N),
             ("gemm dgrad", "tensor", gem(T, K, N)),
-            ("rht_quantize dY (SR)", "hbm", 2.5625 * T * N),
             ("rht_quantize X (amax+RNE)", "hbm", 4.5625 * T * K),
             ("gemm wgrad", "tensor", gem(N, K, T)),
             ("quantize_2d W_up, W_down (amax+W)", "hbm", 4.5625 * 2 * E * Hh * L),
@@ -216,21 +216,22 @@ class Workload:
         B.quantize_1d(self.x, B.RNE, 0, out=self.qx); mk(0)
         B.quantize_2d(self.w, want_t=True, out=self.qw, out_t=self.qwt); mk(1)
         B.gemm(self.qx, self.qw, B.OUT_BF16, out=self.y); mk(2)
-        # both tensor amaxes of dY (row SR quantiser, RHT quantiser) from one read
+        # both tensor amaxes of dY (row SR quantiser, RHT quantiser) from one read,
+        # then both SR operands (and the zero-code count) from one more
         B.dual_amax(self.dy, self.mask, out=self.dy_amax); mk(3)
-        B.quantize_1d(self.dy, B.SR, self.seed, amax_in=self.dy_amax[0:1], out=self.qdy); mk(4)
+        B.dual_sr_quantize(self.dy, self.mask, self.seed, self.wseed, self.dy_amax, out_row=self.qdy, out_t=self.sdy,
+                           zero_count=self.dy_zeros); mk(4)
         self.qwt.amax = self.qw.amax
         B.gemm(self.qdy, self.qwt, B.OUT_BF16, out=self.dx); mk(5)
-        B.rht_quantize(self.dy, self.mask, B.SR, self.wseed, amax_in=self.dy_amax[1:2], out=self.sdy); mk(6)
-        B.rht_quantize(self.x, self.mask, B.RNE, 0, out=self.sx); mk(7)
-        B.gemm(self.sdy, self.sx, B.OUT_FP32, out=self.dw); mk(8)
+        B.rht_quantize(self.x, self.mask, B.RNE, 0, out=self.sx); mk(6)
+        B.gemm(self.sdy, self.sx, B.OUT_FP32, out=self.dw); mk(7)
         B.quantize_2d(self.w_up, want_t=False, out=self.qwu)
-        B.quantize_2d(self.w_down, want_t=False, out=self.qwd); mk(9)
-        B.quantize_1d_grouped(self.a, self.offsets, B.RNE, 0, out=self.qa); mk(10)
+        B.quantize_2d(self.w_down, want_t=False, out=self.qwd); mk(8)
+        B.quantize_1d_grouped(self.a, self.offsets, B.RNE, 0, out=self.qa); mk(9)
         B.grouped_gemm(self.qa, self.offsets, self.qwu, self.moe.expert_hidden, B.OUT_BF16, out=self.h,
-                       c_amax=self.qh.amax); mk(11)
-        B.quantize_1d_grouped(self.h, self.offsets, B.RNE, 0, amax_in=self.qh.amax, out=self.qh); mk(12)
-        B.grouped_gemm(self.qh, self.offsets, self.qwd, self.moe.latent, B.OUT_BF16, out=self.o); mk(13)
+                       c_amax=self.qh.amax); mk(10)
+        B.quantize_1d_grouped(self.h, self.offsets, B.RNE, 0, amax_in=self.qh.amax, out=self.qh); mk(11)
+        B.grouped_gemm(self.qh, self.offsets, self.qwd, self.moe.latent, B.OUT_BF16, out=self.o); mk(12)
 
 
 def gemm_bytes_table(d, m, R: int) -> dict:
@@ -482,7 +483,7 @@ def time_ops(wk, steps: int = 5):
 
 
 # the ops of the Workload step that make up each stated configuration
-CONFIG_OPS = {"c2": (0, 3), "c3": (3, 9), "c4": (9, 14)}
+CONFIG_OPS = {"c2": (0, 3), "c3": (3, 8), "c4": (8, 13)}
 
 
 def measure_configs(dev, pk: dict, fp4: dict, super_wk=None, steps: int = 5) -> dict:
@@ -650,18 +651,20 @@ def main(argv=None):
                 "traffic": traffic, "traffic_unit": "bytes per launch (ncu dram read + write)",
                 "algorithmic_bytes": int(0.5625 * (wk.dense.tokens + wk.dense.out) * wk.dense.hidden
                                          + 2 * wk.dense.tokens * wk.dense.out)}
-    qi = [n for n, _, _ in wk.ops].index("quantize_1d dY (SR)")
+    qi = [n for n, _, _ in wk.ops].index("dual_sr_quantize dY (1x16 SR rows + RHT SR columns, one read)")
     q_dy = op_ms[qi]
     q_gbs = wk.ops[qi][2] / (q_dy * 1e-3) / 1e9
-    roofline_q = {"kernel": "k_quant1d<SR> (dY 1x16 SR, amax supplied)", "bound": "hbm",
+    roofline_q = {"kernel": "k_rht<4> (dY: 1x16 SR rows and RHT SR columns from one read, amaxes supplied)",
+                  "bound": "hbm",
                   "achieved": round(q_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                   "frac": round(q_gbs / pk["hbm_gbs"], 4), "frac_hbm_nominal_8tbs": round(q_gbs / HBM_NOMINAL_GBS, 4),
                   "peak_note": "HBM copy bandwidth (measured)",
-                  "traffic": profiled_quant_traffic(f"k_quant1d_sr_{args.workload}.md", "k_quant1d"),
-                  "alu_estimate": alu_roofline(wk.dense.tokens * wk.dense.out, q_dy, sm_mhz, sms)}
+                  "traffic": profiled_quant_traffic(f"k_rht_dual_sr_{args.workload}.md", "k_rht"),
+                  "alu_estimate": alu_roofline(wk.dense.tokens * wk.dense.out, q_dy, sm_mhz, sms,
+                                               2 * SR_ALU_OPS_PER_ELEMENT)}
 
     supplied = measure_supplied_amax(wk, pk)
-    zeros = int(B.count_zero_codes(wk.qdy).item())
+    zeros = int(wk.dy_zeros.item())
     zero_frac = zeros / float(wk.dense.tokens * wk.dense.out)
     next_rows = measure_next_rows(wk, pk, fp4)
     configs = None
@@ -737,6 +740,9 @@ def measure_supplied_amax(wk: Workload, pk: dict, iters: int = 5):
          lambda: B.quantize_2d(wk.w_up, want_t=False, amax_in=wk.qwu.amax, out=wk.qwu)),
         ("rht_quantize dY (SR)", 2.5625 * T * N,
          lambda: B.rht_quantize(wk.dy, wk.mask, B.SR, wk.wseed, amax_in=wk.sdy.amax, out=wk.sdy)),
+        ("dual_sr_quantize dY (rows and RHT columns, SR)", 3.125 * T * N,
+         lambda: B.dual_sr_quantize(wk.dy, wk.mask, wk.seed, wk.wseed, wk.dy_amax, out_row=wk.qdy, out_t=wk.sdy,
+                                    zero_count=wk.dy_zeros)),
         ("rht_quantize X (RNE)", 2.5625 * T * K,
          lambda: B.rht_quantize(wk.x, wk.mask, B.RNE, 0, amax_in=wk.sx.amax, out=wk.sx)),
         ("quantize_1d_grouped A (RNE)", 2.5625 * R * L,

@@ -240,6 +240,23 @@ nvfp4_status nvfp4_rht_amax(const void *x, int64_t tokens, int64_t cols, int64_t
 nvfp4_status nvfp4_dual_amax(const void *x, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask,
                              float *amax_plain, float *amax_rht, nvfp4_stream_t stream);
 
+/* Both stochastically rounded operands of a gradient dY from one read of it
+ * (Super summary "Infra design": stochastic rounding of gradients, RHT on
+ * the inputs of wgrad; Ultra report 2.2): out_row receives exactly what
+ * nvfp4_quantize_1d(dy, NVFP4_ROUND_SR, seed_row, amax_row) gives (the dgrad
+ * operand [tokens, cols]) and out_t exactly what nvfp4_rht_quantize(dy,
+ * sign_mask, NVFP4_ROUND_SR, seed_rht, amax_rht) gives (the wgrad operand
+ * [cols, tokens]); both are encoded from the same staged tile of dY.
+ * amax_row, amax_rht: device, 1 float each (nvfp4_dual_amax gives both),
+ * copied into out_row->amax and out_t->amax.  zero_count (device, one 64-bit
+ * word, nullable): receives the number of zero-magnitude codes of out_row,
+ * what nvfp4_count_zero_codes(out_row) would count (zeroed by the call).
+ * dy: bf16 [tokens, cols], row stride ld, tokens % 16 == 0, cols % 16 == 0. */
+nvfp4_status nvfp4_dual_sr_quantize(const void *dy, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask,
+                                    uint64_t seed_row, uint64_t seed_rht, const float *amax_row,
+                                    const float *amax_rht, nvfp4_tensor *out_row, nvfp4_tensor *out_t,
+                                    uint64_t *zero_count, nvfp4_stream_t stream);
+
 /* Number of E2M1 codes of magnitude zero (+0 and -0) in a quantised tensor
  * (rows * cols codes): the zero-gradient fraction the pages monitor (Super
  * summary "Infra design"; section 2.2: small gradients underflow to zero).

@@ -31,7 +31,8 @@ STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_NULL", 2: "NVFP4_ERR_SHAPE", 3: "NVFP4_ER
 EXPORTS = ["nvfp4_sf_bytes", "nvfp4_sf_bytes_grouped", "nvfp4_sf_offset", "nvfp4_amax", "nvfp4_quantize_1d",
            "nvfp4_quantize_1d_grouped", "nvfp4_quantize_2d", "nvfp4_quantize_2d_fused_workspace",
            "nvfp4_quantize_2d_fused", "nvfp4_quantize_2d_fused_static", "nvfp4_rht_amax",
-           "nvfp4_rht_quantize", "nvfp4_dual_amax", "nvfp4_count_zero_codes", "nvfp4_quantize_1d_mse",
+           "nvfp4_rht_quantize", "nvfp4_dual_amax", "nvfp4_dual_sr_quantize", "nvfp4_count_zero_codes",
+           "nvfp4_quantize_1d_mse",
            "nvfp4_sr_fp16", "nvfp4_group_k_capacity", "nvfp4_rht_quantize_grouped", "nvfp4_gemm",
            "nvfp4_grouped_gemm", "nvfp4_grouped_gemm_k", "nvfp4_status_string", "nvfp4_last_error",
            "nvfp4_device_status", "nvfp4_launch_count", "nvfp4_debug_inject", "nvfp4_debug_wait_timeout"]
@@ -83,6 +84,7 @@ def lib():
             "nvfp4_quantize_1d_mse": (st, [P, i64, i64, i64, P, TP, P]),
             "nvfp4_dual_amax": (st, [P, i64, i64, i64, ctypes.c_uint16, P, P, P]),
             "nvfp4_count_zero_codes": (st, [TP, P, P]),
+            "nvfp4_dual_sr_quantize": (st, [P, i64, i64, i64, ctypes.c_uint16, u64, u64, P, P, TP, TP, P, P]),
             "nvfp4_rht_quantize_grouped": (st, [P, i64, i64, i64, P, i32, i64, ctypes.c_uint16, ctypes.c_int,
                                                 ctypes.c_uint64, P, TP, P]),
             "nvfp4_grouped_gemm_k": (st, [TP, TP, P, i32, P, i64, ctypes.c_int, P, P]),
@@ -285,6 +287,27 @@ def dual_amax(x: torch.Tensor, sign_mask: int, out: Optional[torch.Tensor] = Non
     _check(lib().nvfp4_dual_amax(_ptr(x), tokens, cols, ld, sign_mask, _ptr(out), ctypes.c_void_p(out.data_ptr() + 4),
                                  _stream(stream)))
     return out
+
+
+def dual_sr_quantize(dy: torch.Tensor, sign_mask: int, seed_row: int, seed_rht: int, amax: torch.Tensor,
+                     out_row: Optional[QTensor] = None, out_t: Optional[QTensor] = None,
+                     zero_count: Optional[torch.Tensor] = None, stream=None):
+    """Both stochastically rounded operands of a gradient from one read:
+    dy bf16 [tokens, cols], amax float32 [2] = (max |dy|, max |RHT(dy)|) as
+    dual_amax gives -> (row operand [tokens, cols] as quantize_1d(SR,
+    seed_row), RHT operand [cols, tokens] as rht_quantize(SR, seed_rht));
+    zero_count (int64 [1], optional) receives the row operand's zero-code
+    count."""
+    tokens, cols, ld = _rows2d(dy)
+    dev = dy.device
+    out_row = empty_qtensor(tokens, cols, dev) if out_row is None else out_row
+    out_t = empty_qtensor(cols, tokens, dev) if out_t is None else out_t
+    assert amax.dtype == torch.float32 and amax.numel() >= 2
+    cr, ct = out_row.c(), out_t.c()
+    _check(lib().nvfp4_dual_sr_quantize(_ptr(dy), tokens, cols, ld, sign_mask, seed_row, seed_rht, _ptr(amax),
+                                        ctypes.c_void_p(amax.data_ptr() + 4), ctypes.byref(cr), ctypes.byref(ct),
+                                        _ptr(zero_count), _stream(stream)))
+    return out_row, out_t
 
 
 def count_zero_codes(q: QTensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:

@@ -489,6 +489,48 @@ nvfp4_status nvfp4_dual_amax(const void* x, int64_t tokens, int64_t cols, int64_
     return launched("k_rht dual amax");
 }
 
+nvfp4_status nvfp4_dual_sr_quantize(const void* dy, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask,
+                                    uint64_t seed_row, uint64_t seed_rht, const float* amax_row, const float* amax_rht,
+                                    nvfp4_tensor* out_row, nvfp4_tensor* out_t, uint64_t* zero_count,
+                                    nvfp4_stream_t stream) {
+    NVFP4_INJECT_CHECK();
+    NVFP4_TRY(check_input(dy, tokens, cols, ld, 16, "dy", false));
+    if (tokens % 16 != 0) return fail(NVFP4_ERR_SHAPE, "tokens=%lld is not a multiple of 16", (long long)tokens);
+    if (cdiv(tokens, 64) > 65535) return fail(NVFP4_ERR_LIMIT, "tokens too large");
+    if (amax_row == nullptr || amax_rht == nullptr) return fail(NVFP4_ERR_NULL, "amax_row or amax_rht is NULL");
+    NVFP4_TRY(check_out(out_row, tokens, cols, true, "out_row"));
+    NVFP4_TRY(check_out(out_t, cols, tokens, true, "out_t"));
+    if (zero_count != nullptr && ((uintptr_t)zero_count & 7u) != 0) return fail(NVFP4_ERR_ALIGN, "zero_count not 8-byte aligned");
+    NVFP4_TRY(check_device());
+    if (zero_count != nullptr) NVFP4_TRY(cuda_call(cudaMemsetAsync(zero_count, 0, sizeof(uint64_t), stream), "memset count"));
+    if (tokens == 0 || cols == 0) {
+        NVFP4_TRY(cuda_call(cudaMemcpyAsync(out_row->amax, amax_row, 4, cudaMemcpyDeviceToDevice, stream), "amax copy"));
+        return cuda_call(cudaMemcpyAsync(out_t->amax, amax_rht, 4, cudaMemcpyDeviceToDevice, stream), "amax copy");
+    }
+    RowSR rsr;
+    rsr.amax_row = amax_row;
+    rsr.seed_row = seed_row;
+    rsr.codes_r = (uint8_t*)out_row->codes;
+    rsr.sf_r = out_row->sf;
+    rsr.zero_count = reinterpret_cast<unsigned long long*>(zero_count);
+    rsr.amax_row_copy = amax_row != out_row->amax ? out_row->amax : nullptr;
+    float* copy_t = amax_rht != out_t->amax ? out_t->amax : nullptr;
+    const dim3 grid((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64));
+    k_rht<4><<<grid, 256, 0, stream>>>((const uint16_t*)dy, tokens, cols, ld, sign_mask, const_cast<float*>(amax_rht),
+                                       seed_rht, (uint8_t*)out_t->codes, out_t->sf, copy_t, nullptr, 1, 0, rsr);
+    NVFP4_TRY(launched("k_rht dual SR"));
+    // scale padding rows of both operands (rows past tokens, or past cols)
+    if (tokens % 128 != 0) {
+        k_zero_pad_rows<<<64, 256, 0, stream>>>(out_row->sf, tokens, cols, nullptr, 0);
+        NVFP4_TRY(launched("k_zero_pad_rows"));
+    }
+    if (cols % 128 != 0) {
+        k_zero_pad_rows<<<64, 256, 0, stream>>>(out_t->sf, cols, tokens, nullptr, 0);
+        NVFP4_TRY(launched("k_zero_pad_rows"));
+    }
+    return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_count_zero_codes(const nvfp4_tensor* t, uint64_t* count, nvfp4_stream_t stream) {
     NVFP4_INJECT_CHECK();
     if (t == nullptr || count == nullptr) return fail(NVFP4_ERR_NULL, "t or count is NULL");

@@ -947,6 +947,21 @@ __device__ __forceinline__ void rht16(float (&x)[16], uint32_t sign_mask) {
 // quantised with its own amax (amax[g]).  A block covers 64 padded tokens of
 // one expert; blocks past kpad[G] do nothing.  Dynamic shared memory: two
 // tables of G+1 ints.
+// MODE 4 (the dual stochastic encoder of a gradient, one read of each tile):
+// MODE 2's transposed RHT operand with seed / amax, and from the same staged
+// tile the row-wise 1x16 SR operand [tokens, cols] of the row quantiser
+// (seed_row, tensor amax amax_row[0]; SR index e = t * cols + c) into
+// codes_r / sf_r, whose zero-magnitude codes are added to *zero_count
+// (nullable).  cols % 16 == 0.
+struct RowSR {
+    const float* amax_row = nullptr;
+    uint64_t seed_row = 0;
+    uint8_t* codes_r = nullptr;
+    uint8_t* sf_r = nullptr;
+    unsigned long long* zero_count = nullptr;
+    float* amax_row_copy = nullptr;     // receives amax_row[0] (nullable)
+};
+
 template <int MODE, bool GROUPED = false>
 __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int64_t tokens,
                                              int64_t cols, int64_t ld, uint32_t sign_mask,
@@ -954,7 +969,7 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
                                              uint8_t* __restrict__ codes_t, uint8_t* __restrict__ sf_t,
                                              float* __restrict__ amax_copy,
                                              const int64_t* __restrict__ offsets = nullptr, int32_t groups = 1,
-                                             int64_t kt = 0) {
+                                             int64_t kt = 0, RowSR rsr = RowSR{}) {
     __shared__ __align__(16) uint16_t tile[64][256 + 8];
     const int64_t c0 = (int64_t)blockIdx.x * 256, t0 = (int64_t)blockIdx.y * 64;
     const int tid = threadIdx.x;
@@ -1039,6 +1054,52 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
         }
         return;
     }
+    if (MODE == 4) {
+        // row operand: thread t encodes blocks 4 (t & 3) .. + 3 (64 channels) of
+        // token row t >> 2 of the tile
+        const int r = tid >> 2, part = tid & 3;
+        const float s_row = tensor_encode_scale(rsr.amax_row[0]);
+        const PhiloxKeys key_r = philox_keys(rsr.seed_row);
+        const int64_t t = t0 + r;
+        uint32_t zeros = 0, word = 0;
+        const bool row_ok = r < ntok;
+        uint32_t cw[8];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int64_t c = c0 + 64 * part + 16 * b;
+            cw[2 * b] = cw[2 * b + 1] = 0u;
+            if (!row_ok || c >= cols) continue;
+            const uint4 va = *reinterpret_cast<const uint4*>(&tile[r][64 * part + 16 * b]);
+            const uint4 vb = *reinterpret_cast<const uint4*>(&tile[r][64 * part + 16 * b + 8]);
+            const uint32_t m = bf16x16_absmax(va, vb);
+            const uint32_t sc = block_scale(__uint_as_float(m << 16), s_row);
+            word |= sc << (8 * b);
+            if (sc != 0) {
+                const float ratio = element_ratio(s_row, sc);
+                const uint64_t e0 = (uint64_t)t * (uint64_t)cols + (uint64_t)c;
+                cw[2 * b] = encode8<true>(va, ratio, false, key_r, e0);
+                cw[2 * b + 1] = encode8<true>(vb, ratio, false, key_r, e0 + 8);
+            }
+            zeros += zero_nibbles(cw[2 * b]) + zero_nibbles(cw[2 * b + 1]);
+        }
+        const int64_t cp = c0 + 64 * part;
+        if (row_ok && cp < cols) {
+            // a code row is cols/2 bytes, a multiple of 8 only: 8-byte stores
+            uint8_t* dst = rsr.codes_r + t * (cols >> 1) + (cp >> 1);
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                if (cp + 16 * b < cols) reinterpret_cast<uint2*>(dst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
+            // four scale columns from a multiple of 4: one word (zeros past cols
+            // are the scale padding of the last atom column)
+            *reinterpret_cast<uint32_t*>(rsr.sf_r + sf_offset(t, cp >> 4, cols)) = word;
+        }
+        if (rsr.zero_count != nullptr) {
+            zeros = __reduce_add_sync(0xFFFFFFFFu, zeros);
+            if ((tid & 31) == 0 && zeros != 0) atomicAdd(rsr.zero_count, (unsigned long long)zeros);
+        }
+        if (rsr.amax_row_copy != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
+            *rsr.amax_row_copy = rsr.amax_row[0];
+    }
     if (!active) return;
     const float s_enc = tensor_encode_scale(amax[g]);
     const PhiloxKeys key = philox_keys(seed);
@@ -1062,7 +1123,7 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
         float f[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(v[i], ratio);
-        if (MODE == 2) {
+        if (MODE == 2 || MODE == 4) {
             const uint64_t e0 = (uint64_t)c * (uint64_t)ocols + (uint64_t)(t0 + 16 * j);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {

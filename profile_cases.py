@@ -21,6 +21,7 @@ the input):
   quant2d_moe_fused k_quant2d_fused: the same weights with their per-expert amax in one launch
   dual_amax         k_rht<3>: max |dY| and max |RHT(dY)| in one read
   rht_sr            k_rht<2>: RHT(dY)^T with SR
+  dual_sr           k_rht<4>: 1x16 SR rows of dY and RHT(dY)^T with SR from one read
   rht_rne           k_rht<1>: RHT(X)^T with RNE
   amax_grouped      k_amax_grouped (then k_quant1d): per-expert amax of the routed activations A
   quant1d_grouped_a k_quant1d<RNE, grouped>: A
@@ -48,7 +49,8 @@ if ROOT not in sys.path:
 from nvfp4_precision_02_b300 import binding as B  # noqa: E402
 from nvfp4_precision_02_b300 import workloads as wl  # noqa: E402
 
-OPS = ["amax", "quant1d_rne", "quant1d_sr", "quant2d", "quant2d_moe", "quant2d_moe_fused", "dual_amax", "rht_sr", "rht_rne",
+OPS = ["amax", "quant1d_rne", "quant1d_sr", "quant2d", "quant2d_moe", "quant2d_moe_fused", "dual_amax", "rht_sr",
+       "dual_sr", "rht_rne",
        "amax_grouped", "quant1d_grouped_a", "quant1d_grouped_h", "rht_grouped_sr", "quant1d_mse", "sr_fp16",
        "count_zero", "gemm_fprop", "gemm_dgrad", "gemm_wgrad", "grouped_up", "grouped_down", "grouped_dgrad",
        "grouped_wgrad"]
@@ -60,12 +62,17 @@ def prepare(op: str, which: str, dev):
     m = wl.ULTRA_MOE if which == "ultra" else wl.SUPER_MOE
     seed, mask = wl.SEEDS["sr"], wl.sign_mask_from_seed(wl.SEEDS["rht_sign"])
     T, K, N = d.tokens, d.hidden, d.out
-    if op in ("quant1d_sr", "dual_amax", "rht_sr", "count_zero"):
+    if op in ("quant1d_sr", "dual_amax", "rht_sr", "count_zero", "dual_sr"):
         dy = wl.dense_inputs(d, which, device=dev, want=("dy",))["dy"]
         am = torch.empty(2, dtype=torch.float32, device=dev)
         B.dual_amax(dy, mask, out=am)
         if op == "dual_amax":
             return lambda: B.dual_amax(dy, mask, out=am)
+        if op == "dual_sr":
+            qr, qt = B.empty_qtensor(T, N, dev), B.empty_qtensor(N, T, dev)
+            zc = torch.empty(1, dtype=torch.int64, device=dev)
+            return lambda: B.dual_sr_quantize(dy, mask, seed, wl.wgrad_seed(seed), am, out_row=qr, out_t=qt,
+                                              zero_count=zc)
         if op == "rht_sr":
             q = B.empty_qtensor(N, T, dev)
             return lambda: B.rht_quantize(dy, mask, B.SR, wl.wgrad_seed(seed), amax_in=am[1:2], out=q)

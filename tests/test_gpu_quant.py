@@ -284,3 +284,28 @@ def test_dual_amax_and_zero_code_count(B, orc, tokens, cols):
         want = int(((codes & 7) == 0).sum() + (((codes >> 4) & 7) == 0).sum())
         assert int(n0.item()) == want
     assert B.device_status() == 0
+
+
+@pytest.mark.parametrize("tokens,cols", [(16, 16), (64, 272), (80, 1040), (1040, 320), (208, 48)])
+def test_dual_sr_quantize(B, orc, tokens, cols):
+    """One read of a gradient gives both stochastically rounded operands: the
+    row operand equals the oracle's 1x16 SR quantisation (seed_row, amax of
+    |dy|) and the transposed operand the oracle's RHT + SR quantisation
+    (seed_rht, amax of |RHT(dy)|), bytes and padding included; the zero count
+    is the number of zero-magnitude codes of the row operand.  Shapes cover
+    a partial 64-token tile, a partial 256-channel tile, rows and columns not
+    multiples of 128 and a scale-column padding."""
+    x = _x(tokens, cols, seed=7 * tokens + cols, scale=1e-3, spread=6.0)
+    mask, s_row, s_rht = 0x2D96, 7, 7 ^ 0x9E3779B97F4A7C15
+    a = B.dual_amax(x.cuda(), mask)
+    zc = torch.full((1,), -1, dtype=torch.int64, device="cuda")
+    qr, qt = B.dual_sr_quantize(x.cuda(), mask, s_row, s_rht, a, zero_count=zc)
+    torch.cuda.synchronize()
+    got = np_u8(a)
+    ref_r = orc.quantize_1d(x, mode=1, seed=s_row, amax_in=float(got[0]))
+    ref_t = orc.rht_quantize(x, mask, mode=1, seed=s_rht, amax_in=float(got[1]))
+    _same(qr, ref_r, tokens, cols)
+    _same(qt, ref_t, cols, tokens)
+    codes = ref_r["codes"]
+    assert int(zc.item()) == int(((codes & 7) == 0).sum() + (((codes >> 4) & 7) == 0).sum())
+    assert B.device_status() == 0

@@ -319,6 +319,7 @@ def test_zero_code_count_full_size(run, orc):
     zero-magnitude nibbles of the same codes."""
     wk, B = run.wk, run.B
     cnt = int(B.count_zero_codes(wk.qdy).item())
+    assert int(wk.dy_zeros.item()) == cnt        # the count the step's dual SR quantiser returned
     c = wk.qdy.codes.cpu().numpy()
     assert cnt == int(((c & 7) == 0).sum()) + int((((c >> 4) & 7) == 0).sum())
     assert 0 < cnt < c.size * 2
