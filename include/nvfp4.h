@@ -188,15 +188,19 @@ size_t nvfp4_quantize_2d_fused_workspace(int64_t batch);
 
 /* The same W result as nvfp4_quantize_2d with amax_in == NULL and out_t ==
  * NULL (per-entry amax, W codes and GEMM-ready scales, optional tile scales)
- * for batched weights whose entries fit in L2, such as the LatentMoE expert
- * weights (2D block scaling of weights, Super summary "Infra design").  One
- * cooperative launch computes each entry's amax and then quantises the entry,
- * re-reading it about one entry plus two items per warp later so that the
- * second read can hit L2.  Whether it does depends on the L2 keeping that
- * window: for the LatentMoE expert weights on B300 most of the second read
- * still came from HBM and the two-launch nvfp4_quantize_2d was faster, so
- * this entry point is an alternative, not the default.  The transposed copy
- * is not produced (use nvfp4_quantize_2d for W^T).
+ * for batched weights such as the LatentMoE expert weights (2D block scaling
+ * of weights, Super summary "Infra design"), in one cooperative launch that
+ * reads each element once from HBM.  When an entry has at most 18 units of
+ * 16 x 256 elements per SM (5120 x 2048 on 148 SMs), every CTA keeps its share
+ * of the entry on chip (TMA into shared memory, then registers) while the
+ * entry's amax is exchanged through the workspace, and then encodes it;
+ * larger entries are read a second time within a short window so that the
+ * second read can hit L2.  Either way the entries are processed one after
+ * another with one grid-wide exchange each, and for the LatentMoE expert
+ * weights on B300 the two-launch nvfp4_quantize_2d (amax, then quantise) is
+ * still faster, so this entry point is an alternative, not the default.
+ * Requires w 16-byte aligned with ld % 8 == 0.  The transposed copy is not
+ * produced (use nvfp4_quantize_2d for W^T).
  * workspace: device, caller-allocated, at least
  * nvfp4_quantize_2d_fused_workspace(batch) bytes, 16-byte aligned; the call
  * zeroes and uses it (per-entry arrival counters), so calls sharing one

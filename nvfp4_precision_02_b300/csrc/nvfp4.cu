@@ -18,6 +18,7 @@
 #include "common.cuh"
 #include "quant.cuh"
 #include "gemm.cuh"
+#include "quant2d_resident.cuh"
 
 using namespace nvfp4;
 
@@ -43,21 +44,26 @@ nvfp4_status fail(nvfp4_status st, const char* fmt, ...) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Device ordinals this library serves: per-device tables below are indexed by
+// the ordinal, and check_device() refuses ordinals at or above the bound.
+constexpr int MAX_DEVICES = 64;
+
 struct DeviceInfo {
     bool checked = false;
     bool ok = false;
     int sms = 0;
     bool gemm_attr = false;
     int pair_clusters = 0;
+    bool q2r_attr = false;
 };
-DeviceInfo g_dev[64];
+DeviceInfo g_dev[MAX_DEVICES];
 std::mutex g_dev_mu;
 
 // Current device must be compute capability 10.3 (B300, sm_103a).
 nvfp4_status check_device(int* sms = nullptr, int* dev_out = nullptr) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    if (e != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
         cudaGetLastError();
         return fail(NVFP4_ERR_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
     }
@@ -402,6 +408,55 @@ nvfp4_status nvfp4_quantize_2d_fused(const void* w, int64_t batch, int64_t rows,
     NVFP4_TRY(cuda_call(cudaMemsetAsync(workspace, 0, nvfp4_quantize_2d_fused_workspace(batch), stream), "memset workspace"));
     if ((rows / 16) * cdiv(cols, Q2F_ITEM_COLS) > (int64_t)0x7FFFFFFF)
         return fail(NVFP4_ERR_LIMIT, "an entry of %lld x %lld is too large", (long long)rows, (long long)cols);
+    const int64_t col_units = cdiv(cols, Q2R_UNIT_COLS);
+    const int64_t units = (rows / 16) * col_units;
+    if (units <= (int64_t)Q2R_MAX_UNITS * sms && batch * rows <= (int64_t)0x7FFFFFFF) {
+        // every entry fits in the CTAs' registers: one read of HBM
+        {
+            std::lock_guard<std::mutex> lk(g_dev_mu);
+            if (!g_dev[dev].q2r_attr) {
+                NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_quant2d_resident, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         Q2R_SMEM_BYTES), "smem attr"));
+                g_dev[dev].q2r_attr = true;
+            }
+        }
+        int per_sm = 0;
+        NVFP4_TRY(cuda_call(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant2d_resident, Q2R_THREADS,
+                                                                          Q2R_SMEM_BYTES), "occupancy"));
+        if (per_sm < 1) return fail(NVFP4_ERR_CUDA, "resident 2D quantiser cannot be resident");
+        auto fn = encode_fn();
+        if (fn == nullptr) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+        const int64_t box_cols = std::min<int64_t>(cols, Q2R_UNIT_COLS);
+        CUtensorMap map;
+        cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(batch * rows)};
+        cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+        cuuint32_t box[2] = {(cuuint32_t)box_cols, 16u};
+        cuuint32_t estr[2] = {1u, 1u};
+        const CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled (weights) failed (%d)", (int)r);
+        Quant2dResidentArgs qa{batch, rows, cols, units, col_units, (int32_t)(box_cols * 2), out->amax,
+                               (uint32_t*)workspace, (uint8_t*)out->codes, out->sf, tile_sf};
+        const int64_t grid = std::min<int64_t>(sms, units);
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(Q2R_THREADS);
+        cfg.dynamicSmemBytes = Q2R_SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        NVFP4_TRY(cuda_call(cudaLaunchKernelEx(&cfg, k_quant2d_resident, map, qa), "k_quant2d_resident launch"));
+        NVFP4_TRY(launched("k_quant2d_resident"));
+        if ((rows % 128) || ((cols / 16) % 4)) {
+            k_quant2d_pad<<<dim3(16, (unsigned)batch), 256, 0, stream>>>(out->sf, nullptr, rows, cols);
+            NVFP4_TRY(launched("k_quant2d_pad"));
+        }
+        return NVFP4_OK;
+    }
     int per_sm = 0;
     NVFP4_TRY(cuda_call(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant2d_fused, Q2F_THREADS, 0), "occupancy"));
     if (per_sm < 1) return fail(NVFP4_ERR_CUDA, "fused 2D quantiser cannot be resident");
@@ -433,7 +488,7 @@ nvfp4_status nvfp4_quantize_2d_fused(const void* w, int64_t batch, int64_t rows,
 static __device__ __align__(256) uint32_t g_q2f_static_scratch[NVFP4_STATIC_MAX_BATCH + 8];
 
 namespace {
-uint32_t* g_static_scratch_ptr[64] = {};
+uint32_t* g_static_scratch_ptr[MAX_DEVICES] = {};   // by device ordinal (check_device bounds it)
 }
 
 nvfp4_status nvfp4_quantize_2d_fused_static(const void* w, int64_t batch, int64_t rows, int64_t cols, int64_t ld,

@@ -621,9 +621,10 @@ __global__ void __launch_bounds__(128) k_quant2d(const uint16_t* __restrict__ w,
 // Per-entry amax and 2D quantisation of a batched weight [batch, rows, cols]
 // (W codes and scales; no W^T) in one launch, reading each element twice
 // within a short window so that the second read, for the codes, can hit L2.
-// Measured on B300 with the LatentMoE expert weights (5.5 and 21 MB per
-// entry), most second reads still missed L2 and this launch took 1.3x the
-// time of the two-launch amax + quantise path, which the step therefore uses.
+// Used for entries too large for k_quant2d_resident (which keeps an entry on
+// chip); measured on B300 with the LatentMoE expert weights (5.5 and 21 MB
+// per entry), most second reads still missed L2 and this launch took 1.3x the
+// time of the two-launch amax + quantise path.
 //
 // Work is split into items of 16 rows x Q2F_ITEM_COLS columns (16x64 strips
 // of 16x16 tiles) of one entry; entry e holds items e*ipe .. (e+1)*ipe - 1.
@@ -642,7 +643,8 @@ __global__ void __launch_bounds__(128) k_quant2d(const uint16_t* __restrict__ w,
 // warp's order, and the launch is cooperative (every warp resident).  Each
 // wait is bounded anyway: the first to give up records DEV_TIMEOUT and raises
 // counters[batch] (the abort word), after which every warp stops.
-// amax[batch] and counters[batch + 1] must be zero on entry.
+// amax[0 .. batch) and counters[0 .. batch] (the last one is the abort word)
+// must be zero on entry.
 constexpr int Q2F_THREADS = 256;
 constexpr int Q2F_STRIPS = 4;                        // 64-column strips of an item
 constexpr int64_t Q2F_ITEM_COLS = 64 * Q2F_STRIPS;

@@ -146,6 +146,8 @@ def _fake_run(orc):
                      torch.from_numpy(q2["amax"].copy()), K, N)
     wk.dy_amax = torch.tensor([orc.amax(wk.dy), orc.rht_amax(wk.dy, MASK)], dtype=torch.float32)
     wk.qdy = _q(orc.quantize_1d(wk.dy, mode=1, seed=SEED), T, N)
+    c = wk.qdy.codes.numpy()
+    wk.dy_zeros = torch.tensor([int(((c & 7) == 0).sum()) + int((((c >> 4) & 7) == 0).sum())], dtype=torch.int64)
     wk.sdy = _q(orc.rht_quantize(wk.dy, MASK, mode=1, seed=wk.wseed), N, T)
     wk.sx = _q(orc.rht_quantize(wk.x, MASK, mode=0), K, T)
     wk.qwu = _q(orc.quantize_2d(wk.w_up, want_t=False), HH, L)

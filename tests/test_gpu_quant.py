@@ -168,9 +168,11 @@ def test_quantize_1d_ties_signed_zeros_saturation(B, orc):
 def test_quantize_2d_fused(B, orc, batch, rows, cols):
     """One-pass (amax in the same cooperative launch) 2D quantisation gives
     the oracle's bytes, for one entry and several, one 16-row strip per entry
-    and many, a column count that leaves a partial 256-column item, entries
-    of fewer items than the grid has warps (40 x 256 items) and of more
-    (2 x 4096 items), and Ultra expert weights (5120 x 2048)."""
+    and many, column counts below one 256-column unit (64, 80, 128) and ones
+    that leave a partial unit (1040), entries of fewer units than the grid
+    has CTAs, Ultra expert weights (5120 x 2048: the largest entry kept on
+    chip, 17 or 18 units per CTA) and an entry too large for that
+    (2048 x 8192: the path that re-reads through L2)."""
     g = torch.Generator().manual_seed(batch * 1000 + rows + cols)
     w = (torch.randn(batch, rows, cols, generator=g) * 0.02 *
          torch.exp(torch.rand(batch, 1, 1, generator=g) * 6 - 3)).to(torch.bfloat16)
