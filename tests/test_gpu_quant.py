@@ -162,6 +162,28 @@ def test_quantize_1d_ties_signed_zeros_saturation(B, orc):
     assert (np_u8(qt.codes).reshape(ref["codes_t"].shape) == ref["codes_t"]).all()
 
 
+@pytest.mark.parametrize("batch,rows,cols", SHAPES_2D + [(5, 64, 1040), (4, 16, 48), (7, 336, 2064)])
+@pytest.mark.parametrize("supplied", [False, True])
+def test_quantize_2d_w_only(B, orc, batch, rows, cols, supplied):
+    """W without W^T (the expert-weight form): bytes, scales, tile scales and
+    amax equal the oracle's, with the amax computed or supplied in another
+    buffer (then copied into the output), and column counts that leave a
+    partial 64-column block (1040, 2064) or fit in one (48)."""
+    g = torch.Generator().manual_seed(rows * 3 + cols + batch)
+    w = (torch.randn(batch, rows, cols, generator=g) * 0.02 *
+         torch.exp(torch.rand(batch, 1, 1, generator=g) * 6 - 3)).to(torch.bfloat16)
+    ref = orc.quantize_2d(w, want_t=False)
+    am = torch.from_numpy(np.asarray(ref["amax"], dtype=np.float32).copy()).cuda() if supplied else None
+    qw, qt, tile = B.quantize_2d(w.cuda(), want_t=False, want_tile_sf=True, amax_in=am)
+    torch.cuda.synchronize()
+    assert qt is None
+    assert (np_u8(qw.codes).reshape(ref["codes"].shape) == ref["codes"]).all()
+    assert (np_u8(qw.sf) == ref["sf"]).all()
+    assert (np_u8(tile) == ref["tile_sf"]).all()
+    assert (np_u8(qw.amax) == ref["amax"]).all()
+    assert B.device_status() == 0
+
+
 @pytest.mark.parametrize("batch,rows,cols", [(1, 48, 80), (2, 144, 1040), (5, 320, 256), (3, 64, 64),
                                              (7, 2688 // 8, 1024 // 8), (4, 16, 3072),
                                              (40, 512, 2048), (2, 2048, 8192), (1, 5120, 2048), (3, 5120, 2048)])
