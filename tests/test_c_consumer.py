@@ -103,13 +103,11 @@ def test_plain_c_program_against_the_library(tmp_path):
 
 
 
-def test_readme_c_example_compiles_and_links(tmp_path):
-    """The C example of README.md compiles as C11 against the header and
-    links against libnvfp4.so and the CUDA runtime (it is not run)."""
+def test_c_example_compiles_and_links(tmp_path):
+    """The C example (examples/fprop.c) compiles as C11 against the header
+    and links against libnvfp4.so and the CUDA runtime (it is not run)."""
     _need("gcc")
-    text = open(os.path.join(ROOT, "README.md")).read()
-    sec = text[text.index("## C\n"):text.index("## Tests")]
-    code = "\n".join(l[4:] for l in sec.splitlines() if l.startswith("    "))
+    code = open(os.path.join(ROOT, "examples", "fprop.c")).read()
     assert "nvfp4_gemm(" in code
     src = tmp_path / "example.c"
     src.write_text(code + "\nint main(void) { return 0; }\n")
