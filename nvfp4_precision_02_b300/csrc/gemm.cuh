@@ -11,12 +11,17 @@
 //
 // Design (one CTA per SM, persistent over output tiles of 128 x 256):
 //   K stage 256 FP4 elements (128 B per row, 128B-swizzled TMA boxes);
-//   4 stages of A 16 KB + B 32 KB + scales 6 KB in shared memory.
-//   warp 0        TMA producer: the scale atoms (512 B each, already in the
-//                 128x4 layout) by cp.async.bulk on a barrier of their own,
-//                 then the A and B boxes by cp.async.bulk.tensor
+//   stages of A 16 KB + B 32 KB + scales 6 KB in shared memory.
+//   warp 0        A/B producer: the A and B boxes by cp.async.bulk.tensor
+//                 (or, when a code row is not a 16-byte multiple, row copies
+//                 into the same swizzled layout by the warp's lanes)
+//   warp 22       scale producer: the stage's scale atoms (512 B each,
+//                 already in the 128x4 layout) by cp.async.bulk on a landing
+//                 barrier of their own, so copy issue is split over two warps
 //   warp 1        allocates TMEM; one lane issues the 4 MMAs 128x256x64 of a
-//                 stage from one asm block (descriptors advanced in place)
+//                 stage from one asm block (descriptors advanced in place) and,
+//                 while they run, tests (without waiting) whether the next
+//                 stage has landed
 //   warps 2..5    scale-factor writers, one per TMEM lane quarter: when a
 //                 stage lands, each lane reads the 16 bytes it owns of every
 //                 128x4 scale atom from shared memory and writes them into
@@ -26,13 +31,12 @@
 //                 which is where the block-scaled MMA reads its scales.
 //   warps 6..21   epilogue: four warps per TMEM lane quarter, 64 accumulator
 //                 columns each; tcgen05.ld, release the accumulator to the
-//                 MMA warp, scale by alpha, round, store.  bf16 output goes
-//                 through a 2 KB 64B-swizzled staging buffer per warp and
-//                 TMA stores of 32 x 32 boxes (a warp's direct stores would
-//                 touch 32 rows per instruction); FP32 output, and rows past
-//                 the end of an expert, are stored directly.
-//   The TMA-store epilogue uses 3 stages (the staging takes the fourth's
-//   space); it is chosen for bf16 outputs of GEMMs with K < 8192.
+//                 MMA warp, scale by alpha, round, store.  Outputs whose rows
+//                 are 16-byte aligned go through a 2 KB 64B-swizzled staging
+//                 buffer per warp and TMA stores of 32-row boxes (32 bf16 or
+//                 16 FP32 columns; a warp's direct stores would touch 32 rows
+//                 per instruction); other outputs, and rows past the end of an
+//                 expert, are stored directly.
 //   TMEM: accumulator columns 0..255; per stage 16 columns of A scales and
 //   32 columns of B scales from column 256.
 //   Moving the scales with tcgen05.st from dedicated warps keeps them off
@@ -40,8 +44,10 @@
 //   cost as much tensor time as half an MMA.
 // CTA pairs (the default; cta_group::2, clusters of two CTAs on two SMs):
 //   tiles of 256 x 256; each CTA holds its 128 A rows and 128 of the 256 B
-//   rows of a stage (38 KB instead of 54 KB per stage, five stages instead
-//   of four), plus its A scales and all 256 rows of B scales in its own TMEM.
+//   rows of a stage (38 KB instead of 54 KB per stage: five stages beside the
+//   32 KB output staging for dense GEMMs, four for grouped ones, whose group
+//   tables take the rest), plus its A scales and all 256 rows of B scales in
+//   its own TMEM.
 //   Rank 0 issues 256 x 256 x 64 MMAs for both; both CTAs' TMA loads complete
 //   on rank 0's full barrier, both CTAs' scale warps and epilogues arrive on
 //   rank 0's barriers, and rank 0's commits arrive on the barriers of both.
