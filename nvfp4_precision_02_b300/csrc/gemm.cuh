@@ -86,7 +86,8 @@ constexpr int G_THREADS = (G_W_SFP + 1) * 32;               // 736
 constexpr int G_TMEM_COLS = 512;
 constexpr int G_SF_COL0 = 256;
 constexpr int G_SF_COLS_PER_STAGE = 48;
-constexpr int G_BAND = 16;                                   // m-tiles per raster band
+constexpr int G_BAND = 16;                                   // m-tiles per raster band (grouped schedules)
+constexpr int G_BAND_DENSE = 32;                             // ... and for one dense GEMM
 constexpr uint64_t G_WAIT_NS = 4000000000ull;                // bounded waits: 4 s
 constexpr int G_BAR_BYTES = 256;                             // barriers, TMEM slot, abort flag
 
@@ -554,16 +555,21 @@ struct TileCoord {
     int32_t ka = -1;  // 64-wide K atoms of the tile; -1: all of K
 };
 
-// Tiles are numbered in bands of G_BAND m-tiles: inside a band, the m-tile
-// runs fastest, so concurrently resident CTAs share B tiles through L2.
+// Tiles are numbered in bands of BAND m-tiles: inside a band, the m-tile
+// runs fastest, so concurrently resident CTAs share B tiles through L2 and
+// every B tile is read from DRAM about once per band.  Measured on the Ultra
+// in_proj GEMMs: bands of 32 m-tiles (4096 rows) took fprop 1.585 -> 1.549 ms
+// against 16 and left dgrad and wgrad unchanged (64 slowed them by 6 %); the
+// grouped down-projection keeps 16 (32 was 0.7 % slower).
+template <int BAND>
 __device__ __forceinline__ TileCoord decode_tile(int64_t t, int mtiles, int ntiles, const int32_t* off,
                                                  const int32_t* pad, int groups) {
-    const int64_t band_tiles = (int64_t)G_BAND * ntiles;
+    const int64_t band_tiles = (int64_t)BAND * ntiles;
     const int band = (int)(t / band_tiles);
     const int64_t local = t - (int64_t)band * band_tiles;
-    const int bsize = min(G_BAND, mtiles - band * G_BAND);
+    const int bsize = min(BAND, mtiles - band * BAND);
     TileCoord c;
-    c.mtg = band * G_BAND + (int)(local % bsize);
+    c.mtg = band * BAND + (int)(local % bsize);
     c.nt = (int)(local / bsize);
     // group: pad[g] <= 128 * mtg < pad[g+1]
     int lo = 0, hi = groups;
@@ -581,14 +587,15 @@ __device__ __forceinline__ TileCoord decode_tile(int64_t t, int mtiles, int ntil
 
 // Tiles of a CTA pair: 256 rows (two 128-row m-tiles of one group, the
 // second possibly past the group's end) x 256 columns, numbered in bands of
-// G_BAND / 2 row pairs like decode_tile.  Returns the m-tile of CTA `rank`.
+// BAND / 2 row pairs like decode_tile.  Returns the m-tile of CTA `rank`.
 // A second m-tile past the group's end has rows = 0 and takes its partner's
 // scale row (mtg), so that its loads stay inside the scale buffer; its
 // results are never stored.
+template <int BAND>
 __device__ __forceinline__ TileCoord decode_pair_tile(int64_t t, int ptiles, int ntiles, const int32_t* off,
                                                       const int32_t* pad, const int32_t* pair, int groups,
                                                       uint32_t rank) {
-    constexpr int PB = G_BAND / 2;
+    constexpr int PB = BAND / 2;
     const int64_t band_tiles = (int64_t)PB * ntiles;
     const int band = (int)(t / band_tiles);
     const int64_t local = t - (int64_t)band * band_tiles;
@@ -732,8 +739,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
     const int64_t t_step = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
     auto tile_at = [&](int64_t t) {
         if (KGROUP) return decode_kgroup_tile(t, kg_mt, ntiles, gt.pad, p.M, p.K, PAIR, rank);
-        return PAIR ? decode_pair_tile(t, ptiles, ntiles, gt.off, gt.pad, gt.pair, groups, rank)
-                    : decode_tile(t, mtiles, ntiles, gt.off, gt.pad, groups);
+        constexpr int BAND = SCHED == G_DENSE ? G_BAND_DENSE : G_BAND;
+        return PAIR ? decode_pair_tile<BAND>(t, ptiles, ntiles, gt.off, gt.pad, gt.pair, groups, rank)
+                    : decode_tile<BAND>(t, mtiles, ntiles, gt.off, gt.pad, groups);
     };
     const int katoms = (int)((p.K + 63) / 64);           // atoms of a whole operand row (scale row stride)
     // K atoms and stages of a tile

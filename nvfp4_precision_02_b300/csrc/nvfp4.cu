@@ -55,6 +55,7 @@ struct DeviceInfo {
     bool gemm_attr = false;
     int pair_clusters = 0;
     bool q2r_attr = false;
+    bool rht_attr = false;
 };
 DeviceInfo g_dev[MAX_DEVICES];
 std::mutex g_dev_mu;
@@ -206,6 +207,39 @@ int amax_blocks(int64_t units) {
 }
 
 }  // namespace
+
+// RHT amax (MODE 0), both amaxes (MODE 3) or RHT + RNE (MODE 1) of a dense
+// operand: the persistent streaming kernel when its rows can be copied in
+// 16-byte pieces, else one CTA per tile.
+template <int MODE>
+static nvfp4_status launch_rht_dense(const void* x, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask,
+                                     float* am, uint8_t* codes, uint8_t* sf, float* copy, nvfp4_stream_t stream) {
+    int sms = 0, dev = 0;
+    NVFP4_TRY(check_device(&sms, &dev));
+    if (ld % 8 == 0 && cols % 8 == 0 && aligned16(x)) {
+        {
+            std::lock_guard<std::mutex> lk(g_dev_mu);
+            if (!g_dev[dev].rht_attr) {
+                NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_rht_stream<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         RHT_STREAM_SMEM), "smem attr"));
+                NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_rht_stream<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         RHT_STREAM_SMEM), "smem attr"));
+                NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_rht_stream<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         RHT_STREAM_SMEM), "smem attr"));
+                g_dev[dev].rht_attr = true;
+            }
+        }
+        const int64_t tiles = cdiv(cols, 256) * cdiv(tokens, 64);
+        const int grid = (int)std::min<int64_t>(tiles, (int64_t)sms * 3);
+        k_rht_stream<MODE><<<grid, 256, RHT_STREAM_SMEM, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask, am,
+                                                                 codes, sf, copy);
+        return launched("k_rht_stream");
+    }
+    k_rht<MODE><<<dim3((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64)), 256, 0, stream>>>(
+        (const uint16_t*)x, tokens, cols, ld, sign_mask, am, 0, codes, sf, copy);
+    return launched("k_rht");
+}
+
 
 extern "C" {
 
@@ -523,9 +557,7 @@ nvfp4_status nvfp4_rht_amax(const void* x, int64_t tokens, int64_t cols, int64_t
     NVFP4_TRY(check_device());
     NVFP4_TRY(cuda_call(cudaMemsetAsync(amax, 0, sizeof(float), stream), "memset amax"));
     if (tokens == 0 || cols == 0) return NVFP4_OK;
-    k_rht<0><<<dim3((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64)), 256, 0, stream>>>(
-        (const uint16_t*)x, tokens, cols, ld, sign_mask, amax, 0, nullptr, nullptr, nullptr);
-    return launched("k_rht amax");
+    return launch_rht_dense<0>(x, tokens, cols, ld, sign_mask, amax, nullptr, nullptr, nullptr, stream);
 }
 
 nvfp4_status nvfp4_dual_amax(const void* x, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask,
@@ -539,9 +571,7 @@ nvfp4_status nvfp4_dual_amax(const void* x, int64_t tokens, int64_t cols, int64_
     NVFP4_TRY(cuda_call(cudaMemsetAsync(amax_plain, 0, sizeof(float), stream), "memset amax"));
     NVFP4_TRY(cuda_call(cudaMemsetAsync(amax_rht, 0, sizeof(float), stream), "memset amax"));
     if (tokens == 0 || cols == 0) return NVFP4_OK;
-    k_rht<3><<<dim3((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64)), 256, 0, stream>>>(
-        (const uint16_t*)x, tokens, cols, ld, sign_mask, amax_rht, 0, nullptr, nullptr, amax_plain);
-    return launched("k_rht dual amax");
+    return launch_rht_dense<3>(x, tokens, cols, ld, sign_mask, amax_rht, nullptr, nullptr, amax_plain, stream);
 }
 
 nvfp4_status nvfp4_dual_sr_quantize(const void* dy, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask,
@@ -617,11 +647,8 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t tokens, int64_t cols, int
     float* copy = nullptr;
     if (am == nullptr) {
         NVFP4_TRY(cuda_call(cudaMemsetAsync(out_t->amax, 0, sizeof(float), stream), "memset amax"));
-        if (tokens > 0 && cols > 0) {
-            k_rht<0><<<dim3((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64)), 256, 0, stream>>>(
-                (const uint16_t*)x, tokens, cols, ld, sign_mask, out_t->amax, 0, nullptr, nullptr, nullptr);
-            NVFP4_TRY(launched("k_rht amax"));
-        }
+        if (tokens > 0 && cols > 0)
+            NVFP4_TRY(launch_rht_dense<0>(x, tokens, cols, ld, sign_mask, out_t->amax, nullptr, nullptr, nullptr, stream));
         am = out_t->amax;
     } else if (amax_in != out_t->amax) {
         copy = out_t->amax;
@@ -631,13 +658,14 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t tokens, int64_t cols, int
         return NVFP4_OK;
     }
     const dim3 grid((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64));
-    if (mode == NVFP4_ROUND_SR)
+    if (mode == NVFP4_ROUND_SR) {
         k_rht<2><<<grid, 256, 0, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask, const_cast<float*>(am), seed,
                                            (uint8_t*)out_t->codes, out_t->sf, copy);
-    else
-        k_rht<1><<<grid, 256, 0, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask, const_cast<float*>(am), seed,
-                                           (uint8_t*)out_t->codes, out_t->sf, copy);
-    NVFP4_TRY(launched("k_rht quantize"));
+        NVFP4_TRY(launched("k_rht quantize"));
+    } else {
+        NVFP4_TRY(launch_rht_dense<1>(x, tokens, cols, ld, sign_mask, const_cast<float*>(am), (uint8_t*)out_t->codes,
+                                      out_t->sf, copy, stream));
+    }
     if (cols % 128 != 0) {
         k_zero_pad_rows<<<64, 256, 0, stream>>>(out_t->sf, cols, tokens, nullptr, 0);
         NVFP4_TRY(launched("k_zero_pad_rows"));

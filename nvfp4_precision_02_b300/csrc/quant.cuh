@@ -1161,4 +1161,133 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
     }
 }
 
+// Persistent form of k_rht for a dense operand whose rows are 16-byte
+// aligned (ld % 8 == 0, cols % 8 == 0): MODE 0 (amax of the transform), 1
+// (transform + RNE into the transposed operand) and 3 (both amaxes).  CTA b
+// takes tiles b, b + G, ... (tile t: token rows 64 (t / tx) .., channels
+// 256 (t % tx) ..); while a tile is transformed from one shared buffer, the
+// next tile's rows are copied into the other by cp.async (16-byte copies,
+// zero-filled outside the tensor), so a CTA always has a tile in flight.  The
+// per-tile arithmetic is that of k_rht; the amaxes are reduced over all of a
+// CTA's tiles and published once.
+constexpr int RHT_TILE_ELEMS = 64 * (256 + 8);
+constexpr int RHT_STREAM_SMEM = 2 * RHT_TILE_ELEMS * 2;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+template <int MODE>
+__global__ void __launch_bounds__(256, 3) k_rht_stream(const uint16_t* __restrict__ x, int64_t tokens, int64_t cols,
+                                                       int64_t ld, uint32_t sign_mask, float* __restrict__ amax,
+                                                       uint8_t* __restrict__ codes_t, uint8_t* __restrict__ sf_t,
+                                                       float* __restrict__ amax_copy) {
+    static_assert(MODE == 0 || MODE == 1 || MODE == 3, "amax and RNE modes only");
+    extern __shared__ __align__(16) uint16_t rht_buf[];
+    const int tid = threadIdx.x;
+    const int64_t tx = (cols + 255) / 256, total = tx * ((tokens + 63) / 64);
+    // stage tile t into buffer b (every thread: eight 16-byte copies)
+    auto stage = [&](int64_t t, int b) {
+        const int64_t r0 = (t / tx) * 64, c0 = (t % tx) * 256;
+        uint16_t* tile = rht_buf + b * RHT_TILE_ELEMS;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = tid + 256 * k;
+            const int rr = i >> 5, cc = (i & 31) * 8;
+            const bool ok = r0 + rr < tokens && c0 + cc < cols;
+            const uint16_t* src = ok ? x + (r0 + rr) * ld + c0 + cc : x;
+            cp_async16((uint32_t)__cvta_generic_to_shared(tile + rr * (256 + 8) + cc), src, ok ? 16u : 0u);
+        }
+        cp_async_commit();
+    };
+    float s_enc = 1.0f;
+    if (MODE == 1) {
+        s_enc = tensor_encode_scale(amax[0]);
+        if (amax_copy != nullptr && blockIdx.x == 0 && tid == 0) amax_copy[0] = amax[0];
+    }
+    float m = 0.0f, mp = 0.0f;
+    int b = 0;
+    int64_t t = blockIdx.x;
+    if (t < total) stage(t, 0);
+    for (; t < total; t += gridDim.x, b ^= 1) {
+        const int64_t tn = t + gridDim.x;
+        if (tn < total) stage(tn, b ^ 1);
+        else cp_async_commit();                       // keep one group per iteration
+        cp_async_wait1();
+        __syncthreads();
+        const uint16_t(*tile)[256 + 8] = reinterpret_cast<const uint16_t(*)[256 + 8]>(rht_buf + b * RHT_TILE_ELEMS);
+        const int64_t t0 = (t / tx) * 64, c = (t % tx) * 256 + tid;
+        const int64_t left16 = (tokens - t0) >> 4;
+        const int nchunks = left16 < 4 ? (int)left16 : 4;
+        if (c < cols) {
+            if (MODE == 0 || MODE == 3) {
+                for (int j = 0; j < nchunks; ++j) {
+                    float v[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[16 * j + i][tid] << 16);
+                    if (MODE == 3) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) mp = fmaxf(mp, fabsf(v[i]));
+                    }
+                    rht16(v, sign_mask);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+                }
+            } else {
+                uint32_t packed[4][2];
+                uint32_t sfw = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    packed[j][0] = packed[j][1] = 0u;
+                    if (j >= nchunks) continue;
+                    float v[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[16 * j + i][tid] << 16);
+                    rht16(v, sign_mask);
+                    float bamax = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(v[i]));
+                    const uint32_t sc = block_scale(bamax, s_enc);
+                    sfw |= sc << (8 * j);
+                    if (sc == 0) continue;
+                    const float ratio = element_ratio(s_enc, sc);
+                    float f[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(v[i], ratio);
+                    const float lo[8] = {f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]};
+                    const float hi[8] = {f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]};
+                    packed[j][0] = e2m1x8_rne(lo);
+                    packed[j][1] = e2m1x8_rne(hi);
+                }
+                uint8_t* crow = codes_t + c * (tokens >> 1) + (t0 >> 1);
+                const int64_t sfc = t0 >> 4;
+                if (nchunks == 4) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
+                    *reinterpret_cast<uint32_t*>(sf_t + sf_offset(c, sfc, tokens)) = sfw;
+                } else {
+                    for (int j = 0; j < nchunks; ++j) {
+                        reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
+                        sf_t[sf_offset(c, sfc + j, tokens)] = (uint8_t)(sfw >> (8 * j));
+                    }
+                    for (int j = nchunks; j < 4; ++j) {
+                        const int64_t cc = sfc + j;       // scale-column padding of the last atom column
+                        if (cc < ((((tokens >> 4) + 3) >> 2) << 2)) sf_t[sf_offset(c, cc, tokens)] = 0;
+                    }
+                }
+            }
+        }
+        __syncthreads();                              // buffer b is refilled two iterations on
+    }
+    if (MODE == 0 || MODE == 3) {
+        block_max_atomic(__float_as_uint(m), amax);
+        if (MODE == 3) {
+            __syncthreads();                          // the reduction buffer is shared by both calls
+            block_max_atomic(__float_as_uint(mp), amax_copy);
+        }
+    }
+}
+
 }  // namespace nvfp4

@@ -112,9 +112,14 @@ def test_quantize_2d(B, orc, batch, rows, cols):
     assert (np_u8(qw.amax) == ref["amax"]).all()
 
 
-@pytest.mark.parametrize("tokens,cols", [(16, 1), (64, 24), (80, 130), (1024, 300), (48, 8)])
+@pytest.mark.parametrize("tokens,cols", [(16, 1), (64, 24), (80, 130), (1024, 300), (48, 8), (1040, 520),
+                                         (8192, 1536)])
 @pytest.mark.parametrize("mode", [0, 1])
 def test_rht_quantize(B, orc, tokens, cols, mode):
+    """RHT + quantise and the RHT amax equal the oracle's; rows of 16-byte
+    multiples (cols % 8 == 0) take the persistent streaming kernel (a last
+    tile of 16 tokens and 8 channels at 1040 x 520; several tiles per CTA at
+    8192 x 1536), others one CTA per tile."""
     x = _x(tokens, cols, seed=tokens * 3 + cols, spread=4.0)
     mask = 0xB5A3 ^ tokens
     q = B.rht_quantize(x.cuda(), mask, mode=mode, seed=1234567)
@@ -288,7 +293,7 @@ def test_quantize_1d_mse(B, orc, rows, cols):
     assert B.device_status() == 0
 
 
-@pytest.mark.parametrize("tokens,cols", [(16, 1), (80, 130), (1024, 300)])
+@pytest.mark.parametrize("tokens,cols", [(16, 1), (80, 130), (1024, 300), (1040, 520), (8192, 1536)])
 def test_dual_amax_and_zero_code_count(B, orc, tokens, cols):
     """One read gives both tensor amaxes of a gradient (plain and after the
     RHT), each equal to the oracle's; the zero-code count of the SR-quantised
