@@ -17,7 +17,7 @@ the input):
   quant1d_rne       k_quant1d<RNE>: X [T, K]
   quant1d_sr        k_quant1d<SR>: dY [T, N]
   quant2d           k_quant2d: W with W^T
-  quant2d_moe       k_quant2d: the batched expert up-projection weights
+  quant2d_moe       k_quant2d_w: the batched expert up-projection weights (W only)
   quant2d_moe_fused k_quant2d_resident: the same weights with their per-expert amax in one launch
   dual_amax         k_rht<3>: max |dY| and max |RHT(dY)| in one read
   rht_sr            k_rht<2>: RHT(dY)^T with SR
