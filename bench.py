@@ -108,19 +108,27 @@ def profiled_traffic(summary: str):
 QUANT_SOURCES = ("nvfp4_precision_02_b300/csrc/quant.cuh", "nvfp4_precision_02_b300/csrc/common.cuh")
 
 
-def profiled_quant_traffic(summary: str, kernel: str):
-    """DRAM bytes per launch of a quantiser from a committed ncu summary
-    (`dram_bytes_per_launch: N`, `kernel_code_sha256: H` over the quantiser
-    sources), or None when missing or stale."""
+def profiled_quant_field(summary: str, field: str):
+    """A number recorded as `<field>: X` in a committed quantiser ncu summary
+    (whose `kernel_code_sha256: H` is the hash of the quantiser sources'
+    code), or None when the summary or the field is missing or the code
+    changed after the capture."""
     path = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    b = re.search(r"dram_bytes_per_launch:\s*(\d+)", text)
+    b = re.search(re.escape(field) + r":\s*([0-9.]+)", text)
     h = re.search(r"kernel_code_sha256:\s*([0-9a-f]{64})", text)
     if not b or not h or h.group(1) != source_hash(QUANT_SOURCES):
         return None
-    return int(b.group(1))
+    return float(b.group(1))
+
+
+def profiled_quant_traffic(summary: str, kernel: str):
+    """DRAM bytes per launch of a quantiser from a committed ncu summary
+    (`dram_bytes_per_launch: N`), or None when missing or stale."""
+    v = profiled_quant_field(summary, "dram_bytes_per_launch")
+    return None if v is None else int(v)
 
 
 def max_over_ranks(value: float, world: int, device) -> float:
@@ -263,15 +271,19 @@ def gemm_roofline(flops: float, nbytes, ms: float, hbm_gbs: float, fp4_tflops: f
             "frac_roofline": round(t / ms, 4)}
 
 
-# integer-ALU operations per element of the SR quantisers, counted from the
-# source: about 18 for the rounding decision, 2.5 for Philox's three-input
-# XORs (its multiplies run on the FMA pipe) and 3 to unpack and pack
-SR_ALU_OPS_PER_ELEMENT = 24
+# integer-ALU operations per element of one SR encoding, estimated from the
+# source: about 10 for the rounding decision with its sign and packing, 2.5
+# for Philox's three-input XORs (its multiplies run on the FMA pipe) and 3.5
+# to unpack, find the block maximum and count zeros.  The ncu summaries of the
+# SR kernels carry the counted figure (alu_ops_per_element), which the bench
+# line reports beside this estimate while the kernel code is unchanged.
+SR_ALU_OPS_PER_ELEMENT = 16
 ALU_LANES_PER_SM = 64          # integer/logic lanes per SM per clock (4 partitions x 16)
 
 
-def alu_roofline(elements: int, ms: float, sm_mhz, sms: int, ops_per_element: int = SR_ALU_OPS_PER_ELEMENT):
-    """ALU roof of an integer-bound kernel from a source-level operation count:
+def alu_roofline(elements: int, ms: float, sm_mhz, sms: int, ops_per_element: float = SR_ALU_OPS_PER_ELEMENT,
+                 note: str = "operation count estimated from the source"):
+    """ALU roof of an integer-bound kernel from an operation count per element:
     elements x ops / (lanes per SM x SMs x SM clock), against the measured time."""
     if not sm_mhz or ms <= 0 or sms <= 0:
         return None
@@ -280,7 +292,7 @@ def alu_roofline(elements: int, ms: float, sm_mhz, sms: int, ops_per_element: in
     return {"bound": "alu", "unit": "Gop/s", "achieved": round(achieved / 1e9, 1), "peak": round(peak / 1e9, 1),
             "frac": round(achieved / peak, 4), "ops_per_element": ops_per_element,
             "floor_ms": round(elements * ops_per_element / peak * 1e3, 4),
-            "note": "operation count estimated from the source, clock = median SM clock of the timed region"}
+            "note": note + ", clock = median SM clock of the timed region"}
 
 
 # ---------------------------------------------------------------- clocks
@@ -662,6 +674,11 @@ def main(argv=None):
                   "traffic": profiled_quant_traffic(f"k_rht_dual_sr_{args.workload}.md", "k_rht"),
                   "alu_estimate": alu_roofline(wk.dense.tokens * wk.dense.out, q_dy, sm_mhz, sms,
                                                2 * SR_ALU_OPS_PER_ELEMENT)}
+    alu_counted = profiled_quant_field(f"k_rht_dual_sr_{args.workload}.md", "alu_ops_per_element")
+    if alu_counted is not None:
+        roofline_q["alu_counted"] = alu_roofline(
+            wk.dense.tokens * wk.dense.out, q_dy, sm_mhz, sms, alu_counted,
+            note="ALU-pipe operations per element counted by ncu (smsp__inst_executed_pipe_alu.sum x 32 / elements)")
 
     supplied = measure_supplied_amax(wk, pk)
     zeros = int(wk.dy_zeros.item())

@@ -103,28 +103,27 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float (&f)[8]) {
 // E2M1 code of v with stochastic rounding by the 32-bit word u.  With grid
 // neighbours lo <= |v| < hi and p = (|v| - lo) / (hi - lo), the magnitude
 // rounds up iff (u >> 8) < p * 2^24, i.e. iff u < 256 * ceil(p * 2^24).
-// Branch-free integer form on the FP32 bits mb of |v|:
-//   |v| >= 0.5: the grid step is bit k of mb (k = 22 on [1, 6), the mantissa
-//               bit; k = 23 on [0.5, 1), the exponent); adding (~u >> (32-k))
-//               to the k bits below it carries into bit k exactly when
-//               (u >> (32-k)) < those bits, and (mb + (~u >> (32-k))) >> k,
-//               minus 252 (k = 22) or 125 (k = 23), is the code; codes past
-//               7 (|v| >= 6, including rounding 6 <= |v| < 8 upwards) clamp
-//               to 7;
-//   |v| < 0.5:  up iff u < 256 * ceil(|v| * 2^25) (|v| * 2^25 < 2^24 is
-//               exact in FP32 and converted with rounding up).
-// It equals the FP32 statement above at both sides of every threshold for
-// every FP32 bit pattern (checked exhaustively on the host); the decision is
-// monotone in u, so that covers all words.
+// Integer form: X holds m = min(|v|, 6) in code steps with 24 fraction bits
+// (X >> 24 = the code rounded down, X mod 2^24 = ceil(p * 2^24)), so adding
+// 2^24 - 1 - (u >> 8) carries into bit 24 exactly when the word rounds up:
+//   m < 1:  the steps are 0.5 wide, X = ceil(m * 2^25) (the product is exact
+//           in FP32; the conversion rounds up);
+//   m >= 1: the grid is the FP32 grid with one mantissa bit, and X is four
+//           times the FP32 bits of m minus those of 0.5 (exponent and top
+//           mantissa bit give the code; the 22 lower mantissa bits, times 4,
+//           are p * 2^24 exactly).
+// Clamping at 6 gives every |v| >= 6 code 7 (rounding 6 <= |v| < 8 upwards
+// included); fminf maps NaN to 6 as well.  It equals the FP32 statement above
+// at both sides of every threshold for every finite FP32 input (checked
+// exhaustively on the host); the decision is monotone in u, so that covers
+// all words.
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u) {
-    const uint32_t bits = __float_as_uint(v);
-    const uint32_t mb = bits & 0x7FFFFFFFu;
-    const bool ge1 = mb >= 0x3F800000u;
-    const uint32_t k = ge1 ? 22u : 23u;
-    const uint32_t c_up = min(((mb + (~u >> (32u - k))) >> k) - (ge1 ? 252u : 125u), 7u);
-    const uint32_t x = __float2uint_ru(fabsf(v) * 33554432.0f);    // ceil(|v| * 2^25)
-    const uint32_t c = mb >= 0x3F000000u ? c_up : (u < (x << 8) ? 1u : 0u);
-    return ((bits >> 28) & 8u) | c;
+    const float m = fminf(fabsf(v), 6.0f);
+    const uint32_t mb = __float_as_uint(m);
+    const uint32_t x = mb >= 0x3F800000u ? mb * 4u + 0x04000000u            // 4 (mb - bits(0.5)) mod 2^32
+                                         : __float2uint_ru(m * 33554432.0f);
+    const uint32_t c = (x + 0x00FFFFFFu - (u >> 8)) >> 24;
+    return ((__float_as_uint(v) >> 28) & 8u) | c;
 }
 
 // Eight E2M1 codes (RNE) of the 8 bf16 values of v (element 2j in the low

@@ -214,35 +214,41 @@ int amax_blocks(int64_t units) {
 
 }  // namespace
 
-// RHT amax (MODE 0), both amaxes (MODE 3) or RHT + RNE (MODE 1) of a dense
-// operand: the persistent streaming kernel when its rows can be copied in
-// 16-byte pieces, else one CTA per tile.
+// One mode of the RHT kernel over a dense operand (amax 0, RNE 1, SR 2, both
+// amaxes 3, dual SR encoder 4): for modes 0, 1 and 3 the persistent streaming
+// kernel when the rows can be copied in 16-byte pieces, else one CTA per tile.
 template <int MODE>
 static nvfp4_status launch_rht_dense(const void* x, int64_t tokens, int64_t cols, int64_t ld, uint16_t sign_mask,
-                                     float* am, uint8_t* codes, uint8_t* sf, float* copy, nvfp4_stream_t stream) {
+                                     float* am, uint8_t* codes, uint8_t* sf, float* copy, nvfp4_stream_t stream,
+                                     uint64_t seed = 0, const RowSR& rsr = RowSR{}) {
     int sms = 0, dev = 0;
     NVFP4_TRY(check_device(&sms, &dev));
-    if (ld % 8 == 0 && cols % 8 == 0 && aligned16(x)) {
-        {
-            std::lock_guard<std::mutex> lk(g_dev_mu);
-            if (!g_dev[dev].rht_attr) {
-                NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_rht_stream<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         RHT_STREAM_SMEM), "smem attr"));
-                NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_rht_stream<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         RHT_STREAM_SMEM), "smem attr"));
-                NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_rht_stream<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         RHT_STREAM_SMEM), "smem attr"));
-                g_dev[dev].rht_attr = true;
+    if constexpr (MODE == 0 || MODE == 1 || MODE == 3) {
+        if (ld % 8 == 0 && cols % 8 == 0 && aligned16(x)) {
+            {
+                std::lock_guard<std::mutex> lk(g_dev_mu);
+                if (!g_dev[dev].rht_attr) {
+                    NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_rht_stream<0>,
+                                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                             RHT_STREAM_SMEM), "smem attr"));
+                    NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_rht_stream<1>,
+                                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                             RHT_STREAM_SMEM), "smem attr"));
+                    NVFP4_TRY(cuda_call(cudaFuncSetAttribute(k_rht_stream<3>,
+                                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                             RHT_STREAM_SMEM), "smem attr"));
+                    g_dev[dev].rht_attr = true;
+                }
             }
+            const int64_t tiles = cdiv(cols, 256) * cdiv(tokens, 64);
+            const int grid = (int)std::min<int64_t>(tiles, (int64_t)sms * 3);
+            k_rht_stream<MODE><<<grid, 256, RHT_STREAM_SMEM, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask,
+                                                                     am, codes, sf, copy);
+            return launched("k_rht_stream");
         }
-        const int64_t tiles = cdiv(cols, 256) * cdiv(tokens, 64);
-        const int grid = (int)std::min<int64_t>(tiles, (int64_t)sms * 3);
-        k_rht_stream<MODE><<<grid, 256, RHT_STREAM_SMEM, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask, am,
-                                                                 codes, sf, copy);
-        return launched("k_rht_stream");
     }
     k_rht<MODE><<<dim3((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64)), 256, 0, stream>>>(
-        (const uint16_t*)x, tokens, cols, ld, sign_mask, am, 0, codes, sf, copy);
+        (const uint16_t*)x, tokens, cols, ld, sign_mask, am, seed, codes, sf, copy, nullptr, 1, 0, rsr);
     return launched("k_rht");
 }
 
@@ -612,10 +618,8 @@ nvfp4_status nvfp4_dual_sr_quantize(const void* dy, int64_t tokens, int64_t cols
     rsr.zero_count = reinterpret_cast<unsigned long long*>(zero_count);
     rsr.amax_row_copy = amax_row != out_row->amax ? out_row->amax : nullptr;
     float* copy_t = amax_rht != out_t->amax ? out_t->amax : nullptr;
-    const dim3 grid((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64));
-    k_rht<4><<<grid, 256, 0, stream>>>((const uint16_t*)dy, tokens, cols, ld, sign_mask, const_cast<float*>(amax_rht),
-                                       seed_rht, (uint8_t*)out_t->codes, out_t->sf, copy_t, nullptr, 1, 0, rsr);
-    NVFP4_TRY(launched("k_rht dual SR"));
+    NVFP4_TRY(launch_rht_dense<4>(dy, tokens, cols, ld, sign_mask, const_cast<float*>(amax_rht),
+                                  (uint8_t*)out_t->codes, out_t->sf, copy_t, stream, seed_rht, rsr));
     // scale padding rows of both operands (rows past tokens, or past cols)
     if (tokens % 128 != 0) {
         k_zero_pad_rows<<<64, 256, 0, stream>>>(out_row->sf, tokens, cols, nullptr, 0);
@@ -669,11 +673,9 @@ nvfp4_status nvfp4_rht_quantize(const void* x, int64_t tokens, int64_t cols, int
         if (copy) NVFP4_TRY(cuda_call(cudaMemcpyAsync(copy, amax_in, 4, cudaMemcpyDeviceToDevice, stream), "amax copy"));
         return NVFP4_OK;
     }
-    const dim3 grid((unsigned)cdiv(cols, 256), (unsigned)cdiv(tokens, 64));
     if (mode == NVFP4_ROUND_SR) {
-        k_rht<2><<<grid, 256, 0, stream>>>((const uint16_t*)x, tokens, cols, ld, sign_mask, const_cast<float*>(am), seed,
-                                           (uint8_t*)out_t->codes, out_t->sf, copy);
-        NVFP4_TRY(launched("k_rht quantize"));
+        NVFP4_TRY(launch_rht_dense<2>(x, tokens, cols, ld, sign_mask, const_cast<float*>(am), (uint8_t*)out_t->codes,
+                                      out_t->sf, copy, stream, seed));
     } else {
         NVFP4_TRY(launch_rht_dense<1>(x, tokens, cols, ld, sign_mask, const_cast<float*>(am), (uint8_t*)out_t->codes,
                                       out_t->sf, copy, stream));

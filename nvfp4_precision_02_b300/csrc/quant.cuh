@@ -917,13 +917,36 @@ __global__ void __launch_bounds__(256) k_quant2d_pad(uint8_t* __restrict__ sf, u
 
 // ------------------------------------------------------------------ RHT
 // y = 0.25 * H16 * (s .* x) on one 16-token chunk, FP32 butterfly with
-// strides 1, 2, 4, 8 (Sylvester order).
+// strides 1, 2, 4, 8 (Sylvester order).  FOLD puts the signs into the first
+// stage: s_i x_i is an exact multiply by +-1 and s_j x_j + (s_i x_i) one fused
+// multiply-add by +-1, which rounds once like the plain add or subtract, so
+// both forms give the same bits.  Measured on Ultra dY, the folded form makes
+// the amax and RNE passes up to 9 % faster and the SR encoders 1 % slower, so
+// those keep the separate sign flips.
+template <bool FOLD>
 __device__ __forceinline__ void rht16(float (&x)[16], uint32_t sign_mask) {
+    if (FOLD) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        if ((sign_mask >> i) & 1u) x[i] = -x[i];
+        for (int i = 0; i < 16; i += 2) {
+            const float si = ((sign_mask >> i) & 1u) ? -1.0f : 1.0f;
+            const float sj = ((sign_mask >> (i + 1)) & 1u) ? -1.0f : 1.0f;
+            const float a = __fmul_rn(x[i], si), c = x[i + 1];
+            x[i] = __fmaf_rn(sj, c, a);
+            x[i + 1] = __fmaf_rn(-sj, c, a);
+        }
+    } else {
 #pragma unroll
-    for (int h = 1; h < 16; h <<= 1)
+        for (int i = 0; i < 16; ++i)
+            if ((sign_mask >> i) & 1u) x[i] = -x[i];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const float a = x[i], c = x[i + 1];
+            x[i] = __fadd_rn(a, c);
+            x[i + 1] = __fsub_rn(a, c);
+        }
+    }
+#pragma unroll
+    for (int h = 2; h < 16; h <<= 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
             if ((i & h) == 0) {
@@ -963,6 +986,118 @@ struct RowSR {
     unsigned long long* zero_count = nullptr;
     float* amax_row_copy = nullptr;     // receives amax_row[0] (nullable)
 };
+
+using RhtTile = uint16_t[256 + 8];
+
+// Row operand of the dual encoder from a staged 64 x 256 tile (token rows t0
+// .., channels c0 ..; ntok valid rows): thread tid encodes blocks
+// 4 (tid & 3) .. + 3 (64 channels) of token row tid >> 2 with the row SR words
+// and stores its codes and scale word.  Returns its zero-magnitude codes.
+__device__ __forceinline__ uint32_t rht_rows_sr(const RhtTile* tile, int tid, int64_t t0, int64_t c0, int ntok,
+                                                int64_t cols, const RowSR& rsr, float s_row,
+                                                const PhiloxKeys& key_r) {
+    const int r = tid >> 2, part = tid & 3;
+    const int64_t t = t0 + r;
+    uint32_t zeros = 0, word = 0;
+    const bool row_ok = r < ntok;
+    uint32_t cw[8];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int64_t c = c0 + 64 * part + 16 * b;
+        cw[2 * b] = cw[2 * b + 1] = 0u;
+        if (!row_ok || c >= cols) continue;
+        const uint4 va = *reinterpret_cast<const uint4*>(&tile[r][64 * part + 16 * b]);
+        const uint4 vb = *reinterpret_cast<const uint4*>(&tile[r][64 * part + 16 * b + 8]);
+        const uint32_t m = bf16x16_absmax(va, vb);
+        const uint32_t sc = block_scale(__uint_as_float(m << 16), s_row);
+        word |= sc << (8 * b);
+        if (sc != 0) {
+            const float ratio = element_ratio(s_row, sc);
+            const uint64_t e0 = (uint64_t)t * (uint64_t)cols + (uint64_t)c;
+            cw[2 * b] = encode8<true>(va, ratio, false, key_r, e0);
+            cw[2 * b + 1] = encode8<true>(vb, ratio, false, key_r, e0 + 8);
+        }
+        zeros += zero_nibbles(cw[2 * b]) + zero_nibbles(cw[2 * b + 1]);
+    }
+    const int64_t cp = c0 + 64 * part;
+    if (row_ok && cp < cols) {
+        // a code row is cols/2 bytes, a multiple of 8 only: 8-byte stores
+        uint8_t* dst = rsr.codes_r + t * (cols >> 1) + (cp >> 1);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            if (cp + 16 * b < cols) reinterpret_cast<uint2*>(dst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
+        // four scale columns from a multiple of 4: one word (zeros past cols
+        // are the scale padding of the last atom column)
+        *reinterpret_cast<uint32_t*>(rsr.sf_r + sf_offset(t, cp >> 4, cols)) = word;
+    }
+    return zeros;
+}
+
+// Transposed RHT operand from a staged tile: thread tid owns channel c (the
+// tile's column tid) and the tile's nchunks 16-token chunks starting at token
+// t0 of the [*, ocols] output; each chunk is transformed, block-scaled and
+// encoded (SR words of element c * ocols + token, or RNE), then the codes and
+// scale bytes are stored.
+template <bool SR, bool FOLD>
+__device__ __forceinline__ void rht_cols_encode(const RhtTile* tile, int tid, int64_t c, int64_t t0, int nchunks,
+                                                int64_t ocols, uint32_t sign_mask, float s_enc,
+                                                const PhiloxKeys& key, uint8_t* __restrict__ codes_t,
+                                                uint8_t* __restrict__ sf_t) {
+    uint32_t packed[4][2];
+    uint32_t sfw = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        packed[j][0] = packed[j][1] = 0u;
+        if (j >= nchunks) continue;
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[16 * j + i][tid] << 16);
+        rht16<FOLD>(v, sign_mask);
+        float bamax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(v[i]));
+        const uint32_t sc = block_scale(bamax, s_enc);
+        sfw |= sc << (8 * j);
+        if (sc == 0) continue;
+        const float ratio = element_ratio(s_enc, sc);
+        float f[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(v[i], ratio);
+        if (SR) {
+            const uint64_t e0 = (uint64_t)c * (uint64_t)ocols + (uint64_t)(t0 + 16 * j);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 wd = sr_words(key, (e0 >> 2) + q);
+                const uint32_t ws[4] = {wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) packed[j][q >> 1] |= e2m1_sr(f[4 * q + i], ws[i]) << (4 * (4 * (q & 1) + i));
+            }
+        } else {
+            const float lo[8] = {f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]};
+            const float hi[8] = {f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]};
+            packed[j][0] = e2m1x8_rne(lo);
+            packed[j][1] = e2m1x8_rne(hi);
+        }
+    }
+    uint8_t* crow = codes_t + c * (ocols >> 1) + (t0 >> 1);
+    const int64_t sfc = t0 >> 4;
+    // a code row is ocols/2 bytes (a multiple of 8), so 8-byte stores are aligned
+    if (nchunks == 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
+        *reinterpret_cast<uint32_t*>(sf_t + sf_offset(c, sfc, ocols)) = sfw;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j < nchunks) {
+                reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
+                sf_t[sf_offset(c, sfc + j, ocols)] = (uint8_t)(sfw >> (8 * j));
+            } else if (sfc + j < ((((ocols >> 4) + 3) >> 2) << 2)) {
+                sf_t[sf_offset(c, sfc + j, ocols)] = 0;   // scale-column padding of the last atom column
+            }
+        }
+    }
+}
 
 template <int MODE, bool GROUPED = false>
 __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int64_t tokens,
@@ -1044,7 +1179,7 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
 #pragma unroll
                     for (int i = 0; i < 16; ++i) mp = fmaxf(mp, fabsf(v[i]));
                 }
-                rht16(v, sign_mask);
+                rht16<MODE != 2 && MODE != 4>(v, sign_mask);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
             }
@@ -1057,44 +1192,9 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
         return;
     }
     if (MODE == 4) {
-        // row operand: thread t encodes blocks 4 (t & 3) .. + 3 (64 channels) of
-        // token row t >> 2 of the tile
-        const int r = tid >> 2, part = tid & 3;
         const float s_row = tensor_encode_scale(rsr.amax_row[0]);
         const PhiloxKeys key_r = philox_keys(rsr.seed_row);
-        const int64_t t = t0 + r;
-        uint32_t zeros = 0, word = 0;
-        const bool row_ok = r < ntok;
-        uint32_t cw[8];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int64_t c = c0 + 64 * part + 16 * b;
-            cw[2 * b] = cw[2 * b + 1] = 0u;
-            if (!row_ok || c >= cols) continue;
-            const uint4 va = *reinterpret_cast<const uint4*>(&tile[r][64 * part + 16 * b]);
-            const uint4 vb = *reinterpret_cast<const uint4*>(&tile[r][64 * part + 16 * b + 8]);
-            const uint32_t m = bf16x16_absmax(va, vb);
-            const uint32_t sc = block_scale(__uint_as_float(m << 16), s_row);
-            word |= sc << (8 * b);
-            if (sc != 0) {
-                const float ratio = element_ratio(s_row, sc);
-                const uint64_t e0 = (uint64_t)t * (uint64_t)cols + (uint64_t)c;
-                cw[2 * b] = encode8<true>(va, ratio, false, key_r, e0);
-                cw[2 * b + 1] = encode8<true>(vb, ratio, false, key_r, e0 + 8);
-            }
-            zeros += zero_nibbles(cw[2 * b]) + zero_nibbles(cw[2 * b + 1]);
-        }
-        const int64_t cp = c0 + 64 * part;
-        if (row_ok && cp < cols) {
-            // a code row is cols/2 bytes, a multiple of 8 only: 8-byte stores
-            uint8_t* dst = rsr.codes_r + t * (cols >> 1) + (cp >> 1);
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-                if (cp + 16 * b < cols) reinterpret_cast<uint2*>(dst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
-            // four scale columns from a multiple of 4: one word (zeros past cols
-            // are the scale padding of the last atom column)
-            *reinterpret_cast<uint32_t*>(rsr.sf_r + sf_offset(t, cp >> 4, cols)) = word;
-        }
+        uint32_t zeros = rht_rows_sr(tile, tid, t0, c0, ntok, cols, rsr, s_row, key_r);
         if (rsr.zero_count != nullptr) {
             zeros = __reduce_add_sync(0xFFFFFFFFu, zeros);
             if ((tid & 31) == 0 && zeros != 0) atomicAdd(rsr.zero_count, (unsigned long long)zeros);
@@ -1105,60 +1205,8 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
     if (!active) return;
     const float s_enc = tensor_encode_scale(amax[g]);
     const PhiloxKeys key = philox_keys(seed);
-    uint32_t packed[4][2];
-    uint32_t sfw = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        packed[j][0] = packed[j][1] = 0u;
-        if (j >= nchunks) continue;
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[16 * j + i][tid] << 16);
-        rht16(v, sign_mask);
-        float bamax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(v[i]));
-        const uint32_t sc = block_scale(bamax, s_enc);
-        sfw |= sc << (8 * j);
-        if (sc == 0) continue;
-        const float ratio = element_ratio(s_enc, sc);
-        float f[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(v[i], ratio);
-        if (MODE == 2 || MODE == 4) {
-            const uint64_t e0 = (uint64_t)c * (uint64_t)ocols + (uint64_t)(t0 + 16 * j);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 wd = sr_words(key, (e0 >> 2) + q);
-                const uint32_t ws[4] = {wd.x, wd.y, wd.z, wd.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) packed[j][q >> 1] |= e2m1_sr(f[4 * q + i], ws[i]) << (4 * (4 * (q & 1) + i));
-            }
-        } else {
-            const float lo[8] = {f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]};
-            const float hi[8] = {f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]};
-            packed[j][0] = e2m1x8_rne(lo);
-            packed[j][1] = e2m1x8_rne(hi);
-        }
-    }
-    uint8_t* crow = codes_t + c * (ocols >> 1) + (t0 >> 1);
-    const int64_t sfc = t0 >> 4;
-    // a code row is ocols/2 bytes (a multiple of 8), so 8-byte stores are aligned
-    if (nchunks == 4) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
-        *reinterpret_cast<uint32_t*>(sf_t + sf_offset(c, sfc, ocols)) = sfw;
-    } else {
-        for (int j = 0; j < nchunks; ++j) {
-            reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
-            sf_t[sf_offset(c, sfc + j, ocols)] = (uint8_t)(sfw >> (8 * j));
-        }
-        for (int j = nchunks; j < 4; ++j) {
-            // scale-column padding of the last atom column (tokens/16 % 4 != 0)
-            const int64_t cc = sfc + j;
-            if (cc < ((((ocols >> 4) + 3) >> 2) << 2)) sf_t[sf_offset(c, cc, ocols)] = 0;
-        }
-    }
+    rht_cols_encode<MODE == 2 || MODE == 4, MODE != 2 && MODE != 4>(tile, tid, c, t0, nchunks, ocols, sign_mask,
+                                                                    s_enc, key, codes_t, sf_t);
 }
 
 // Persistent form of k_rht for a dense operand whose rows are 16-byte
@@ -1169,7 +1217,9 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
 // next tile's rows are copied into the other by cp.async (16-byte copies,
 // zero-filled outside the tensor), so a CTA always has a tile in flight.  The
 // per-tile arithmetic is that of k_rht; the amaxes are reduced over all of a
-// CTA's tiles and published once.
+// CTA's tiles and published once.  The SR modes stay with k_rht: they are
+// bound by the integer pipe, and this kernel's three CTAs per SM (two tile
+// buffers each) made the Ultra dual encoder 2 % slower than k_rht's four.
 constexpr int RHT_TILE_ELEMS = 64 * (256 + 8);
 constexpr int RHT_STREAM_SMEM = 2 * RHT_TILE_ELEMS * 2;
 
@@ -1207,6 +1257,7 @@ __global__ void __launch_bounds__(256, 3) k_rht_stream(const uint16_t* __restric
         s_enc = tensor_encode_scale(amax[0]);
         if (amax_copy != nullptr && blockIdx.x == 0 && tid == 0) amax_copy[0] = amax[0];
     }
+    const PhiloxKeys no_key{};
     float m = 0.0f, mp = 0.0f;
     int b = 0;
     int64_t t = blockIdx.x;
@@ -1217,7 +1268,7 @@ __global__ void __launch_bounds__(256, 3) k_rht_stream(const uint16_t* __restric
         else cp_async_commit();                       // keep one group per iteration
         cp_async_wait1();
         __syncthreads();
-        const uint16_t(*tile)[256 + 8] = reinterpret_cast<const uint16_t(*)[256 + 8]>(rht_buf + b * RHT_TILE_ELEMS);
+        const RhtTile* tile = reinterpret_cast<const RhtTile*>(rht_buf + b * RHT_TILE_ELEMS);
         const int64_t t0 = (t / tx) * 64, c = (t % tx) * 256 + tid;
         const int64_t left16 = (tokens - t0) >> 4;
         const int nchunks = left16 < 4 ? (int)left16 : 4;
@@ -1231,52 +1282,13 @@ __global__ void __launch_bounds__(256, 3) k_rht_stream(const uint16_t* __restric
 #pragma unroll
                         for (int i = 0; i < 16; ++i) mp = fmaxf(mp, fabsf(v[i]));
                     }
-                    rht16(v, sign_mask);
+                    rht16<true>(v, sign_mask);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
                 }
             } else {
-                uint32_t packed[4][2];
-                uint32_t sfw = 0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    packed[j][0] = packed[j][1] = 0u;
-                    if (j >= nchunks) continue;
-                    float v[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[16 * j + i][tid] << 16);
-                    rht16(v, sign_mask);
-                    float bamax = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(v[i]));
-                    const uint32_t sc = block_scale(bamax, s_enc);
-                    sfw |= sc << (8 * j);
-                    if (sc == 0) continue;
-                    const float ratio = element_ratio(s_enc, sc);
-                    float f[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(v[i], ratio);
-                    const float lo[8] = {f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]};
-                    const float hi[8] = {f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]};
-                    packed[j][0] = e2m1x8_rne(lo);
-                    packed[j][1] = e2m1x8_rne(hi);
-                }
-                uint8_t* crow = codes_t + c * (tokens >> 1) + (t0 >> 1);
-                const int64_t sfc = t0 >> 4;
-                if (nchunks == 4) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
-                    *reinterpret_cast<uint32_t*>(sf_t + sf_offset(c, sfc, tokens)) = sfw;
-                } else {
-                    for (int j = 0; j < nchunks; ++j) {
-                        reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
-                        sf_t[sf_offset(c, sfc + j, tokens)] = (uint8_t)(sfw >> (8 * j));
-                    }
-                    for (int j = nchunks; j < 4; ++j) {
-                        const int64_t cc = sfc + j;       // scale-column padding of the last atom column
-                        if (cc < ((((tokens >> 4) + 3) >> 2) << 2)) sf_t[sf_offset(c, cc, tokens)] = 0;
-                    }
-                }
+                rht_cols_encode<false, true>(tile, tid, c, t0, nchunks, tokens, sign_mask, s_enc, no_key, codes_t,
+                                             sf_t);
             }
         }
         __syncthreads();                              // buffer b is refilled two iterations on

@@ -40,15 +40,15 @@ static uint32_t sr_def(float v, uint32_t u) {
     return ((float)(u >> 8) < p * 16777216.0f) ? k + 1 : k;
 }
 
-/* the kernel's integer form */
+/* the kernel's integer form: m = min(|v|, 6) in code steps with 24
+ * fraction bits (ceil(m * 2^25) below 1, four times the FP32 bits of m minus
+ * those of 0.5 from 1 on), plus 2^24 - 1 - (u >> 8), bits 24 and up */
 static uint32_t sr_short(float v, uint32_t u) {
-    const uint32_t mb = b_of(v) & 0x7FFFFFFFu;
-    const int ge1 = mb >= 0x3F800000u;
-    const uint32_t k = ge1 ? 22u : 23u;
-    uint32_t c_up = ((mb + (~u >> (32u - k))) >> k) - (ge1 ? 252u : 125u);
-    if (c_up > 7u) c_up = 7u;
-    const uint32_t x = (uint32_t)ceilf(fabsf(v) * 33554432.0f);   /* exact product, ceil */
-    return mb >= 0x3F000000u ? c_up : (u < (x << 8) ? 1u : 0u);
+    const float m = fminf(fabsf(v), 6.0f);
+    const uint32_t mb = b_of(m);
+    const uint32_t x = mb >= 0x3F800000u ? mb * 4u + 0x04000000u
+                                         : (uint32_t)ceilf(m * 33554432.0f);   /* exact product, ceil */
+    return (x + 0x00FFFFFFu - (u >> 8)) >> 24;
 }
 
 /* first word that does not round up: 256 * ceil(p * 2^24) (2^32: none) */

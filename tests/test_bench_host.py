@@ -129,10 +129,11 @@ def test_gemm_roofline_and_bytes_table():
 
 
 def test_alu_roofline():
-    # 541 M elements x 24 operations at 64 lanes x 148 SMs x 2032 MHz: a 0.675 ms floor
+    # 541 M elements x ops at 64 lanes x 148 SMs x 2032 MHz
     r = bench.alu_roofline(16384 * 33024, 0.95, 2032.0, 148)
-    assert r["bound"] == "alu" and r["ops_per_element"] == bench.SR_ALU_OPS_PER_ELEMENT
-    assert abs(r["floor_ms"] - 16384 * 33024 * 24 / (64 * 148 * 2032e6) * 1e3) < 1e-4
+    n = bench.SR_ALU_OPS_PER_ELEMENT
+    assert r["bound"] == "alu" and r["ops_per_element"] == n
+    assert abs(r["floor_ms"] - 16384 * 33024 * n / (64 * 148 * 2032e6) * 1e3) < 1e-4
     assert abs(r["frac"] - r["floor_ms"] / 0.95) < 1e-3
     assert bench.alu_roofline(100, 1.0, None, 148) is None
 

@@ -324,11 +324,27 @@ def test_dual_sr_quantize(B, orc, tokens, cols):
     is the number of zero-magnitude codes of the row operand.  Shapes cover
     a partial 64-token tile, a partial 256-channel tile, rows and columns not
     multiples of 128 and a scale-column padding."""
+    _dual_sr_case(B, orc, tokens, cols, 0)
+
+
+@pytest.mark.parametrize("tokens,cols", [(80, 272), (1040, 48)])
+def test_dual_sr_quantize_strided_rows(B, orc, tokens, cols):
+    """The same with rows 8 bytes past a 16-byte multiple apart (ld = cols +
+    4), which the per-tile kernel takes instead of the streaming one."""
+    _dual_sr_case(B, orc, tokens, cols, 4)
+
+
+def _dual_sr_case(B, orc, tokens, cols, pad):
     x = _x(tokens, cols, seed=7 * tokens + cols, scale=1e-3, spread=6.0)
     mask, s_row, s_rht = 0x2D96, 7, 7 ^ 0x9E3779B97F4A7C15
-    a = B.dual_amax(x.cuda(), mask)
+    xd = x.cuda()
+    if pad:
+        wide = torch.zeros(tokens, cols + pad, dtype=torch.bfloat16, device="cuda")
+        wide[:, :cols] = xd
+        xd = wide[:, :cols]
+    a = B.dual_amax(xd, mask)
     zc = torch.full((1,), -1, dtype=torch.int64, device="cuda")
-    qr, qt = B.dual_sr_quantize(x.cuda(), mask, s_row, s_rht, a, zero_count=zc)
+    qr, qt = B.dual_sr_quantize(xd, mask, s_row, s_rht, a, zero_count=zc)
     torch.cuda.synchronize()
     got = np_u8(a)
     ref_r = orc.quantize_1d(x, mode=1, seed=s_row, amax_in=float(got[0]))
