@@ -993,6 +993,8 @@ using RhtTile = uint16_t[256 + 8];
 // .., channels c0 ..; ntok valid rows): thread tid encodes blocks
 // 4 (tid & 3) .. + 3 (64 channels) of token row tid >> 2 with the row SR words
 // and stores its codes and scale word.  Returns its zero-magnitude codes.
+// The block loop stays rolled: the SR encoders are large, and the smaller
+// code made the Ultra dual encoder 7 % faster (fewer instruction-fetch stalls).
 __device__ __forceinline__ uint32_t rht_rows_sr(const RhtTile* tile, int tid, int64_t t0, int64_t c0, int ntok,
                                                 int64_t cols, const RowSR& rsr, float s_row,
                                                 const PhiloxKeys& key_r) {
@@ -1000,36 +1002,31 @@ __device__ __forceinline__ uint32_t rht_rows_sr(const RhtTile* tile, int tid, in
     const int64_t t = t0 + r;
     uint32_t zeros = 0, word = 0;
     const bool row_ok = r < ntok;
-    uint32_t cw[8];
-#pragma unroll
+    const int64_t cp = c0 + 64 * part;
+    // a code row is cols/2 bytes, a multiple of 8 only: 8-byte stores
+    uint8_t* dst = rsr.codes_r + t * (cols >> 1) + (cp >> 1);
+#pragma unroll 1
     for (int b = 0; b < 4; ++b) {
-        const int64_t c = c0 + 64 * part + 16 * b;
-        cw[2 * b] = cw[2 * b + 1] = 0u;
-        if (!row_ok || c >= cols) continue;
+        const int64_t c = cp + 16 * b;
+        if (!row_ok || c >= cols) break;
         const uint4 va = *reinterpret_cast<const uint4*>(&tile[r][64 * part + 16 * b]);
         const uint4 vb = *reinterpret_cast<const uint4*>(&tile[r][64 * part + 16 * b + 8]);
         const uint32_t m = bf16x16_absmax(va, vb);
         const uint32_t sc = block_scale(__uint_as_float(m << 16), s_row);
         word |= sc << (8 * b);
+        uint32_t w0 = 0u, w1 = 0u;
         if (sc != 0) {
             const float ratio = element_ratio(s_row, sc);
             const uint64_t e0 = (uint64_t)t * (uint64_t)cols + (uint64_t)c;
-            cw[2 * b] = encode8<true>(va, ratio, false, key_r, e0);
-            cw[2 * b + 1] = encode8<true>(vb, ratio, false, key_r, e0 + 8);
+            w0 = encode8<true>(va, ratio, false, key_r, e0);
+            w1 = encode8<true>(vb, ratio, false, key_r, e0 + 8);
         }
-        zeros += zero_nibbles(cw[2 * b]) + zero_nibbles(cw[2 * b + 1]);
+        zeros += zero_nibbles(w0) + zero_nibbles(w1);
+        reinterpret_cast<uint2*>(dst)[b] = make_uint2(w0, w1);
     }
-    const int64_t cp = c0 + 64 * part;
-    if (row_ok && cp < cols) {
-        // a code row is cols/2 bytes, a multiple of 8 only: 8-byte stores
-        uint8_t* dst = rsr.codes_r + t * (cols >> 1) + (cp >> 1);
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-            if (cp + 16 * b < cols) reinterpret_cast<uint2*>(dst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
-        // four scale columns from a multiple of 4: one word (zeros past cols
-        // are the scale padding of the last atom column)
-        *reinterpret_cast<uint32_t*>(rsr.sf_r + sf_offset(t, cp >> 4, cols)) = word;
-    }
+    // four scale columns from a multiple of 4: one word (zeros past cols are
+    // the scale padding of the last atom column)
+    if (row_ok && cp < cols) *reinterpret_cast<uint32_t*>(rsr.sf_r + sf_offset(t, cp >> 4, cols)) = word;
     return zeros;
 }
 
@@ -1037,63 +1034,96 @@ __device__ __forceinline__ uint32_t rht_rows_sr(const RhtTile* tile, int tid, in
 // tile's column tid) and the tile's nchunks 16-token chunks starting at token
 // t0 of the [*, ocols] output; each chunk is transformed, block-scaled and
 // encoded (SR words of element c * ocols + token, or RNE), then the codes and
-// scale bytes are stored.
+// scale bytes are stored (a code row is ocols/2 bytes, a multiple of 8, so
+// 8-byte stores are aligned).  The SR chunk loop stays rolled (smaller code:
+// 8-13 % faster SR encoders); the RNE one is unrolled (5 % faster RNE pass).
 template <bool SR, bool FOLD>
 __device__ __forceinline__ void rht_cols_encode(const RhtTile* tile, int tid, int64_t c, int64_t t0, int nchunks,
                                                 int64_t ocols, uint32_t sign_mask, float s_enc,
                                                 const PhiloxKeys& key, uint8_t* __restrict__ codes_t,
                                                 uint8_t* __restrict__ sf_t) {
-    uint32_t packed[4][2];
     uint32_t sfw = 0;
+    const int64_t sfc = t0 >> 4;
+    if constexpr (SR) {
+        uint2* crow = reinterpret_cast<uint2*>(codes_t + c * (ocols >> 1) + (t0 >> 1));
+#pragma unroll 1
+        for (int j = 0; j < nchunks; ++j) {
+            uint32_t p0 = 0u, p1 = 0u;
+            float v[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        packed[j][0] = packed[j][1] = 0u;
-        if (j >= nchunks) continue;
-        float v[16];
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[16 * j + i][tid] << 16);
+            rht16<FOLD>(v, sign_mask);
+            float bamax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[16 * j + i][tid] << 16);
-        rht16<FOLD>(v, sign_mask);
-        float bamax = 0.0f;
+            for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(v[i]));
+            const uint32_t sc = block_scale(bamax, s_enc);
+            sfw |= sc << (8 * j);
+            if (sc != 0) {
+                const float ratio = element_ratio(s_enc, sc);
+                float f[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(v[i]));
-        const uint32_t sc = block_scale(bamax, s_enc);
-        sfw |= sc << (8 * j);
-        if (sc == 0) continue;
-        const float ratio = element_ratio(s_enc, sc);
-        float f[16];
+                for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(v[i], ratio);
+                const uint64_t e0 = (uint64_t)c * (uint64_t)ocols + (uint64_t)(t0 + 16 * j);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(v[i], ratio);
-        if (SR) {
-            const uint64_t e0 = (uint64_t)c * (uint64_t)ocols + (uint64_t)(t0 + 16 * j);
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 wd = sr_words(key, (e0 >> 2) + q);
+                    const uint32_t ws[4] = {wd.x, wd.y, wd.z, wd.w};
+                    uint32_t acc = 0u;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 wd = sr_words(key, (e0 >> 2) + q);
-                const uint32_t ws[4] = {wd.x, wd.y, wd.z, wd.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) packed[j][q >> 1] |= e2m1_sr(f[4 * q + i], ws[i]) << (4 * (4 * (q & 1) + i));
+                    for (int i = 0; i < 4; ++i) acc |= e2m1_sr(f[4 * q + i], ws[i]) << (4 * (4 * (q & 1) + i));
+                    if (q < 2) p0 |= acc; else p1 |= acc;
+                }
             }
+            crow[j] = make_uint2(p0, p1);
+        }
+        if (nchunks == 4) {
+            *reinterpret_cast<uint32_t*>(sf_t + sf_offset(c, sfc, ocols)) = sfw;
         } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (j < nchunks) sf_t[sf_offset(c, sfc + j, ocols)] = (uint8_t)(sfw >> (8 * j));
+                else if (sfc + j < ((((ocols >> 4) + 3) >> 2) << 2)) sf_t[sf_offset(c, sfc + j, ocols)] = 0;
+            }
+        }
+    } else {
+        uint32_t packed[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            packed[j][0] = packed[j][1] = 0u;
+            if (j >= nchunks) continue;
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float((uint32_t)tile[16 * j + i][tid] << 16);
+            rht16<FOLD>(v, sign_mask);
+            float bamax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(v[i]));
+            const uint32_t sc = block_scale(bamax, s_enc);
+            sfw |= sc << (8 * j);
+            if (sc == 0) continue;
+            const float ratio = element_ratio(s_enc, sc);
+            float f[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f[i] = __fmul_rn(v[i], ratio);
             const float lo[8] = {f[0], f[1], f[2], f[3], f[4], f[5], f[6], f[7]};
             const float hi[8] = {f[8], f[9], f[10], f[11], f[12], f[13], f[14], f[15]};
             packed[j][0] = e2m1x8_rne(lo);
             packed[j][1] = e2m1x8_rne(hi);
         }
-    }
-    uint8_t* crow = codes_t + c * (ocols >> 1) + (t0 >> 1);
-    const int64_t sfc = t0 >> 4;
-    // a code row is ocols/2 bytes (a multiple of 8), so 8-byte stores are aligned
-    if (nchunks == 4) {
+        uint2* crow = reinterpret_cast<uint2*>(codes_t + c * (ocols >> 1) + (t0 >> 1));
+        if (nchunks == 4) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
-        *reinterpret_cast<uint32_t*>(sf_t + sf_offset(c, sfc, ocols)) = sfw;
-    } else {
+            for (int j = 0; j < 4; ++j) crow[j] = make_uint2(packed[j][0], packed[j][1]);
+            *reinterpret_cast<uint32_t*>(sf_t + sf_offset(c, sfc, ocols)) = sfw;
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (j < nchunks) {
-                reinterpret_cast<uint2*>(crow)[j] = make_uint2(packed[j][0], packed[j][1]);
-                sf_t[sf_offset(c, sfc + j, ocols)] = (uint8_t)(sfw >> (8 * j));
-            } else if (sfc + j < ((((ocols >> 4) + 3) >> 2) << 2)) {
-                sf_t[sf_offset(c, sfc + j, ocols)] = 0;   // scale-column padding of the last atom column
+            for (int j = 0; j < 4; ++j) {
+                if (j < nchunks) {
+                    crow[j] = make_uint2(packed[j][0], packed[j][1]);
+                    sf_t[sf_offset(c, sfc + j, ocols)] = (uint8_t)(sfw >> (8 * j));
+                } else if (sfc + j < ((((ocols >> 4) + 3) >> 2) << 2)) {
+                    sf_t[sf_offset(c, sfc + j, ocols)] = 0;   // scale-column padding of the last atom column
+                }
             }
         }
     }
