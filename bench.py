@@ -22,8 +22,9 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import re
+import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -531,8 +532,7 @@ def measure_configs(dev, pk: dict, fp4: dict, super_wk=None, steps: int = 5) -> 
                                 "note": "launch-bound: 50 back-to-back calls per op"}
     own = super_wk is None
     wk = Workload("super", dev) if own else super_wk
-    wk.step()
-    torch.cuda.synchronize()
+    steady_ms(wk.step, warm_ms=30.0, timed_ms=0.0, min_iters=1)     # out of the idle state first
     ms = time_ops(wk, steps)
     names = {"c2": "c2_super_in_proj_fprop", "c3": "c3_super_backward", "c4": "c4_super_latent_moe"}
     for key, (i0, i1) in CONFIG_OPS.items():
@@ -737,6 +737,33 @@ def host_mem_available() -> int:
     return 0
 
 
+def steady_ms(fn, warm_ms: float = 30.0, timed_ms: float = 10.0, min_iters: int = 5) -> float:
+    """CUDA-event time per call of fn in steady state.  The calls run back to
+    back for at least warm_ms first, then enough calls to cover timed_ms are
+    timed.  After a pause, the first milliseconds of work run slower even with
+    the SM clock at its maximum: on a B300, the Ultra X quantiser took
+    0.073 ms per call after its inputs were generated and 0.123 ms after 5 s
+    idle, each timed over 5 calls."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    fn()
+    e1.record()
+    torch.cuda.synchronize()
+    est = max(e0.elapsed_time(e1), 1e-3)
+    for _ in range(max(1, math.ceil(warm_ms / est))):
+        fn()
+    n = max(min_iters, math.ceil(timed_ms / est))
+    e0.record()
+    for _ in range(n):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
 def measure_supplied_amax(wk: Workload, pk: dict, iters: int = 5):
     """Each quantiser of the step with its amax supplied (the step's own
     amaxes, already in the output tensors), timed alone after the timed
@@ -769,16 +796,7 @@ def measure_supplied_amax(wk: Workload, pk: dict, iters: int = 5):
     ]
     out = {}
     for name, nbytes, fn in cases:
-        fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(iters):
-            fn()
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / iters
-        out[name] = op_entry("hbm", nbytes, ms, pk, {})
+        out[name] = op_entry("hbm", nbytes, steady_ms(fn, min_iters=iters), pk, {})
     return out
 
 
@@ -815,16 +833,7 @@ def measure_next_rows(wk: Workload, pk: dict, fp4: dict, iters: int = 3):
     ]
     out = {}
     for name, kind, work, fn in cases:
-        fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(iters):
-            fn()
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / iters
-        out[name] = op_entry(kind, work, ms, pk, fp4)
+        out[name] = op_entry(kind, work, steady_ms(fn, min_iters=iters), pk, fp4)
     # PTQ block scales by minimum squared error (next row f3) on the in_proj weight
     qptq = B.empty_qtensor(wk.dense.out, wk.dense.hidden, dev)
     B.quantize_1d_mse(wk.w, amax_in=wk.qw.amax, out=qptq)
@@ -843,15 +852,7 @@ def measure_next_rows(wk: Workload, pk: dict, fp4: dict, iters: int = 3):
     # FP16 SR of an SSM cache (next row f4): 256 sequences x 256 heads x 64 x state 128, FP32 in
     ssm = torch.randn(256 * 256 * 64 * 128, device=dev)
     ssm16 = torch.empty(ssm.numel(), dtype=torch.float16, device=dev)
-    B.sr_fp16(ssm, 5, out=ssm16)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(iters):
-        B.sr_fp16(ssm, 5, out=ssm16)
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / iters
+    ms = steady_ms(lambda: B.sr_fp16(ssm, 5, out=ssm16), min_iters=iters)
     out["sr_fp16 SSM cache (FP32 -> FP16, 6 B / element)"] = op_entry("hbm", 6.0 * ssm.numel(), ms, pk, fp4)
     del ssm, ssm16
     # the wgrad writes E * Hh * L FP32 outputs: its HBM roof
