@@ -29,8 +29,9 @@
  *      amax == 0 -> 1; an infinite quotient clamps to FLT_MAX; dec = 1/S_enc.
  *   R2 block scale   sf = E4M3_RNE_satfinite((bamax / 6) * S_enc), two FP32
  *      ops in that order.
- *   R3 element       sf == 0 -> code +0; else v = x * (S_enc / sf) in FP32 and
- *      v is rounded to E2M1 (RNE, saturating at 6), sign copied from x.
+ *   R3 element       sf == 0 -> code +0; else v = x * (S_enc / sf) in FP32 (an
+ *      infinite quotient clamps to FLT_MAX, as in R1) and v is rounded to
+ *      E2M1 (RNE, saturating at 6), sign copied from x.
  *   R4 SR            Philox4x32 with 5 rounds, key = seed, counter =
  *      (e >> 2, 0, 0), word e & 3, e = row-major index in the quantised
  *      output; round up iff (u >> 8) < p * 2^24.
@@ -210,6 +211,17 @@ uint8_t oracle_block_scale(float bamax, float s_enc)
     return oracle_e4m3_encode(sf);
 }
 
+/* Element multiplier S_enc / e4m3(sf) of a block (R3): one FP32 division;
+ * an infinite quotient clamps to FLT_MAX, as R1's tensor scale does (it
+ * overflows only when S_enc is already near FLT_MAX and sf is a small
+ * subnormal E4M3 value; the clamp keeps 0 * multiplier at 0). */
+static float element_multiplier(float s_enc, float sfv)
+{
+    float r = s_enc / sfv;
+    if (isinf(r)) r = FLT_MAX;
+    return r;
+}
+
 /* Encode one block of n values (n <= 16, all sharing block scale sf).
  * Output: one 4-bit code per byte of codes[].  For SR the element of value
  * j has output index e0 + j * estride. */
@@ -220,7 +232,7 @@ static void encode_block(const float *x, int n, float s_enc, uint8_t sf,
     int j;
     float r;
     if (sf == 0) { for (j = 0; j < n; ++j) codes[j] = 0; return; }
-    r = s_enc / (float)oracle_e4m3_value(sf);
+    r = element_multiplier(s_enc, (float)oracle_e4m3_value(sf));
     for (j = 0; j < n; ++j) {
         float v = x[j] * r;
         if (mode == 0) codes[j] = (uint8_t)oracle_e2m1_rne(v);
@@ -643,7 +655,7 @@ static uint8_t mse_block(const float *x, float s_enc, float dec, uint8_t *codes)
     if (bamax == 0.0f) { for (j = 0; j < 16; ++j) codes[j] = 0; return 0; }
     for (c = 1; c <= 126; ++c) {
         const float sc = (float)oracle_e4m3_value(c);
-        const float r = s_enc / sc;
+        const float r = element_multiplier(s_enc, sc);
         const float step = sc * dec;
         float err = 0.0f;
         for (j = 0; j < 16; ++j) {
@@ -656,7 +668,7 @@ static uint8_t mse_block(const float *x, float s_enc, float dec, uint8_t *codes)
         if (bestc == 0 || err <= best) { best = err; bestc = c; }
     }
     {
-        const float r = s_enc / (float)oracle_e4m3_value(bestc);
+        const float r = element_multiplier(s_enc, (float)oracle_e4m3_value(bestc));
         for (j = 0; j < 16; ++j) codes[j] = (uint8_t)oracle_e2m1_rne(x[j] * r);
     }
     return (uint8_t)bestc;

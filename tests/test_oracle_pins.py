@@ -97,6 +97,23 @@ def test_tensor_scale_special_cases(orc):
     assert orc.decode_scale(2688.0) == 1.0
 
 
+def test_element_multiplier_overflow_clamps(orc):
+    """Reading R3 with R1's clamp, worked by hand.  Tensor amax 1e-37:
+    2688 / amax overflows, so S_enc = FLT_MAX.  Block max 2^-132 (bf16
+    0x0002): (2^-132 / 6) * FLT_MAX = 0.0104, E4M3 code 5 (5 * 2^-9, a
+    subnormal scale).  FLT_MAX / (5 * 2^-9) overflows as well and clamps to
+    FLT_MAX, so 2^-132 * FLT_MAX = 0.0625, +-2^-133 * FLT_MAX = +-0.03125 and
+    +-0 stay +-0: every element rounds to zero, negative ones to code 0x8.
+    Without the clamp the multiplier is inf: 2^-132 would encode as 6 (code
+    7) and the zeros as NaN."""
+    bits = np.zeros((1, 16), dtype=np.uint16)
+    bits[0, :5] = [0x0000, 0x8000, 0x0002, 0x8001, 0x0001]
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    ref = orc.quantize_1d(x, mode=0, amax_in=1e-37)
+    assert ref["sf"][orc.sf_offset(0, 0, 16)] == 0x05
+    assert list(ref["codes"][0]) == [0x80, 0x80] + [0] * 6
+
+
 def test_block_scale_max_maps_to_448(orc):
     # the block holding the tensor amax gets scale 448 (largest E4M3) for any amax
     rng = np.random.default_rng(2)
