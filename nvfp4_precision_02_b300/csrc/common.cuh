@@ -77,9 +77,13 @@ __device__ __forceinline__ uint32_t block_scale(float bamax, float s_enc) {
     return e4m3_from_float(__fmul_rn(div6_rn(bamax), s_enc));
 }
 
-// Per-element multiplier S_enc / sf (only used when sf != 0).
+// Per-element multiplier S_enc / sf (only used when sf != 0).  An infinite
+// quotient clamps to FLT_MAX, as the tensor scale does: it overflows only
+// when S_enc is already clamped and sf is a small subnormal E4M3 value, and
+// the clamp keeps 0 * multiplier at 0 instead of NaN.
 __device__ __forceinline__ float element_ratio(float s_enc, uint32_t sf) {
-    return __fdiv_rn(s_enc, e4m3_to_float(sf));
+    const float r = __fdiv_rn(s_enc, e4m3_to_float(sf));
+    return isinf(r) ? 3.402823466e38f : r;
 }
 
 // Eight E2M1 codes (round to nearest even, saturating at 6, sign copied)

@@ -795,9 +795,8 @@ __global__ void __launch_bounds__(256) k_quant1d_mse(const uint16_t* __restrict_
     const float s_enc = tensor_encode_scale(amax[0]);
     const float dec = tensor_decode_scale(amax[0]);
     if (threadIdx.x >= 1 && threadIdx.x <= 126) {
-        const float e = e4m3_to_float(threadIdx.x);
-        s_ratio[threadIdx.x] = __fdiv_rn(s_enc, e);
-        s_step[threadIdx.x] = __fmul_rn(e, dec);
+        s_ratio[threadIdx.x] = element_ratio(s_enc, threadIdx.x);
+        s_step[threadIdx.x] = __fmul_rn(e4m3_to_float(threadIdx.x), dec);
     }
     if (amax_copy != nullptr && blockIdx.x == 0 && threadIdx.x == 0) amax_copy[0] = amax[0];
     __syncthreads();
@@ -916,14 +915,36 @@ __global__ void __launch_bounds__(256) k_quant2d_pad(uint8_t* __restrict__ sf, u
 }
 
 // ------------------------------------------------------------------ RHT
+// Two lanes of the butterfly at once: (a0, a1) += (b0, b1) and (b0, b1) =
+// old (a0, a1) - (b0, b1), each lane rounded once (add/sub.rn.f32x2, the same
+// IEEE operation as __fadd_rn / __fsub_rn, subnormals kept).
+__device__ __forceinline__ void addsub2(float& a0, float& a1, float& b0, float& b1) {
+    asm("{\n\t.reg .b64 a, b, s, d;\n\t"
+        "mov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\t"
+        "add.rn.f32x2 s, a, b;\n\tsub.rn.f32x2 d, a, b;\n\t"
+        "mov.b64 {%0, %1}, s;\n\tmov.b64 {%2, %3}, d;\n\t}"
+        : "+f"(a0), "+f"(a1), "+f"(b0), "+f"(b1));
+}
+
+// (a0, a1) *= c, each lane rounded once (mul.rn.f32x2).
+__device__ __forceinline__ void mul2(float& a0, float& a1, float c) {
+    asm("{\n\t.reg .b64 a, k;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 k, {%2, %2};\n\t"
+        "mul.rn.f32x2 a, a, k;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(c));
+}
+
 // y = 0.25 * H16 * (s .* x) on one 16-token chunk, FP32 butterfly with
-// strides 1, 2, 4, 8 (Sylvester order).  FOLD puts the signs into the first
-// stage: s_i x_i is an exact multiply by +-1 and s_j x_j + (s_i x_i) one fused
-// multiply-add by +-1, which rounds once like the plain add or subtract, so
-// both forms give the same bits.  Measured on Ultra dY, the folded form makes
-// the amax and RNE passes up to 9 % faster and the SR encoders 1 % slower, so
-// those keep the separate sign flips.
-template <bool FOLD>
+// strides 1, 2, 4, 8 (Sylvester order); strides 2, 4 and 8 and the factor
+// 1/4 run on pairs of lanes (packed f32x2 operations).  FOLD puts the signs
+// into the first stage: s_i x_i is an exact multiply by +-1 and
+// s_j x_j + (s_i x_i) one fused multiply-add by +-1, which rounds once like
+// the plain add or subtract, so both forms give the same bits.  Measured on
+// Ultra dY, the folded form makes the amax and RNE passes up to 9 % faster and
+// the SR encoders 1 % slower, so those keep the separate sign flips.  SCALE
+// false leaves out the factor 1/4 (for maxima: max RN(|y_i| / 4) =
+// RN(max |y_i| / 4), rounding being monotone, so it is applied once to the max).
+template <bool FOLD, bool SCALE = true>
 __device__ __forceinline__ void rht16(float (&x)[16], uint32_t sign_mask) {
     if (FOLD) {
 #pragma unroll
@@ -948,14 +969,12 @@ __device__ __forceinline__ void rht16(float (&x)[16], uint32_t sign_mask) {
 #pragma unroll
     for (int h = 2; h < 16; h <<= 1)
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if ((i & h) == 0) {
-                const float a = x[i], c = x[i + h];
-                x[i] = __fadd_rn(a, c);
-                x[i + h] = __fsub_rn(a, c);
-            }
+        for (int i = 0; i < 16; i += 2)
+            if ((i & h) == 0) addsub2(x[i], x[i + 1], x[i + h], x[i + h + 1]);
+    if (SCALE) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = __fmul_rn(x[i], 0.25f);
+        for (int i = 0; i < 16; i += 2) mul2(x[i], x[i + 1], 0.25f);
+    }
 }
 
 // CTA = 64 tokens x 256 channels, 256 threads.  The tile is staged in
@@ -1209,11 +1228,12 @@ __global__ void __launch_bounds__(256) k_rht(const uint16_t* __restrict__ x, int
 #pragma unroll
                     for (int i = 0; i < 16; ++i) mp = fmaxf(mp, fabsf(v[i]));
                 }
-                rht16<MODE != 2 && MODE != 4>(v, sign_mask);
+                rht16<MODE != 2 && MODE != 4, false>(v, sign_mask);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
             }
         }
+        m = __fmul_rn(m, 0.25f);                // the transform's factor 1/4, once
         block_max_atomic(__float_as_uint(m), amax + g);
         if (MODE == 3) {
             __syncthreads();                    // the reduction buffer is shared by both calls
@@ -1312,7 +1332,7 @@ __global__ void __launch_bounds__(256, 3) k_rht_stream(const uint16_t* __restric
 #pragma unroll
                         for (int i = 0; i < 16; ++i) mp = fmaxf(mp, fabsf(v[i]));
                     }
-                    rht16<true>(v, sign_mask);
+                    rht16<true, false>(v, sign_mask);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
                 }
@@ -1324,6 +1344,7 @@ __global__ void __launch_bounds__(256, 3) k_rht_stream(const uint16_t* __restric
         __syncthreads();                              // buffer b is refilled two iterations on
     }
     if (MODE == 0 || MODE == 3) {
+        m = __fmul_rn(m, 0.25f);                      // the transform's factor 1/4, once
         block_max_atomic(__float_as_uint(m), amax);
         if (MODE == 3) {
             __syncthreads();                          // the reduction buffer is shared by both calls

@@ -334,8 +334,30 @@ def test_dual_sr_quantize_strided_rows(B, orc, tokens, cols):
     _dual_sr_case(B, orc, tokens, cols, 4)
 
 
-def _dual_sr_case(B, orc, tokens, cols, pad):
-    x = _x(tokens, cols, seed=7 * tokens + cols, scale=1e-3, spread=6.0)
+@pytest.mark.parametrize("tokens,cols", [(80, 272), (1040, 528)])
+def test_rht_paths_in_the_subnormal_range(B, orc, tokens, cols):
+    """Inputs near the bottom of the FP32 range (|x| ~ 1e-38, some of them
+    bf16 subnormals): the transform's sums and its factor 1/4 produce FP32
+    subnormals, which every RHT path (amax, both amaxes, RNE, SR, the dual
+    encoder) must round exactly as the oracle's FP32 arithmetic does."""
+    x = _x(tokens, cols, seed=5 * tokens + cols, scale=2e-38, spread=3.0)
+    assert (x.float().abs() < 1.1754944e-38).any()
+    mask = 0x6A39
+    a = B.dual_amax(x.cuda(), mask)
+    r = B.rht_amax(x.cuda(), mask)
+    torch.cuda.synchronize()
+    got = np_u8(a)
+    assert got[0] == np.float32(orc.amax(x)) and got[1] == np.float32(orc.rht_amax(x, mask))
+    assert np_u8(r)[0] == got[1]
+    for mode in (0, 1):
+        q = B.rht_quantize(x.cuda(), mask, mode=mode, seed=99)
+        torch.cuda.synchronize()
+        _same(q, orc.rht_quantize(x, mask, mode=mode, seed=99), cols, tokens)
+    _dual_sr_case(B, orc, tokens, cols, 0, scale=2e-38, spread=3.0)
+
+
+def _dual_sr_case(B, orc, tokens, cols, pad, scale=1e-3, spread=6.0):
+    x = _x(tokens, cols, seed=7 * tokens + cols, scale=scale, spread=spread)
     mask, s_row, s_rht = 0x2D96, 7, 7 ^ 0x9E3779B97F4A7C15
     xd = x.cuda()
     if pad:
