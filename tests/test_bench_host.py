@@ -181,3 +181,57 @@ def test_gpus_n_starts_n_ranks():
 
 if __name__ == "__main__":
     sys.exit(pytest.main([__file__, "-q"]))
+
+
+# Kernels of the Ultra step's launch list (profiles/launches_ultra_full_step.md)
+# and the ncu summaries that cover them, with the sources each summary's
+# kernel_code_sha256 is taken over.
+_Q = "nvfp4_precision_02_b300/csrc/"
+STEP_KERNEL_SUMMARIES = {
+    "k_gemm_nvfp4<bf16, TMA store, pair, groups along M>": ["k_gemm_nvfp4_grouped_up_super.md",
+                                                            "k_gemm_nvfp4_grouped_down_super.md"],
+    "k_gemm_nvfp4<bf16, TMA store, pair, dense>": ["k_gemm_nvfp4_fprop_ultra.md", "k_gemm_nvfp4_dgrad_ultra.md"],
+    "k_gemm_nvfp4<fp32, TMA store, pair, dense>": ["k_gemm_nvfp4_wgrad_ultra.md"],
+    "k_quant2d_w<2>": ["k_quant2d_w_moe_super.md"],
+    "k_amax": ["k_amax_ultra.md"],
+    "k_quant1d<RNE, grouped, band>": ["k_quant1d_grouped_h_ultra.md"],
+    "k_rht<4>": ["k_rht_dual_sr_ultra.md"],
+    "k_amax_grouped": ["k_amax_grouped_super.md"],
+    "k_rht_stream<3>": ["k_rht_stream_dual_amax_ultra.md"],
+    "k_quant2d": ["k_quant2d_ultra.md"],
+    "k_rht_stream<1>": ["k_rht_stream_rne_ultra.md"],
+    "k_quant1d<RNE>": ["k_quant1d_rne_ultra.md"],
+    "k_rht_stream<0>": ["k_rht_stream_amax_ultra.md"],
+}
+
+
+def _summary_sources(name):
+    if name.startswith("k_gemm"):
+        return bench.GEMM_SOURCES
+    if name.startswith("k_quant2d_w"):
+        return (_Q + "quant2d_w.cuh",) + bench.QUANT_SOURCES
+    if name.startswith("k_quant2d_resident"):
+        return (_Q + "quant2d_resident.cuh",) + bench.QUANT_SOURCES
+    return bench.QUANT_SOURCES
+
+
+def test_every_step_kernel_has_an_ncu_summary():
+    """Each kernel in the step's launch list has a committed ncu summary with
+    its DRAM bytes and code hash; a summary whose hash no longer matches its
+    sources is reported (the kernel changed after the capture)."""
+    import re
+    import warnings
+    with open(os.path.join(ROOT, "profiles", "launches_ultra_full_step.md")) as f:
+        text = f.read()
+    labels = [m.group(1).strip() for m in re.finditer(r"^\| (k_[^|(]+?)\s*(?:\([^|]*\))? \| \d+ \|", text, re.M)]
+    assert labels, "no kernel rows in the launch list"
+    for lab in labels:
+        assert lab in STEP_KERNEL_SUMMARIES, f"launch-list kernel without a summary: {lab}"
+        for name in STEP_KERNEL_SUMMARIES[lab]:
+            with open(os.path.join(ROOT, "profiles", name)) as f:
+                body = f.read()
+            assert re.search(r"dram_bytes_per_launch:\s*\d+", body), name
+            h = re.search(r"kernel_code_sha256:\s*([0-9a-f]{64})", body)
+            assert h, name
+            if h.group(1) != bench.source_hash(_summary_sources(name)):
+                warnings.warn(f"{name}: kernel code changed since the capture")
